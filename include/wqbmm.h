@@ -1,0 +1,151 @@
+/*
+ * wqbmm — A16W4 per-group pseudo-quantized matmul by MSD (multi-step decomposition) on GB300 (sm_103a).
+ *
+ * The operation (WeightQuantBatchMatmulExperiment page, section 4.1, eleven steps; spec in section 4.2):
+ *   inputs   x fp16 [M, K] row-major; w signed int4 [K, N]; antiquant_scale fp16 [K/G, N] row-major
+ *   output   y fp16 [M, N] row-major
+ *   for each row m and each K-group g of G consecutive k:
+ *     A_max = max |x[m, k]| over the group
+ *     tmp1 = 7.49 * x / A_max,       A1 = round(tmp1)
+ *     tmp2 = (tmp1 - A1) * 14.98,    A2 = round(tmp2)
+ *     tmp3 = (tmp2 - A2) * 14.98,    A3 = round(tmp3)        (each A_i in [-7, 7])
+ *     Y_i[m, n] = sum over the group's k of A_i[m, k] * w[k, n]            (exact integers)
+ *     Y_group = (Y1/7.49 + Y2/(7.49*14.98) + Y3/(7.49*14.98^2)) * A_max * antiquant_scale[g, n]
+ *   y[m, n] = sum over the groups of Y_group, rounded once to fp16 (nearest-even).
+ * The unfold runs in IEEE binary32 with the constants 7.49f and 14.98f, every operation rounded on its own and the
+ * division correctly rounded; "round" is half-to-even. A group whose A_max is 0 contributes 0.
+ *
+ * Weight format: the caller's int4 weights are packed two per byte along K (page section 4.3): uint8 [K/2, N], byte
+ * (kk, n) holds w[2kk, n] in its low nibble and w[2kk+1, n] in its high nibble, two's complement. Before the first
+ * run the weights are re-laid once (wqbmm_prepack_weight) into the library's tile layout, the way a size query plus
+ * an ND-to-tiled transform precede a quantized matmul on the page "aclnnCalculateMatmulWeightSizeV2 接口详解"
+ * (sections on the function prototype and on its cooperation with aclnnTransMatmulWeight).
+ *
+ * Conventions for every entry point:
+ *   - All pointers are caller-owned. Pointers marked "device" must be device memory of the current CUDA device;
+ *     the library allocates nothing and keeps no state beyond cached device attributes and the device status word.
+ *   - Work is enqueued asynchronously on `stream` (0 = the legacy default stream); the library never synchronizes,
+ *     except wqbmm_read_device_status, which waits for `stream`.
+ *   - Arguments are validated before anything is enqueued. On any error nothing is launched and outputs are
+ *     untouched. Validation of sizes and pointers needs no GPU; the architecture check needs the current device to
+ *     be compute capability 10.3.
+ *   - Status codes follow the pattern of the page "aclnnCalculateMatmulWeightSizeV2 接口详解", section on return
+ *     values (null pointer, invalid parameter and runtime/platform errors are distinct codes).
+ */
+#ifndef WQBMM_H
+#define WQBMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define WQBMM_API __attribute__((visibility("default")))
+#else
+#define WQBMM_API
+#endif
+
+/* Same type as cudaStream_t, without requiring the CUDA headers. */
+typedef struct CUstream_st *wqbmm_stream_t;
+
+typedef enum {
+    WQBMM_OK = 0,
+    WQBMM_ERR_NULLPTR = 1,            /* a required pointer argument is null */
+    WQBMM_ERR_INVALID = 2,            /* a size, alignment or workspace-size rule below is broken */
+    WQBMM_ERR_UNSUPPORTED_ARCH = 3,   /* the current device is not compute capability 10.3 (GB300) */
+    WQBMM_ERR_CUDA = 4,               /* a CUDA runtime call failed (no device, launch failure, ...) */
+    WQBMM_ERR_DEVICE_TIMEOUT = 5      /* a kernel gave up a bounded wait (read by wqbmm_read_device_status) */
+} wqbmm_status;
+
+/* Shape rules shared by the entry points that take (M, K, N, G):
+ *   1 <= M, K, N <= 2^31 - 1;  G in {32, 64, 128};  K % G == 0;  N % 8 == 0;  M * N, M * K < 2^62.
+ * Alignment rules: x, antiquant_scale, y, the prepacked weights and the workspace start on 16-byte boundaries. */
+
+/*
+ * Size in bytes of the prepacked weight buffer for a K x N int4 weight. Host only; no GPU needed.
+ * Layout (for reference; callers treat it as opaque): tiles of 128 output columns x 128 k, tile (nt, kb) at byte
+ * offset (nt * ceil(K/128) + kb) * 8192; inside a tile, row r (column n = 128 nt + r) holds 64 bytes with k = 128 kb
+ * + 2j in the low nibble and k + 1 in the high nibble of byte j, each stored as w + 8 (offset binary, 0..15); padding
+ * holds w = 0. Total = ceil(N/128) * ceil(K/128) * 8192 bytes.
+ * Errors: WQBMM_ERR_NULLPTR if bytes is null; WQBMM_ERR_INVALID if the shape rules fail.
+ */
+WQBMM_API wqbmm_status wqbmm_prepacked_weight_bytes(int64_t K, int64_t N, int64_t G, size_t *bytes);
+
+/*
+ * Re-lays packed int4 weights into the prepacked tile layout (one kernel launch on `stream`).
+ *   w_packed     device, uint8 [K/2, N] as described above (read only)
+ *   w_prepacked  device, wqbmm_prepacked_weight_bytes(K, N, G) bytes (written)
+ * The two buffers must not overlap. Errors: NULLPTR, INVALID (shape or alignment), UNSUPPORTED_ARCH, CUDA.
+ */
+WQBMM_API wqbmm_status wqbmm_prepack_weight(const uint8_t *w_packed, void *w_prepacked, int64_t K, int64_t N,
+                                            int64_t G, wqbmm_stream_t stream);
+
+/*
+ * Workspace bytes wqbmm_run needs for this shape on any GB300 (0 when the shape needs none). Host only.
+ * The workspace holds split-K partial sums and per-tile arrival counters. It must be zero-filled once before its
+ * first use; every successful run leaves the counters at zero again, so the same workspace can be reused by later
+ * runs on the same stream without clearing. Runs that execute concurrently must use different workspaces.
+ * Errors: NULLPTR if bytes is null; INVALID if the shape rules fail.
+ */
+WQBMM_API wqbmm_status wqbmm_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t G, size_t *bytes);
+
+/*
+ * y = MSD matmul of x with the prepacked weights and antiquant_scale (the eleven steps above), on `stream`.
+ *   x                device, fp16 [M, K] row-major
+ *   w_prepacked      device, output of wqbmm_prepack_weight for the same K, N, G
+ *   antiquant_scale  device, fp16 [K/G, N] row-major
+ *   y                device, fp16 [M, N] row-major (written; must not overlap the inputs or the workspace)
+ *   workspace        device, at least wqbmm_workspace_bytes(M, K, N, G) bytes (may be null when that is 0)
+ * The result is deterministic: split-K partial sums are reduced in a fixed order.
+ * Errors: NULLPTR, INVALID (shape, alignment, workspace too small), UNSUPPORTED_ARCH, CUDA (launch failure).
+ * A kernel that gives up a bounded internal wait records WQBMM_ERR_DEVICE_TIMEOUT in the device status word.
+ */
+WQBMM_API wqbmm_status wqbmm_run(const void *x, const void *w_prepacked, const void *antiquant_scale, void *y,
+                                 int64_t M, int64_t K, int64_t N, int64_t G, void *workspace,
+                                 size_t workspace_bytes, wqbmm_stream_t stream);
+
+/*
+ * Exposes steps 1-8 exactly as the run kernel computes them (for bit-exact checks).
+ *   x       device, fp16 [M, K]
+ *   planes  device, int8 [3, M, K]: plane i of row m at planes[(i * M + m) * K + k], values in [-7, 7]
+ *   amax    device, float [M, K/G]: A_max of each row and group
+ * Shape rules as above with N ignored. Errors: NULLPTR, INVALID, UNSUPPORTED_ARCH, CUDA.
+ */
+WQBMM_API wqbmm_status wqbmm_debug_unfold(const void *x, int64_t M, int64_t K, int64_t G, int8_t *planes,
+                                          float *amax, wqbmm_stream_t stream);
+
+/*
+ * Exposes step 9 for one group g as the run kernel's tensor-core path computes it (for bit-exact checks).
+ *   y123  device, int32 [3, M, N]: Y_i[m, n] of group g at y123[(i * M + m) * N + n]
+ * 0 <= g < K/G. Errors: NULLPTR, INVALID, UNSUPPORTED_ARCH, CUDA.
+ */
+WQBMM_API wqbmm_status wqbmm_debug_group_partials(const void *x, const void *w_prepacked, int64_t M, int64_t K,
+                                                  int64_t N, int64_t G, int64_t g, int32_t *y123,
+                                                  wqbmm_stream_t stream);
+
+/*
+ * Reads (and, if clear != 0, resets) the current device's status word after waiting for `stream`.
+ * *code is 0 when no kernel of this library has recorded an error; otherwise it is WQBMM_ERR_DEVICE_TIMEOUT in the
+ * low 8 bits and the site of the wait that gave up in bits 8-15.
+ * Errors: NULLPTR, CUDA.
+ */
+WQBMM_API wqbmm_status wqbmm_read_device_status(int32_t *code, int clear, wqbmm_stream_t stream);
+
+/*
+ * Runs one kernel that waits on a barrier nothing will complete, with the given limit in nanoseconds
+ * (1e6 <= limit_ns <= 2e9). The kernel gives up, records WQBMM_ERR_DEVICE_TIMEOUT in the status word and returns, so
+ * the bounded-wait error path can be checked without a hang. Errors: INVALID, UNSUPPORTED_ARCH, CUDA.
+ */
+WQBMM_API wqbmm_status wqbmm_debug_wait_timeout(int64_t limit_ns, wqbmm_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+WQBMM_API const char *wqbmm_status_string(wqbmm_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WQBMM_H */

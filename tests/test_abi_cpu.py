@@ -1,0 +1,132 @@
+"""The C-ABI library builds for sm_103a, loads, exports every entry point include/wqbmm.h declares, and rejects bad
+arguments before touching a device (status codes in the manner of the page "aclnnCalculateMatmulWeightSizeV2
+接口详解", section on return values: null pointers, invalid parameters and platform errors are distinct codes).
+None of these tests launches a kernel.
+"""
+import os
+import re
+import subprocess
+
+import pytest
+
+import weight_quantized_matmul_gb300 as wq
+from weight_quantized_matmul_gb300 import build as wqbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "wqbmm.h")
+A = 0x10000          # a 16-byte aligned fake device address: validation must reject before any use of it
+MIS = 0x10008        # 8-byte aligned only
+
+
+@pytest.fixture(scope="module")
+def lib():
+    wqbuild.build()
+    return wq.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^WQBMM_API\s+(?:const\s+)?\w+\s*\*?\s*(wqbmm_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert declared_functions() == sorted(wq.SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", wq.library_path()], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\b(wqbmm_\w+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+    # nothing but the C ABI leaks out of the library
+    assert all(s.startswith("wqbmm_") for s in exported)
+
+
+def test_build_targets_sm_103a_only():
+    flags = " ".join(wqbuild.NVCC_FLAGS)
+    assert flags.count("-gencode") == 1 and "arch=compute_103a,code=sm_103a" in flags
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert wq.wqbmm_status_string(code).startswith("WQBMM_")
+    assert "UNKNOWN" in wq.wqbmm_status_string(99)
+
+
+def test_prepacked_weight_bytes():
+    assert wq.wqbmm_prepacked_weight_bytes(4096, 4096, 128) == 4096 * 4096 // 2
+    assert wq.wqbmm_prepacked_weight_bytes(96, 1000, 32) == 8 * 1 * 8192     # padded to 128 x 128 tiles
+    assert wq.wqbmm_prepacked_weight_bytes(8192, 28672, 64) == 8192 * 28672 // 2
+
+
+def test_workspace_bytes():
+    # decode: 32 column tiles split over K (sized for up to 160 SMs, two CTAs each: 10 slices)
+    assert wq.wqbmm_workspace_bytes(1, 4096, 4096, 128) == 10 * 4096 * 4 + 256
+    # enough tiles to fill the GPU: no split, no workspace
+    assert wq.wqbmm_workspace_bytes(2048, 8192, 28672, 64) == 0
+    assert wq.wqbmm_workspace_bytes(128, 5120, 13824, 128) == 0
+
+
+# (entry, args, expected status) — table-driven error paths
+NULLPTR, INVALID = wq.ERR_NULLPTR, wq.ERR_INVALID
+CASES = [
+    ("size_null", lambda L: L.wqbmm_prepacked_weight_bytes(128, 128, 128, None), NULLPTR),
+    ("size_bad_group", lambda L: L.wqbmm_prepacked_weight_bytes(128, 128, 48, _sz()), INVALID),
+    ("size_k_not_multiple_of_group", lambda L: L.wqbmm_prepacked_weight_bytes(96, 128, 64, _sz()), INVALID),
+    ("size_n_not_multiple_of_8", lambda L: L.wqbmm_prepacked_weight_bytes(128, 12, 128, _sz()), INVALID),
+    ("size_zero_k", lambda L: L.wqbmm_prepacked_weight_bytes(0, 128, 128, _sz()), INVALID),
+    ("size_negative_n", lambda L: L.wqbmm_prepacked_weight_bytes(128, -8, 128, _sz()), INVALID),
+    ("size_k_too_large", lambda L: L.wqbmm_prepacked_weight_bytes(1 << 31, 8, 128, _sz()), INVALID),
+    ("ws_null", lambda L: L.wqbmm_workspace_bytes(1, 128, 128, 128, None), NULLPTR),
+    ("ws_zero_m", lambda L: L.wqbmm_workspace_bytes(0, 128, 128, 128, _sz()), INVALID),
+    ("prepack_null_src", lambda L: L.wqbmm_prepack_weight(None, A, 128, 128, 128, None), NULLPTR),
+    ("prepack_null_dst", lambda L: L.wqbmm_prepack_weight(A, None, 128, 128, 128, None), NULLPTR),
+    ("prepack_misaligned_dst", lambda L: L.wqbmm_prepack_weight(A, MIS, 128, 128, 128, None), INVALID),
+    ("prepack_bad_group", lambda L: L.wqbmm_prepack_weight(A, A, 128, 128, 16, None), INVALID),
+    ("run_null_x", lambda L: L.wqbmm_run(None, A, A, A, 1, 128, 128, 128, A, 1 << 20, None), NULLPTR),
+    ("run_null_w", lambda L: L.wqbmm_run(A, None, A, A, 1, 128, 128, 128, A, 1 << 20, None), NULLPTR),
+    ("run_null_scale", lambda L: L.wqbmm_run(A, A, None, A, 1, 128, 128, 128, A, 1 << 20, None), NULLPTR),
+    ("run_null_y", lambda L: L.wqbmm_run(A, A, A, None, 1, 128, 128, 128, A, 1 << 20, None), NULLPTR),
+    ("run_null_workspace_needed", lambda L: L.wqbmm_run(A, A, A, A, 1, 4096, 4096, 128, None, 0, None), NULLPTR),
+    ("run_zero_m", lambda L: L.wqbmm_run(A, A, A, A, 0, 128, 128, 128, A, 1 << 20, None), INVALID),
+    ("run_negative_k", lambda L: L.wqbmm_run(A, A, A, A, 1, -128, 128, 128, A, 1 << 20, None), INVALID),
+    ("run_k_not_multiple_of_group", lambda L: L.wqbmm_run(A, A, A, A, 1, 160, 128, 128, A, 1 << 20, None),
+     INVALID),
+    ("run_group_not_supported", lambda L: L.wqbmm_run(A, A, A, A, 1, 256, 128, 256, A, 1 << 20, None), INVALID),
+    ("run_n_ragged_by_4", lambda L: L.wqbmm_run(A, A, A, A, 1, 128, 132, 128, A, 1 << 20, None), INVALID),
+    ("run_m_too_large", lambda L: L.wqbmm_run(A, A, A, A, 1 << 31, 128, 128, 128, A, 1 << 20, None), INVALID),
+    ("run_misaligned_x", lambda L: L.wqbmm_run(MIS, A, A, A, 1, 128, 128, 128, A, 1 << 20, None), INVALID),
+    ("run_misaligned_y", lambda L: L.wqbmm_run(A, A, A, MIS, 1, 128, 128, 128, A, 1 << 20, None), INVALID),
+    ("run_misaligned_scale", lambda L: L.wqbmm_run(A, A, MIS, A, 1, 128, 128, 128, A, 1 << 20, None), INVALID),
+    ("run_misaligned_weights", lambda L: L.wqbmm_run(A, MIS, A, A, 1, 128, 128, 128, A, 1 << 20, None), INVALID),
+    ("run_misaligned_workspace", lambda L: L.wqbmm_run(A, A, A, A, 1, 4096, 4096, 128, MIS, 1 << 20, None),
+     INVALID),
+    ("unfold_null_planes", lambda L: L.wqbmm_debug_unfold(A, 1, 128, 128, None, A, None), NULLPTR),
+    ("unfold_bad_group", lambda L: L.wqbmm_debug_unfold(A, 1, 128, 100, A, A, None), INVALID),
+    ("partials_group_out_of_range", lambda L: L.wqbmm_debug_group_partials(A, A, 1, 256, 128, 128, 2, A, None),
+     INVALID),
+    ("partials_negative_group", lambda L: L.wqbmm_debug_group_partials(A, A, 1, 256, 128, 128, -1, A, None),
+     INVALID),
+    ("status_null", lambda L: L.wqbmm_read_device_status(None, 0, None), NULLPTR),
+    ("timeout_limit_too_small", lambda L: L.wqbmm_debug_wait_timeout(10, None), INVALID),
+    ("timeout_limit_too_large", lambda L: L.wqbmm_debug_wait_timeout(10 ** 10, None), INVALID),
+]
+
+
+def _sz():
+    import ctypes
+    return ctypes.byref(ctypes.c_size_t(0))
+
+
+@pytest.mark.parametrize("name,call,want", CASES, ids=[c[0] for c in CASES])
+def test_rejected_before_any_device_work(lib, name, call, want):
+    assert call(lib) == want
+
+
+def test_no_device_is_a_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    # valid arguments, but no GPU: the device check fails with a CUDA error and nothing is launched
+    assert lib.wqbmm_run(A, A, A, A, 2048, 8192, 28672, 64, None, 0, None) == wq.ERR_CUDA

@@ -1,0 +1,286 @@
+"""Parity of the CUDA path with the CPU oracle, through the C ABI, on a GB300.
+
+Bars (method: WeightQuantBatchMatmulExperiment page, section 4.1):
+  - prepacked weights: byte-exact against the documented tile layout;
+  - steps 1-8 (A_max and the three planes, wqbmm_debug_unfold): bit-exact against the oracle's binary32 unfold;
+  - step 9 (per-group integer Y1..Y3 from the tensor-core path, wqbmm_debug_group_partials): bit-exact;
+  - steps 1-11 (wqbmm_run, fp16 y): |y - y_ref| <= 2e-3 * max|y_ref| + 1 fp16 ulp(y_ref) against the oracle in
+    binary64 (and in binary32 unfold), element by element; at full workload sizes on seeded sampled rows.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import weight_quantized_matmul_gb300 as wq
+from weight_quantized_matmul_gb300 import build as wqbuild
+from weight_quantized_matmul_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def fp16_ulp(v):
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -14)))
+    return 2.0 ** (e - 10)
+
+
+def assert_within_tolerance(got, ref, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    tol = 2e-3 * np.abs(ref).max() + fp16_ulp(ref)
+    err = np.abs(got - ref)
+    bad = err > tol
+    assert not bad.any(), (f"{what}: {int(bad.sum())}/{bad.size} outside tolerance, max err {err.max():.4g}, "
+                           f"max |ref| {np.abs(ref).max():.4g}, first bad {np.argwhere(bad)[:3].tolist()}")
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    wqbuild.build()
+    torch.cuda.set_device(0)
+    wq.wqbmm_read_device_status(clear=True)
+    return torch.device("cuda:0")
+
+
+@pytest.fixture(autouse=True)
+def device_status_clean(dev):
+    yield
+    torch.cuda.synchronize()
+    assert wq.wqbmm_read_device_status() == 0
+
+
+def to_dev(a, dev):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def gpu_run(x, wp, sc, G, dev, M=None):
+    M, K = x.shape
+    N = sc.shape[1]
+    xd, wd, sd = to_dev(x, dev), to_dev(wp, dev), to_dev(sc, dev)
+    w_pre = wq.prepack_weight(wd, K, N, G)
+    y = wq.msd_matmul(xd, w_pre, sd, G)
+    return y.cpu().numpy()
+
+
+def prepack_layout(wp, K, N):
+    """The tile layout documented for wqbmm_prepacked_weight_bytes, restated with numpy."""
+    nt, kb = -(-N // 128), -(-K // 128)
+    padded = np.zeros((kb * 64, nt * 128), dtype=np.uint8)
+    padded[:K // 2, :N] = wp
+    padded ^= 0x88
+    return padded.reshape(kb, 64, nt, 128).transpose(2, 0, 3, 1).reshape(-1)
+
+
+# ------------------------------------------------------------------------------------------- prepack
+
+@pytest.mark.parametrize("K,N,G", [(128, 128, 128), (4096, 4096, 128), (96, 1000, 32), (640, 264, 64)])
+def test_prepack_matches_documented_layout(dev, K, N, G):
+    wp = I.make_w_packed(I.small_case(1, K, N, G, seed=K + N))
+    got = wq.prepack_weight(to_dev(wp, dev), K, N, G).cpu().numpy()
+    np.testing.assert_array_equal(got, prepack_layout(wp, K, N))
+
+
+# ------------------------------------------------------------------------------------------- steps 1-8
+
+def special_x():
+    """Rows that stress the unfold: ties in binary32, zero groups, subnormals, the fp16 extremes, -0."""
+    rows = []
+    r = np.zeros(128, dtype=np.float16)
+    r[0], r[1] = 0.53125, 0.03857421875                # binary32 tie tmp3 = 2.5 (half-even -> 2)
+    r[32], r[33] = 0.52294921875, 0.04107666015625     # tie tmp3 = -2.5
+    rows.append(r)
+    rows.append(np.zeros(128, dtype=np.float16))                       # all-zero groups
+    r = np.full(128, -0.0, dtype=np.float16)
+    r[5] = 5.960464477539063e-08                                       # smallest subnormal
+    r[70] = -6.103515625e-05
+    rows.append(r)
+    r = I.fp16(np.linspace(-65504, 65504, 128))
+    rows.append(r)
+    allv = np.arange(65536, dtype=np.uint32).astype(np.uint16).view(np.float16)
+    fin = allv[np.isfinite(allv)]
+    rng = fin[(I.raw_u64(99, 1, 0, 128 * 8) % np.uint64(fin.size)).astype(np.int64)].reshape(8, 128)
+    rows.extend(list(rng))
+    return np.stack(rows).astype(np.float16)
+
+
+@pytest.mark.parametrize("G", [32, 64, 128])
+@pytest.mark.parametrize("dist", ["normal", "t3_clip60", "normal_cols20", "uniform3"])
+def test_unfold_bit_exact(dev, G, dist):
+    x = I.make_x(I.small_case(37, 1024, 8, G, seed=G, x_dist=dist, x_sigma=3.0 if dist == "uniform3" else 1.0))
+    M, K = x.shape
+    planes = torch.empty((3, M, K), dtype=torch.int8, device=dev)
+    amax = torch.empty((M, K // G), dtype=torch.float32, device=dev)
+    wq.wqbmm_debug_unfold(to_dev(x, dev), M, K, G, planes, amax)
+    p_ref, a_ref = oracle.unfold(x, G, oracle.MODE_F)
+    np.testing.assert_array_equal(planes.cpu().numpy(), p_ref)
+    np.testing.assert_array_equal(amax.cpu().numpy(), a_ref.astype(np.float32))
+
+
+@pytest.mark.parametrize("G", [32, 64, 128])
+def test_unfold_bit_exact_special_values(dev, G):
+    x = special_x()
+    M, K = x.shape
+    planes = torch.empty((3, M, K), dtype=torch.int8, device=dev)
+    amax = torch.empty((M, K // G), dtype=torch.float32, device=dev)
+    wq.wqbmm_debug_unfold(to_dev(x, dev), M, K, G, planes, amax)
+    p_ref, a_ref = oracle.unfold(x, G, oracle.MODE_F)
+    np.testing.assert_array_equal(planes.cpu().numpy(), p_ref)
+    np.testing.assert_array_equal(amax.cpu().numpy(), a_ref.astype(np.float32))
+
+
+# ------------------------------------------------------------------------------------------- step 9
+
+PARTIAL_CASES = [
+    # M, K, N, G, groups to check, x dist, w dist
+    (1, 256, 128, 128, [0, 1], "normal", "u8"),
+    (3, 512, 264, 64, [0, 5, 7], "t3_clip60", "u8"),
+    (5, 96, 1000, 32, [0, 2], "normal", "u8"),
+    (8, 1024, 384, 128, [3], "normal_cols20", "pm1_mix"),
+    (16, 640, 136, 64, [9], "uniform3", "u7"),
+    (17, 384, 256, 128, [2], "normal", "u8"),
+    (40, 256, 128, 32, [0, 7], "normal", "u8"),
+]
+
+
+@pytest.mark.parametrize("M,K,N,G,groups,xd,wd", PARTIAL_CASES)
+def test_group_partials_bit_exact(dev, M, K, N, G, groups, xd, wd):
+    x, wp, _ = I.make_inputs(I.small_case(M, K, N, G, seed=M * 7 + K, x_dist=xd, w_dist=wd))
+    w_pre = wq.prepack_weight(to_dev(wp, dev), K, N, G)
+    xdv = to_dev(x, dev)
+    for g in groups:
+        y123 = torch.full((3, M, N), -12345, dtype=torch.int32, device=dev)
+        wq.wqbmm_debug_group_partials(xdv, w_pre, M, K, N, G, g, y123)
+        np.testing.assert_array_equal(y123.cpu().numpy(), oracle.group_partials(x, wp, N, G, g, oracle.MODE_F),
+                                      err_msg=f"group {g}")
+
+
+@pytest.mark.parametrize("wval", [7, -8, 1, -1])
+def test_group_partials_exact_at_extreme_magnitudes(dev, wval):
+    """x constant per group gives planes (7, 7, 5) everywhere; with constant weights the integer sums reach the
+    largest magnitudes the format allows (|Y| up to 7 * 8 * G), where inexact FP32 accumulation would show."""
+    M, K, N, G = 4, 256, 128, 128
+    x = np.ones((M, K), dtype=np.float16)
+    x[1] = -2.0
+    x[2, :128] = 0.25
+    w = np.full((K, N), wval, dtype=np.int8)
+    wp = I.pack_int4_along_k(w)
+    w_pre = wq.prepack_weight(to_dev(wp, dev), K, N, G)
+    for g in range(2):
+        y123 = torch.zeros((3, M, N), dtype=torch.int32, device=dev)
+        wq.wqbmm_debug_group_partials(to_dev(x, dev), w_pre, M, K, N, G, g, y123)
+        ref = oracle.group_partials(x, wp, N, G, g, oracle.MODE_F)
+        np.testing.assert_array_equal(y123.cpu().numpy(), ref)
+
+
+# ------------------------------------------------------------------------------------------- steps 1-11
+
+RUN_CASES = [
+    # M, K, N, G, x dist, w dist, scale lo, hi
+    (1, 128, 128, 128, "normal", "u8", 0.005, 0.02),
+    (3, 512, 264, 64, "t3_clip60", "u8", -1.0, 1.0),
+    (5, 384, 136, 32, "normal", "u8", 0.005, 0.02),
+    (7, 96, 1000, 32, "uniform3", "u7", -3.0, 3.0),
+    (2, 8192, 128, 64, "normal", "u8", 0.001, 0.01),
+    (12, 2048, 640, 128, "normal_cols20", "pm1_mix", 0.005, 0.02),
+    (17, 640, 392, 64, "normal", "u8", 0.005, 0.02),
+    (40, 1280, 520, 128, "t3_clip60", "u8", 0.002, 0.03),
+    (130, 512, 256, 64, "normal", "u8", 0.005, 0.02),
+]
+
+
+@pytest.mark.parametrize("M,K,N,G,xd,wd,lo,hi", RUN_CASES)
+def test_run_matches_oracle(dev, M, K, N, G, xd, wd, lo, hi):
+    x, wp, sc = I.make_inputs(I.small_case(M, K, N, G, seed=M + K + N, x_dist=xd, w_dist=wd, scale_lo=lo,
+                                           scale_hi=hi))
+    y = gpu_run(x, wp, sc, G, dev)
+    assert_within_tolerance(y, oracle.msd_matmul(x, wp, sc, G, mode=oracle.MODE_D), "binary64 oracle")
+    assert_within_tolerance(y, oracle.msd_matmul(x, wp, sc, G, mode=oracle.MODE_F), "binary32-unfold oracle")
+
+
+def test_run_zero_and_constant_rows(dev):
+    M, K, N, G = 6, 512, 256, 128
+    x, wp, sc = I.make_inputs(I.small_case(M, K, N, G, seed=3))
+    x[0] = 0
+    x[1, 128:256] = 0
+    x[2] = np.float16(0.75)
+    x[3, :128] = np.float16(-60.0)
+    y = gpu_run(x, wp, sc, G, dev)
+    assert not y[0].any()
+    assert_within_tolerance(y, oracle.msd_matmul(x, wp, sc, G), "special rows")
+
+
+def test_run_deterministic_and_workspace_left_clean(dev):
+    wl = I.WORKLOADS["decode_m1_k4096_n4096"]
+    x, wp, sc = I.make_inputs(wl)
+    xd, sd = to_dev(x, dev), to_dev(sc, dev)
+    w_pre = wq.prepack_weight(to_dev(wp, dev), wl.K, wl.N, wl.G)
+    ws = wq.allocate_workspace(wl.M, wl.K, wl.N, wl.G, dev)
+    assert ws is not None
+    outs = []
+    for _ in range(3):
+        y = torch.empty((wl.M, wl.N), dtype=torch.float16, device=dev)
+        wq.wqbmm_run(xd, w_pre, sd, y, wl.M, wl.K, wl.N, wl.G, ws)
+        outs.append(y.cpu().numpy().view(np.uint16))
+    assert all(np.array_equal(outs[0], o) for o in outs[1:])
+    # the arrival counters sit after the partial sums; all must be back at zero
+    counters = ws.cpu().numpy()[-256:].view(np.uint32)
+    assert not counters.any()
+
+
+def test_run_errors_leave_output_untouched(dev):
+    M, K, N, G = 1, 4096, 4096, 128
+    x, wp, sc = I.make_inputs(I.small_case(M, K, N, G, seed=5))
+    xd, sd = to_dev(x, dev), to_dev(sc, dev)
+    w_pre = wq.prepack_weight(to_dev(wp, dev), K, N, G)
+    ws = wq.allocate_workspace(M, K, N, G, dev)
+    y = torch.full((M, N), 7.0, dtype=torch.float16, device=dev)
+    with pytest.raises(wq.WqbmmError) as e:
+        wq.wqbmm_run(xd, w_pre, sd, y, M, K, N, G, ws, 64)                   # workspace too small
+    assert e.value.status == wq.ERR_INVALID
+    with pytest.raises(wq.WqbmmError) as e:
+        wq.wqbmm_run(xd, w_pre, sd, y, M, K + 64, N, G, ws)                  # K not a multiple of G
+    assert e.value.status == wq.ERR_INVALID
+    torch.cuda.synchronize()
+    assert (y == 7.0).all()
+
+
+def test_bounded_wait_reports_timeout(dev):
+    """A kernel waits on a barrier nothing completes; it gives up after 50 ms and records the timeout."""
+    wq.wqbmm_debug_wait_timeout(50_000_000)
+    code = wq.wqbmm_read_device_status(clear=True)
+    assert code & 0xFF == wq.ERR_DEVICE_TIMEOUT and (code >> 8) == 9
+    assert wq.wqbmm_read_device_status() == 0
+    # the context is still usable
+    x, wp, sc = I.make_inputs(I.small_case(2, 256, 128, 128, seed=1))
+    assert_within_tolerance(gpu_run(x, wp, sc, 128, dev), oracle.msd_matmul(x, wp, sc, 128), "after timeout")
+
+
+# ------------------------------------------------------------------------------------------- full workloads
+
+@pytest.mark.parametrize("name", ["pr1_m16_k1024_n1024", "decode_m1_k4096_n4096", "ffn_up_m8_k4096_n11008",
+                                  "page_sample_m1_k8192_n12288"])
+def test_workload_full_output(dev, name):
+    wl = I.WORKLOADS[name]
+    x, wp, sc = I.make_inputs(wl)
+    y = gpu_run(x, wp, sc, wl.G, dev)
+    assert_within_tolerance(y, oracle.msd_matmul(x, wp, sc, wl.G, mode=oracle.MODE_D), name)
+
+
+@pytest.mark.parametrize("name,nrows", [("mid_m128_k5120_n13824", 16), ("prefill_m2048_k8192_n28672", 64)])
+def test_workload_sampled_rows(dev, name, nrows):
+    wl = I.WORKLOADS[name]
+    x, wp, sc = I.make_inputs(wl)
+    y = gpu_run(x, wp, sc, wl.G, dev)
+    rows = I.sample_rows(wl, nrows)
+    ref = oracle.msd_matmul(x, wp, sc, wl.G, mode=oracle.MODE_D, rows=rows)
+    assert_within_tolerance(y[rows], ref, name)
+    # one group's integer partials on the same rows, bit-exact (the tensor-core step at full size)
+    g = wl.groups // 2
+    y123 = torch.empty((3, wl.M, wl.N), dtype=torch.int32, device=dev)
+    w_pre = wq.prepack_weight(to_dev(wp, dev), wl.K, wl.N, wl.G)
+    wq.wqbmm_debug_group_partials(to_dev(x, dev), w_pre, wl.M, wl.K, wl.N, wl.G, g, y123)
+    got = y123.cpu().numpy()[:, rows]
+    np.testing.assert_array_equal(got, oracle.group_partials(x, wp, wl.N, wl.G, g, oracle.MODE_F, rows=rows))

@@ -1,0 +1,178 @@
+"""A16W4 per-group pseudo-quantized matmul by MSD for GB300 (sm_103a).
+
+Python binding of the C ABI declared in include/wqbmm.h. Every function here only marshals arguments (torch tensors
+or raw device pointers, sizes, a stream) and calls the library of the same name; all arithmetic runs in the CUDA
+kernels of libwqbmm.so. There is no fallback: if the library is missing or the device is not a GB300, calls raise.
+PyTorch is used for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "WqbmmError", "library_path", "load_library", "wqbmm_prepacked_weight_bytes", "wqbmm_prepack_weight",
+    "wqbmm_workspace_bytes", "wqbmm_run", "wqbmm_debug_unfold", "wqbmm_debug_group_partials",
+    "wqbmm_read_device_status", "wqbmm_debug_wait_timeout", "wqbmm_status_string", "prepack_weight",
+    "allocate_workspace", "msd_matmul", "SYMBOLS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libwqbmm.so")
+_lock = threading.Lock()
+_lib = None
+
+OK, ERR_NULLPTR, ERR_INVALID, ERR_UNSUPPORTED_ARCH, ERR_CUDA, ERR_DEVICE_TIMEOUT = range(6)
+
+# every entry point include/wqbmm.h declares
+SYMBOLS = (
+    "wqbmm_prepacked_weight_bytes", "wqbmm_prepack_weight", "wqbmm_workspace_bytes", "wqbmm_run",
+    "wqbmm_debug_unfold", "wqbmm_debug_group_partials", "wqbmm_read_device_status", "wqbmm_debug_wait_timeout",
+    "wqbmm_status_string",
+)
+
+
+class WqbmmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {wqbmm_status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """The loaded libwqbmm.so (built in-tree by __graft_entry__.build())."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(f"{_LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; "
+                                   f"g.build()\"`")
+            lib = ctypes.CDLL(_LIB_PATH)
+            i64, p, sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+            st = ctypes.c_int
+            sig = {
+                "wqbmm_prepacked_weight_bytes": [i64, i64, i64, ctypes.POINTER(sz)],
+                "wqbmm_prepack_weight": [p, p, i64, i64, i64, p],
+                "wqbmm_workspace_bytes": [i64, i64, i64, i64, ctypes.POINTER(sz)],
+                "wqbmm_run": [p, p, p, p, i64, i64, i64, i64, p, sz, p],
+                "wqbmm_debug_unfold": [p, i64, i64, i64, p, p, p],
+                "wqbmm_debug_group_partials": [p, p, i64, i64, i64, i64, i64, p, p],
+                "wqbmm_read_device_status": [ctypes.POINTER(ctypes.c_int32), ctypes.c_int, p],
+                "wqbmm_debug_wait_timeout": [i64, p],
+            }
+            for name, args in sig.items():
+                f = getattr(lib, name)
+                f.argtypes = args
+                f.restype = st
+            lib.wqbmm_status_string.argtypes = [st]
+            lib.wqbmm_status_string.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def _ptr(a) -> int | None:
+    if a is None:
+        return None
+    if isinstance(a, int):
+        return a
+    return a.data_ptr()
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise WqbmmError(status, where)
+
+
+def wqbmm_status_string(status: int) -> str:
+    return load_library().wqbmm_status_string(int(status)).decode()
+
+
+def wqbmm_prepacked_weight_bytes(K: int, N: int, G: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load_library().wqbmm_prepacked_weight_bytes(K, N, G, ctypes.byref(out)), "wqbmm_prepacked_weight_bytes")
+    return out.value
+
+
+def wqbmm_prepack_weight(w_packed, w_prepacked, K: int, N: int, G: int, stream=None) -> None:
+    _check(load_library().wqbmm_prepack_weight(_ptr(w_packed), _ptr(w_prepacked), K, N, G, _stream(stream)),
+           "wqbmm_prepack_weight")
+
+
+def wqbmm_workspace_bytes(M: int, K: int, N: int, G: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load_library().wqbmm_workspace_bytes(M, K, N, G, ctypes.byref(out)), "wqbmm_workspace_bytes")
+    return out.value
+
+
+def wqbmm_run(x, w_prepacked, antiquant_scale, y, M: int, K: int, N: int, G: int, workspace=None,
+              workspace_bytes: int | None = None, stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().wqbmm_run(_ptr(x), _ptr(w_prepacked), _ptr(antiquant_scale), _ptr(y), M, K, N, G,
+                                     _ptr(workspace), workspace_bytes, _stream(stream)), "wqbmm_run")
+
+
+def wqbmm_debug_unfold(x, M: int, K: int, G: int, planes, amax, stream=None) -> None:
+    _check(load_library().wqbmm_debug_unfold(_ptr(x), M, K, G, _ptr(planes), _ptr(amax), _stream(stream)),
+           "wqbmm_debug_unfold")
+
+
+def wqbmm_debug_group_partials(x, w_prepacked, M: int, K: int, N: int, G: int, g: int, y123, stream=None) -> None:
+    _check(load_library().wqbmm_debug_group_partials(_ptr(x), _ptr(w_prepacked), M, K, N, G, g, _ptr(y123),
+                                                     _stream(stream)), "wqbmm_debug_group_partials")
+
+
+def wqbmm_read_device_status(clear: bool = False, stream=None) -> int:
+    code = ctypes.c_int32(0)
+    _check(load_library().wqbmm_read_device_status(ctypes.byref(code), int(bool(clear)), _stream(stream)),
+           "wqbmm_read_device_status")
+    return code.value
+
+
+def wqbmm_debug_wait_timeout(limit_ns: int, stream=None) -> None:
+    _check(load_library().wqbmm_debug_wait_timeout(limit_ns, _stream(stream)), "wqbmm_debug_wait_timeout")
+
+
+# ---------------------------------------------------------------------------- allocation helpers (torch memory)
+
+def prepack_weight(w_packed, K: int, N: int, G: int, stream=None):
+    """uint8 [K/2, N] packed int4 on the GPU -> a new uint8 tensor in the prepacked tile layout."""
+    import torch
+    out = torch.empty(wqbmm_prepacked_weight_bytes(K, N, G), dtype=torch.uint8, device=w_packed.device)
+    wqbmm_prepack_weight(w_packed, out, K, N, G, stream)
+    return out
+
+
+def allocate_workspace(M: int, K: int, N: int, G: int, device):
+    """Zero-filled workspace for wqbmm_run (None when the shape needs none)."""
+    import torch
+    nbytes = wqbmm_workspace_bytes(M, K, N, G)
+    if nbytes == 0:
+        return None
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device)
+
+
+def msd_matmul(x, w_prepacked, antiquant_scale, G: int, y=None, workspace=None, stream=None):
+    """y [M, N] fp16 = MSD matmul of x [M, K] fp16 with prepacked int4 weights and antiquant_scale [K/G, N] fp16."""
+    import torch
+    M, K = x.shape
+    N = antiquant_scale.shape[1]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    if workspace is None:
+        workspace = allocate_workspace(M, K, N, G, x.device)
+    wqbmm_run(x, w_prepacked, antiquant_scale, y, M, K, N, G, workspace, None, stream)
+    return y

@@ -1,0 +1,557 @@
+// Device code of the A16W4 per-group MSD matmul (WeightQuantBatchMatmulExperiment page, section 4.1).
+//
+// Kernels:
+//   prepack_kernel      packed int4 [K/2, N] -> 128x128 tiles, output-column-major, offset-binary nibbles
+//   unfold_debug_kernel steps 1-8 to global memory (int8 planes, float A_max), same arithmetic as the run kernel
+//   msd_kernel<NMMA>    steps 1-11 fused: per CTA one 128-column tile of y, a tile of rows and a K-slice
+//   wait_timeout_kernel a bounded wait that nothing completes (exercises the timeout path)
+//
+// The run kernel computes the swapped product D^T = W^T . A_int^T on the 5th-generation tensor core: the MMA's
+// M side is 128 weight columns (so TMEM lane = output column n), its N side is the three stacked residual planes
+// of the row tile (NMMA = 16, 32 or 48 stacked rows), one MMA chain per K-group restarted at every group so the
+// integer partial sums stay exact in FP32. Roles inside a CTA (320 threads):
+//   warp 0      TMA producer: bulk-copies packed weight tiles (8 KB per 128 k) into a 4-stage ring
+//   warp 1      TMEM owner and single-thread MMA issuer (tcgen05.mma kind::f8f6f4, E4M3 x E4M3 -> F32)
+//   warps 2-5   weight converters: int4 (offset binary) -> E4M3 bytes in the 128-byte-swizzled K-major layout
+//   warps 6-9   unfold (A_max, three planes as E4M3, per-group constants) one k-block ahead, then the epilogue:
+//               TMEM -> registers, Y_i = D_i - 8 S_i folded into the combine, scale, accumulate over groups
+// Weights are stored as u = w + 8 in [0, 15] so that the int4 -> E4M3 conversion is two byte permutes and an OR;
+// the MMA then yields D_i = sum A_i u = Y_i + 8 S_i with S_i = sum A_i over the group, removed in the combine.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace wqbmm {
+
+constexpr int kTileN = 128;                          // output columns per CTA (MMA M)
+constexpr int kKBlock = 128;                         // k per pipeline stage (one 128-byte E4M3 swizzle row)
+constexpr int kPackedTileBytes = kTileN * kKBlock / 2;  // 8192
+constexpr int kATileBytes = kTileN * kKBlock;        // 16384
+constexpr int kPStages = 4;                          // packed weight ring
+constexpr int kCStages = 3;                          // converted weights / planes / constants ring
+constexpr int kLookahead = kCStages - 1;             // unfold runs this many k-blocks ahead of the epilogue
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kConvWarp0 = 2;
+constexpr int kNumConvWarps = 4;
+constexpr int kEpiWarp0 = 6;
+constexpr int kNumEpiWarps = 4;
+constexpr int kEpiBarrierId = 1;
+constexpr int kMaxGroupsPerKBlock = kKBlock / 32;
+constexpr int kConstFloatsPerGroup = 8 * 16;          // a1 a2 a3 corr S1 S2 S3 (pad) x 16 rows
+constexpr int kConstStageFloats = kMaxGroupsPerKBlock * kConstFloatsPerGroup;
+
+// Method constants (page section 4.1): unfold factors and the combine weights 1/7.49, 1/(7.49*14.98), ...
+constexpr float kF1 = 7.49f;
+constexpr float kF2 = 14.98f;
+constexpr float kC1 = static_cast<float>(1.0 / 7.49);
+constexpr float kC2 = static_cast<float>(1.0 / (7.49 * 14.98));
+constexpr float kC3 = static_cast<float>(1.0 / (7.49 * 14.98 * 14.98));
+
+// Wait-site ids recorded with a timeout
+enum WaitSite : int {
+    kSiteProducerEmpty = 1,
+    kSiteConvFull = 2,
+    kSiteConvEmpty = 3,
+    kSiteMmaOperands = 4,
+    kSiteMmaTmemEmpty = 5,
+    kSiteEpiOperandsEmpty = 6,
+    kSiteEpiTmemFull = 7,
+    kSiteDebugWait = 9,
+};
+
+template <int NMMA>
+struct Cfg {
+    static_assert(NMMA == 16 || NMMA == 32 || NMMA == 48, "MMA N must be 16, 32 or 48");
+    static constexpr int kMaxM = NMMA / 3;                         // rows of x per CTA (plane stride in B rows)
+    static constexpr int kBufStride = NMMA <= 16 ? 16 : (NMMA <= 32 ? 32 : 64);   // TMEM columns per buffer
+    static constexpr int kTmemCols = 2 * kBufStride < 32 ? 32 : 2 * kBufStride;
+    static constexpr int kBTileBytes = NMMA * kKBlock;
+    // shared memory carve-up (offsets from a 1024-byte aligned base)
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + kCStages * kATileBytes;
+    static constexpr int kOffP = kOffB + kCStages * kBTileBytes;
+    static constexpr int kOffConst = kOffP + kPStages * kPackedTileBytes;
+    static constexpr int kOffBar = kOffConst + kCStages * kConstStageFloats * 4;
+    static constexpr int kNumBars = 2 * kPStages + 3 * kCStages + 4;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kSmemBytes = kOffMisc + 64 + 1024;       // + alignment slack
+};
+
+struct RunParams {
+    const __half *x;
+    const uint8_t *w;           // prepacked tiles
+    const __half *scale;
+    __half *y;
+    float *ws_part;             // [splits, M, N] split-K partial sums (splits > 1)
+    uint32_t *ws_count;         // [m_tiles, n_tiles] arrival counters (splits > 1)
+    int32_t *dbg_y123;          // [3, M, N] integer partials of group dbg_group (debug mode), else null
+    int M, K, N, G;
+    int m_sub, n_tiles, m_tiles, splits, kb_total;
+    int dbg_group;              // -1 in normal runs
+};
+
+// ------------------------------------------------------------------------------------------------ unfold
+
+// Steps 2-7 for four values of one group, IEEE binary32 with every operation rounded on its own (no contraction);
+// rintf rounds half to even. A group whose A_max is 0 gives zero planes.
+__device__ __forceinline__ void msd_unfold4(const float (&x)[4], float amax, float (&a1)[4], float (&a2)[4],
+                                            float (&a3)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (amax == 0.0f) {
+            a1[j] = a2[j] = a3[j] = 0.0f;
+            continue;
+        }
+        const float t1 = __fdiv_rn(__fmul_rn(kF1, x[j]), amax);
+        const float r1 = rintf(t1);
+        const float t2 = __fmul_rn(__fsub_rn(t1, r1), kF2);
+        const float r2 = rintf(t2);
+        const float t3 = __fmul_rn(__fsub_rn(t2, r2), kF2);
+        a1[j] = r1;
+        a2[j] = r2;
+        a3[j] = rintf(t3);
+    }
+}
+
+// Four fp16 of one row starting at k (k % 4 == 0); zeros past K or for rows past M.
+__device__ __forceinline__ void load_x4(const __half *x, int M, int K, int row, int k, float (&v)[4]) {
+    v[0] = v[1] = v[2] = v[3] = 0.0f;
+    if (row < M && k < K) {
+        const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(x + static_cast<size_t>(row) * K + k));
+        const __half2 h01 = *reinterpret_cast<const __half2 *>(&raw.x);
+        const __half2 h23 = *reinterpret_cast<const __half2 *>(&raw.y);
+        const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+        v[0] = f01.x;
+        v[1] = f01.y;
+        v[2] = f23.x;
+        v[3] = f23.y;
+    }
+}
+
+// Max / sum over the lanes that share one group: a group spans G/4 consecutive lanes (4 values per lane).
+__device__ __forceinline__ float group_max(float v, int lanes_per_group) {
+    for (int off = 1; off < lanes_per_group; off <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+__device__ __forceinline__ float group_sum(float v, int lanes_per_group) {
+    for (int off = 1; off < lanes_per_group; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+// Byte offset of (row, k) in a K-major 128-byte-swizzled operand tile with 128-byte rows.
+__device__ __forceinline__ uint32_t sw128_offset(int row, int kbyte) {
+    return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 + ((((kbyte >> 4) ^ (row & 7)) << 4)) +
+                                 (kbyte & 15));
+}
+
+// ------------------------------------------------------------------------------------------------ int4 -> e4m3
+
+// E4M3 encodings of 0..7 and 8..15 (bytes little-endian in each word)
+constexpr uint32_t kLut0to3 = 0x44403800u, kLut4to7 = 0x4E4C4A48u;
+constexpr uint32_t kLut8to11 = 0x53525150u, kLut12to15 = 0x57565554u;
+
+// Four offset-binary nibbles (sel bits 15..0, nibble j -> output byte j) to four E4M3 bytes. Nibbles 0..7 select
+// from the low table; 8..15 have their msb set, which makes prmt emit the (zero) sign of a positive table byte, so
+// the low lookup yields 0 for them. The second lookup runs on the nibbles with msb flipped and covers 8..15.
+__device__ __forceinline__ uint32_t u4x4_to_e4m3(uint32_t sel, uint32_t sel_flipped) {
+    return prmt(kLut0to3, kLut4to7, sel) | prmt(kLut8to11, kLut12to15, sel_flipped);
+}
+
+// ------------------------------------------------------------------------------------------------ kernels
+
+__global__ void prepack_kernel(const uint8_t *__restrict__ in, uint8_t *__restrict__ out, int K, int N,
+                               int kb_total) {
+    __shared__ uint8_t tile[kKBlock / 2][kTileN + 4];
+    const int nt = blockIdx.x, kb = blockIdx.y;
+    const int half_k = K / 2;
+    for (int idx = threadIdx.x; idx < (kKBlock / 2) * kTileN; idx += blockDim.x) {
+        const int kk = idx / kTileN, c = idx % kTileN;
+        const int gk = kb * (kKBlock / 2) + kk, gn = nt * kTileN + c;
+        uint8_t v = 0;                                               // two zero weights
+        if (gk < half_k && gn < N) v = in[static_cast<size_t>(gk) * N + gn];
+        tile[kk][c] = static_cast<uint8_t>(v ^ 0x88u);               // w -> w + 8 in both nibbles
+    }
+    __syncthreads();
+    uint8_t *dst = out + (static_cast<size_t>(nt) * kb_total + kb) * kPackedTileBytes;
+    for (int idx = threadIdx.x; idx < kPackedTileBytes; idx += blockDim.x) {
+        const int r = idx / (kKBlock / 2), j = idx % (kKBlock / 2);
+        dst[idx] = tile[j][r];
+    }
+}
+
+// One warp per (row, 128-k block): the same lane mapping and arithmetic as the run kernel's unfold.
+__global__ void unfold_debug_kernel(const __half *__restrict__ x, int M, int K, int G, int8_t *__restrict__ planes,
+                                    float *__restrict__ amax_out) {
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x;
+    const int kwarp = (blockIdx.y * (blockDim.x / 32) + threadIdx.x / 32) * kKBlock;
+    if (kwarp >= K) return;                                          // whole warp: no lane left behind a shuffle
+    const int kbase = kwarp + lane * 4;
+    const bool valid = kbase < K;                                    // lanes past K compute on zeros, store nothing
+    float v[4];
+    load_x4(x, M, K, row, kbase, v);
+    const int lpg = G / 4;
+    float am = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    am = group_max(am, lpg);
+    float a1[4], a2[4], a3[4];
+    msd_unfold4(v, am, a1, a2, a3);
+    if (!valid) return;
+    const size_t plane = static_cast<size_t>(M) * K;
+    const size_t base = static_cast<size_t>(row) * K + kbase;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        planes[base + j] = static_cast<int8_t>(__float2int_rn(a1[j]));
+        planes[plane + base + j] = static_cast<int8_t>(__float2int_rn(a2[j]));
+        planes[2 * plane + base + j] = static_cast<int8_t>(__float2int_rn(a3[j]));
+    }
+    if ((lane & (lpg - 1)) == 0) amax_out[static_cast<size_t>(row) * (K / G) + kbase / G] = am;
+}
+
+__global__ void wait_timeout_kernel(uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(&bar), 1);
+        abort_flag = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // nothing arrives on this barrier: the wait must give up and record the timeout
+        mbar_wait(smem_addr(&bar), 0, &abort_flag, kSiteDebugWait, limit_ns);
+        mbar_arrive(smem_addr(&bar));                                // complete the phase before exit
+    }
+}
+
+template <int NMMA>
+__global__ void __launch_bounds__(kThreads, 2) msd_kernel(const RunParams p) {
+    using C = Cfg<NMMA>;
+    constexpr int kMaxM = C::kMaxM;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *a_ring = smem + C::kOffA;
+    uint8_t *b_ring = smem + C::kOffB;
+    uint8_t *p_ring = smem + C::kOffP;
+    float *const_ring = reinterpret_cast<float *>(smem + C::kOffConst);
+    const uint32_t bar0 = smem_addr(smem + C::kOffBar);
+    // barrier addresses: full_p[P] empty_p[P] full_a[C] full_b[C] empty_o[C] full_t[2] empty_t[2]
+    auto full_p = [&](int s) { return bar0 + 8u * s; };
+    auto empty_p = [&](int s) { return bar0 + 8u * (kPStages + s); };
+    auto full_a = [&](int c) { return bar0 + 8u * (2 * kPStages + c); };
+    auto full_b = [&](int c) { return bar0 + 8u * (2 * kPStages + kCStages + c); };
+    auto empty_o = [&](int c) { return bar0 + 8u * (2 * kPStages + 2 * kCStages + c); };
+    auto full_t = [&](int b) { return bar0 + 8u * (2 * kPStages + 3 * kCStages + b); };
+    auto empty_t = [&](int b) { return bar0 + 8u * (2 * kPStages + 3 * kCStages + 2 + b); };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+    int *last_flag = reinterpret_cast<int *>(smem + C::kOffMisc + 8);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nt = blockIdx.x, mt = blockIdx.y, sp = blockIdx.z;
+    const int M = p.M, K = p.K, N = p.N, G = p.G;
+    const int m0 = mt * p.m_sub;
+    int kb0, kb1;
+    if (p.dbg_group >= 0) {
+        kb0 = p.dbg_group * G / kKBlock;
+        kb1 = kb0 + 1;
+    } else {
+        kb0 = static_cast<int>(static_cast<int64_t>(sp) * p.kb_total / p.splits);
+        kb1 = static_cast<int>(static_cast<int64_t>(sp + 1) * p.kb_total / p.splits);
+    }
+    const int nkb = kb1 - kb0;
+
+    // ---- set-up: barriers, TMEM, zeroed plane tiles (rows past the row tile must read as zero)
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPStages; ++s) {
+            mbar_init(full_p(s), 1);
+            mbar_init(empty_p(s), kNumConvWarps);
+        }
+        for (int c = 0; c < kCStages; ++c) {
+            mbar_init(full_a(c), kNumConvWarps);
+            mbar_init(full_b(c), kNumEpiWarps);
+            mbar_init(empty_o(c), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(full_t(b), 1);
+            mbar_init(empty_t(b), kNumEpiWarps);
+        }
+        *abort_flag = 0;
+        *last_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+        tc_fence_before_sync();
+    }
+    for (int i = threadIdx.x; i < kCStages * C::kBTileBytes / 16; i += kThreads)
+        reinterpret_cast<uint4 *>(b_ring)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == kProducerWarp) {
+        // ================================================================ TMA producer
+        if (lane == 0) {
+            const uint64_t policy = l2_policy_evict_first();
+            const uint8_t *src = p.w + (static_cast<size_t>(nt) * p.kb_total + kb0) * kPackedTileBytes;
+            int issued = 0;
+            for (; issued < nkb; ++issued) {
+                const int s = issued % kPStages;
+                const uint32_t ph = (issued / kPStages) & 1;
+                if (!mbar_wait(empty_p(s), ph ^ 1, abort_flag, kSiteProducerEmpty)) break;
+                mbar_arrive_expect_tx(full_p(s), kPackedTileBytes);
+                bulk_g2s(smem_addr(p_ring + s * kPackedTileBytes), src + static_cast<size_t>(issued) * kPackedTileBytes,
+                         kPackedTileBytes, full_p(s), policy);
+            }
+            // no copy may still be writing shared memory when the CTA exits
+            for (int j = issued > kPStages ? issued - kPStages : 0; j < issued; ++j)
+                mbar_wait_drain(full_p(j % kPStages), (j / kPStages) & 1);
+        }
+    } else if (warp == kMmaWarp) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_e4m3_f32(NMMA);
+            int j = 0;                       // CTA-local group counter
+            int last_j[2] = {-1, -1};
+            for (int i = 0; i < nkb; ++i) {
+                const int c = i % kCStages;
+                const uint32_t ph = (i / kCStages) & 1;
+                if (!mbar_wait(full_a(c), ph, abort_flag, kSiteMmaOperands)) break;
+                if (!mbar_wait(full_b(c), ph, abort_flag, kSiteMmaOperands)) break;
+                tc_fence_after_sync();
+                const int kb = kb0 + i;
+                const int kend = min(K, (kb + 1) * kKBlock);
+                const int ng = (kend - kb * kKBlock) / G;
+                const uint32_t a_base = smem_addr(a_ring + c * kATileBytes);
+                const uint32_t b_base = smem_addr(b_ring + c * C::kBTileBytes);
+                bool stop = false;
+                for (int gg = 0; gg < ng; ++gg, ++j) {
+                    const int b = j & 1;
+                    if (!mbar_wait(empty_t(b), ((j >> 1) & 1) ^ 1, abort_flag, kSiteMmaTmemEmpty)) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * C::kBufStride);
+                    for (int ks = 0; ks < G / 32; ++ks) {
+                        const uint32_t kofs = static_cast<uint32_t>(gg * G + ks * 32);
+                        umma_f8f6f4(d_tmem, sdesc_kmajor_sw128(a_base + kofs), sdesc_kmajor_sw128(b_base + kofs),
+                                    idesc, ks > 0 ? 1u : 0u);
+                    }
+                    umma_commit(full_t(b));
+                    last_j[b] = j;
+                }
+                if (stop) break;
+                umma_commit(empty_o(c));
+            }
+            // no MMA may still be writing TMEM when it is freed
+            for (int b = 0; b < 2; ++b)
+                if (last_j[b] >= 0) mbar_wait_drain(full_t(b), (last_j[b] >> 1) & 1);
+        }
+        __syncwarp();
+    } else if (warp < kConvWarp0 + kNumConvWarps) {
+        // ================================================================ int4 -> E4M3 converters
+        const int ct = threadIdx.x - kConvWarp0 * 32;
+        for (int i = 0; i < nkb; ++i) {
+            const int s = i % kPStages, c = i % kCStages;
+            bool ok = true;
+            if (lane == 0)
+                ok = mbar_wait(full_p(s), (i / kPStages) & 1, abort_flag, kSiteConvFull) &&
+                     mbar_wait(empty_o(c), ((i / kCStages) & 1) ^ 1, abort_flag, kSiteConvEmpty);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            const uint8_t *src = p_ring + s * kPackedTileBytes;
+            uint8_t *dst = a_ring + c * kATileBytes;
+#pragma unroll
+            for (int it = 0; it < kPackedTileBytes / 8 / (kNumConvWarps * 32); ++it) {
+                const int q = ct + it * kNumConvWarps * 32;     // 16-k chunk of one weight row
+                const int row = q >> 3, ch = q & 7;
+                const uint2 v = *reinterpret_cast<const uint2 *>(src + q * 8);
+                const uint32_t vx = v.x ^ 0x88888888u, vy = v.y ^ 0x88888888u;
+                uint4 o;
+                o.x = u4x4_to_e4m3(v.x, vx);
+                o.y = u4x4_to_e4m3(v.x >> 16, vx >> 16);
+                o.z = u4x4_to_e4m3(v.y, vy);
+                o.w = u4x4_to_e4m3(v.y >> 16, vy >> 16);
+                *reinterpret_cast<uint4 *>(dst + (row >> 3) * 1024 + (row & 7) * 128 + ((ch ^ (row & 7)) << 4)) = o;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(empty_p(s));
+                mbar_arrive(full_a(c));
+            }
+        }
+    } else {
+        // ================================================================ unfold + epilogue
+        const int ew = warp - kEpiWarp0;                 // unfold row assignment
+        const int quarter = warp & 3;                    // TMEM lanes this warp may read
+        const int et = threadIdx.x - kEpiWarp0 * 32;
+        const int n = nt * kTileN + quarter * 32 + lane;
+        const int lpg = G / 4;                           // lanes per group in the unfold
+        const int rows_valid = min(p.m_sub, M - m0);
+        float yacc[kMaxM];
+#pragma unroll
+        for (int m = 0; m < kMaxM; ++m) yacc[m] = 0.0f;
+
+        auto unfold_kblock = [&](int i) {
+            const int c = i % kCStages;
+            const int kb = kb0 + i;
+            uint8_t *bt = b_ring + c * C::kBTileBytes;
+            float *cst = const_ring + c * kConstStageFloats;
+            const int kbyte = lane * 4;
+            for (int m = ew; m < p.m_sub; m += kNumEpiWarps) {
+                float v[4];
+                load_x4(p.x, M, K, m0 + m, kb * kKBlock + kbyte, v);
+                float am = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+                am = group_max(am, lpg);
+                float a1[4], a2[4], a3[4];
+                msd_unfold4(v, am, a1, a2, a3);
+                const uint32_t w1 = e4m3x2(a1[1], a1[0]) | (e4m3x2(a1[3], a1[2]) << 16);
+                const uint32_t w2 = e4m3x2(a2[1], a2[0]) | (e4m3x2(a2[3], a2[2]) << 16);
+                const uint32_t w3 = e4m3x2(a3[1], a3[0]) | (e4m3x2(a3[3], a3[2]) << 16);
+                *reinterpret_cast<uint32_t *>(bt + sw128_offset(m, kbyte)) = w1;
+                *reinterpret_cast<uint32_t *>(bt + sw128_offset(kMaxM + m, kbyte)) = w2;
+                *reinterpret_cast<uint32_t *>(bt + sw128_offset(2 * kMaxM + m, kbyte)) = w3;
+                const float s1 = group_sum((a1[0] + a1[1]) + (a1[2] + a1[3]), lpg);
+                const float s2 = group_sum((a2[0] + a2[1]) + (a2[2] + a2[3]), lpg);
+                const float s3 = group_sum((a3[0] + a3[1]) + (a3[2] + a3[3]), lpg);
+                if ((lane & (lpg - 1)) == 0) {
+                    float *cg = cst + (lane / lpg) * kConstFloatsPerGroup;
+                    const float c1 = kC1 * am, c2 = kC2 * am, c3 = kC3 * am;
+                    cg[0 * 16 + m] = c1;
+                    cg[1 * 16 + m] = c2;
+                    cg[2 * 16 + m] = c3;
+                    cg[3 * 16 + m] = 8.0f * (c1 * s1 + c2 * s2 + c3 * s3);
+                    cg[4 * 16 + m] = s1;
+                    cg[5 * 16 + m] = s2;
+                    cg[6 * 16 + m] = s3;
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full_b(c));
+        };
+
+        const int nlook = nkb < kLookahead ? nkb : kLookahead;
+        for (int i = 0; i < nlook; ++i) unfold_kblock(i);        // first uses of the ring slots: no wait
+        named_bar_sync(kEpiBarrierId, kNumEpiWarps * 32);         // constants visible to all epilogue threads
+
+        bool ok = true;
+        int j = 0;
+        for (int i = 0; i < nkb; ++i) {
+            const int iu = i + kLookahead;
+            if (ok && iu < nkb) {
+                const int c = iu % kCStages;
+                ok = mbar_wait(empty_o(c), ((iu / kCStages) & 1) ^ 1, abort_flag, kSiteEpiOperandsEmpty);
+                if (ok) unfold_kblock(iu);
+            }
+            const int kb = kb0 + i;
+            const int gfirst = kb * kKBlock / G;
+            const int ng = (min(K, (kb + 1) * kKBlock) - kb * kKBlock) / G;
+            const float *cst = const_ring + (i % kCStages) * kConstStageFloats;
+            for (int gg = 0; gg < ng && ok; ++gg, ++j) {
+                const int b = j & 1;
+                const int g = gfirst + gg;
+                const bool use_scale = p.dbg_group < 0 && n < N;     // debug runs pass no scale
+                const float s_n = use_scale ? __half2float(p.scale[static_cast<size_t>(g) * N + n]) : 0.0f;
+                ok = mbar_wait(full_t(b), (j >> 1) & 1, abort_flag, kSiteEpiTmemFull);
+                if (!ok) break;
+                tc_fence_after_sync();
+                uint32_t d[3][16];
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                       static_cast<uint32_t>(b * C::kBufStride);
+                tmem_ld16(taddr, d[0]);
+                if (NMMA > 16) tmem_ld16(taddr + 16, d[1]);
+                if (NMMA > 32) tmem_ld16(taddr + 32, d[2]);
+                tmem_wait_ld();
+                reg_fence16(d[0]);
+                if (NMMA > 16) reg_fence16(d[1]);
+                if (NMMA > 32) reg_fence16(d[2]);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_t(b));
+                const float *cg = cst + gg * kConstFloatsPerGroup;
+                if (p.dbg_group >= 0) {
+                    if (g == p.dbg_group && n < N) {
+#pragma unroll
+                        for (int m = 0; m < kMaxM; ++m) {
+                            if (m < rows_valid) {
+#pragma unroll
+                                for (int pl = 0; pl < 3; ++pl) {
+                                    const int col = pl * kMaxM + m;
+                                    const float dv = __uint_as_float(d[col >> 4][col & 15]);
+                                    const float yi = dv - 8.0f * cg[(4 + pl) * 16 + m];
+                                    p.dbg_y123[(static_cast<size_t>(pl) * M + m0 + m) * N + n] = __float2int_rn(yi);
+                                }
+                            }
+                        }
+                    }
+                    continue;
+                }
+#pragma unroll
+                for (int m = 0; m < kMaxM; ++m) {
+                    const float d1 = __uint_as_float(d[m >> 4][m & 15]);
+                    const float d2 = __uint_as_float(d[(kMaxM + m) >> 4][(kMaxM + m) & 15]);
+                    const float d3 = __uint_as_float(d[(2 * kMaxM + m) >> 4][(2 * kMaxM + m) & 15]);
+                    float t = fmaf(cg[m], d1, -cg[48 + m]);
+                    t = fmaf(cg[16 + m], d2, t);
+                    t = fmaf(cg[32 + m], d3, t);
+                    yacc[m] = fmaf(s_n, t, yacc[m]);
+                }
+            }
+            // one decision for all epilogue threads; also orders the constants of later k-blocks
+            ok = !named_bar_or(kEpiBarrierId, kNumEpiWarps * 32, !ok);
+            if (!ok) break;
+        }
+
+        if (ok && p.dbg_group < 0) {
+            if (p.splits == 1) {
+#pragma unroll
+                for (int m = 0; m < kMaxM; ++m)
+                    if (m < rows_valid && n < N) p.y[static_cast<size_t>(m0 + m) * N + n] = __float2half_rn(yacc[m]);
+            } else {
+                float *part = p.ws_part + static_cast<size_t>(sp) * M * N;
+#pragma unroll
+                for (int m = 0; m < kMaxM; ++m)
+                    if (m < rows_valid && n < N) part[static_cast<size_t>(m0 + m) * N + n] = yacc[m];
+                __threadfence();
+                named_bar_sync(kEpiBarrierId, kNumEpiWarps * 32);
+                if (et == 0) {
+                    const uint32_t prev = atomicAdd(p.ws_count + static_cast<size_t>(mt) * p.n_tiles + nt, 1u);
+                    *last_flag = (prev == static_cast<uint32_t>(p.splits - 1));
+                }
+                named_bar_sync(kEpiBarrierId, kNumEpiWarps * 32);
+                if (*last_flag) {
+                    __threadfence();
+#pragma unroll
+                    for (int m = 0; m < kMaxM; ++m) {
+                        if (m < rows_valid && n < N) {
+                            float acc = 0.0f;
+                            for (int s = 0; s < p.splits; ++s)
+                                acc += __ldcg(p.ws_part + (static_cast<size_t>(s) * M + m0 + m) * N + n);
+                            p.y[static_cast<size_t>(m0 + m) * N + n] = __float2half_rn(acc);
+                        }
+                    }
+                    if (et == 0) p.ws_count[static_cast<size_t>(mt) * p.n_tiles + nt] = 0u;
+                }
+            }
+        }
+    }
+
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+}  // namespace wqbmm

@@ -1,0 +1,302 @@
+// C ABI of the A16W4 per-group MSD matmul for GB300 (declared and documented in include/wqbmm.h).
+// Host code: argument validation (no GPU needed), split-K planning, kernel launches on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include "msd_kernels.cuh"
+#include "wqbmm.h"
+
+namespace wqbmm {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kPlanSms = 160;       // workspace sizing assumes at most this many SMs, so it needs no device
+constexpr int kCtasPerSm = 2;       // shared memory (about 110 KB) and TMEM allow two run CTAs per SM
+
+struct DeviceInfo {
+    bool probed = false;
+    bool supported = false;
+    int sms = 0;
+    bool smem_set[3] = {false, false, false};
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+
+struct Shape {
+    int64_t M, K, N, G;
+};
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+wqbmm_status check_kng(int64_t K, int64_t N, int64_t G) {
+    if (K < 1 || N < 1 || K > INT_MAX || N > INT_MAX) return WQBMM_ERR_INVALID;
+    if (G != 32 && G != 64 && G != 128) return WQBMM_ERR_INVALID;
+    if (K % G != 0 || N % 8 != 0) return WQBMM_ERR_INVALID;
+    if (ceil_div(K, kKBlock) > 65535) return WQBMM_ERR_INVALID;    // prepack grid.y
+    return WQBMM_OK;
+}
+
+wqbmm_status check_shape(const Shape &s) {
+    wqbmm_status st = check_kng(s.K, s.N, s.G);
+    if (st != WQBMM_OK) return st;
+    if (s.M < 1 || s.M > INT_MAX) return WQBMM_ERR_INVALID;
+    if (s.M > (INT64_C(1) << 62) / s.N || s.M > (INT64_C(1) << 62) / s.K) return WQBMM_ERR_INVALID;
+    return WQBMM_OK;
+}
+
+// Rows of x per CTA and the MMA N (three stacked planes padded to 16, 32 or 48 rows).
+struct Plan {
+    int m_sub, m_tiles, n_tiles, kb_total, splits, nmma;
+};
+
+Plan make_plan(const Shape &s, int sms) {
+    Plan p{};
+    p.m_tiles = static_cast<int>(ceil_div(s.M, 16));
+    p.m_sub = static_cast<int>(ceil_div(s.M, p.m_tiles));
+    p.nmma = p.m_sub <= 5 ? 16 : (p.m_sub <= 10 ? 32 : 48);
+    p.n_tiles = static_cast<int>(ceil_div(s.N, kTileN));
+    p.kb_total = static_cast<int>(ceil_div(s.K, kKBlock));
+    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+    const int64_t target = static_cast<int64_t>(kCtasPerSm) * sms;
+    int64_t splits = 1;
+    if (tiles < sms) splits = target / tiles;
+    if (splits > p.kb_total) splits = p.kb_total;
+    if (splits < 1) splits = 1;
+    p.splits = static_cast<int>(splits);
+    return p;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+size_t workspace_for(const Shape &s, const Plan &p) {
+    if (p.splits <= 1) return 0;
+    return align256(static_cast<size_t>(p.splits) * s.M * s.N * sizeof(float)) +
+           align256(static_cast<size_t>(p.m_tiles) * p.n_tiles * sizeof(uint32_t));
+}
+
+// Current device must be compute capability 10.3; caches the SM count.
+wqbmm_status current_device(int *dev_out, DeviceInfo **info_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return WQBMM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return WQBMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo &d = g_devices[dev];
+    if (!d.probed) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return WQBMM_ERR_CUDA;
+        d.supported = (major == 10 && minor == 3);
+        d.sms = sms;
+        d.probed = true;
+    }
+    if (!d.supported) return WQBMM_ERR_UNSUPPORTED_ARCH;
+    *dev_out = dev;
+    *info_out = &d;
+    return WQBMM_OK;
+}
+
+template <int NMMA>
+wqbmm_status launch_msd(const RunParams &rp, const Plan &plan, DeviceInfo *info, cudaStream_t stream) {
+    constexpr int idx = NMMA / 16 - 1;
+    const int smem = Cfg<NMMA>::kSmemBytes;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (!info->smem_set[idx]) {
+            if (cudaFuncSetAttribute(msd_kernel<NMMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+                cudaSuccess)
+                return WQBMM_ERR_CUDA;
+            info->smem_set[idx] = true;
+        }
+    }
+    const dim3 grid(plan.n_tiles, plan.m_tiles, rp.dbg_group >= 0 ? 1 : plan.splits);
+    msd_kernel<NMMA><<<grid, kThreads, smem, stream>>>(rp);
+    return cudaPeekAtLastError() == cudaSuccess ? WQBMM_OK : WQBMM_ERR_CUDA;
+}
+
+wqbmm_status launch_plan(const RunParams &rp, const Plan &plan, DeviceInfo *info, cudaStream_t stream) {
+    if (plan.m_tiles > 65535 || plan.splits > 65535) return WQBMM_ERR_INVALID;
+    switch (plan.nmma) {
+        case 16: return launch_msd<16>(rp, plan, info, stream);
+        case 32: return launch_msd<32>(rp, plan, info, stream);
+        default: return launch_msd<48>(rp, plan, info, stream);
+    }
+}
+
+}  // namespace
+}  // namespace wqbmm
+
+using namespace wqbmm;
+
+extern "C" {
+
+const char *wqbmm_status_string(wqbmm_status status) {
+    switch (status) {
+        case WQBMM_OK: return "WQBMM_OK";
+        case WQBMM_ERR_NULLPTR: return "WQBMM_ERR_NULLPTR: a required pointer is null";
+        case WQBMM_ERR_INVALID: return "WQBMM_ERR_INVALID: size, alignment or workspace rule broken";
+        case WQBMM_ERR_UNSUPPORTED_ARCH: return "WQBMM_ERR_UNSUPPORTED_ARCH: device is not compute capability 10.3";
+        case WQBMM_ERR_CUDA: return "WQBMM_ERR_CUDA: a CUDA runtime call failed";
+        case WQBMM_ERR_DEVICE_TIMEOUT: return "WQBMM_ERR_DEVICE_TIMEOUT: a kernel gave up a bounded wait";
+    }
+    return "WQBMM_ERR_UNKNOWN";
+}
+
+wqbmm_status wqbmm_prepacked_weight_bytes(int64_t K, int64_t N, int64_t G, size_t *bytes) {
+    if (!bytes) return WQBMM_ERR_NULLPTR;
+    const wqbmm_status st = check_kng(K, N, G);
+    if (st != WQBMM_OK) return st;
+    *bytes = static_cast<size_t>(ceil_div(N, kTileN)) * ceil_div(K, kKBlock) * kPackedTileBytes;
+    return WQBMM_OK;
+}
+
+wqbmm_status wqbmm_prepack_weight(const uint8_t *w_packed, void *w_prepacked, int64_t K, int64_t N, int64_t G,
+                                  wqbmm_stream_t stream) {
+    if (!w_packed || !w_prepacked) return WQBMM_ERR_NULLPTR;
+    wqbmm_status st = check_kng(K, N, G);
+    if (st != WQBMM_OK) return st;
+    if (!aligned16(w_prepacked)) return WQBMM_ERR_INVALID;
+    int dev;
+    DeviceInfo *info;
+    if ((st = current_device(&dev, &info)) != WQBMM_OK) return st;
+    const dim3 grid(static_cast<unsigned>(ceil_div(N, kTileN)), static_cast<unsigned>(ceil_div(K, kKBlock)));
+    prepack_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        w_packed, static_cast<uint8_t *>(w_prepacked), static_cast<int>(K), static_cast<int>(N),
+        static_cast<int>(ceil_div(K, kKBlock)));
+    return cudaPeekAtLastError() == cudaSuccess ? WQBMM_OK : WQBMM_ERR_CUDA;
+}
+
+wqbmm_status wqbmm_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t G, size_t *bytes) {
+    if (!bytes) return WQBMM_ERR_NULLPTR;
+    const Shape s{M, K, N, G};
+    const wqbmm_status st = check_shape(s);
+    if (st != WQBMM_OK) return st;
+    *bytes = workspace_for(s, make_plan(s, kPlanSms));
+    return WQBMM_OK;
+}
+
+wqbmm_status wqbmm_run(const void *x, const void *w_prepacked, const void *antiquant_scale, void *y, int64_t M,
+                       int64_t K, int64_t N, int64_t G, void *workspace, size_t workspace_bytes,
+                       wqbmm_stream_t stream) {
+    if (!x || !w_prepacked || !antiquant_scale || !y) return WQBMM_ERR_NULLPTR;
+    const Shape s{M, K, N, G};
+    wqbmm_status st = check_shape(s);
+    if (st != WQBMM_OK) return st;
+    if (!aligned16(x) || !aligned16(w_prepacked) || !aligned16(antiquant_scale) || !aligned16(y))
+        return WQBMM_ERR_INVALID;
+    int dev;
+    DeviceInfo *info;
+    // the plan for this device never needs more workspace than wqbmm_workspace_bytes reports
+    const Plan worst = make_plan(s, kPlanSms);
+    if (workspace_for(s, worst) > 0 && !workspace) return WQBMM_ERR_NULLPTR;
+    if (workspace && !aligned16(workspace)) return WQBMM_ERR_INVALID;
+    if ((st = current_device(&dev, &info)) != WQBMM_OK) return st;
+    const Plan plan = make_plan(s, info->sms < kPlanSms ? info->sms : kPlanSms);
+    const size_t need = workspace_for(s, plan);
+    if (workspace_bytes < need) return WQBMM_ERR_INVALID;
+    RunParams rp{};
+    rp.x = static_cast<const __half *>(x);
+    rp.w = static_cast<const uint8_t *>(w_prepacked);
+    rp.scale = static_cast<const __half *>(antiquant_scale);
+    rp.y = static_cast<__half *>(y);
+    if (plan.splits > 1) {
+        rp.ws_part = static_cast<float *>(workspace);
+        rp.ws_count = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) +
+                                                   align256(static_cast<size_t>(plan.splits) * M * N * sizeof(float)));
+    }
+    rp.M = static_cast<int>(M);
+    rp.K = static_cast<int>(K);
+    rp.N = static_cast<int>(N);
+    rp.G = static_cast<int>(G);
+    rp.m_sub = plan.m_sub;
+    rp.n_tiles = plan.n_tiles;
+    rp.m_tiles = plan.m_tiles;
+    rp.splits = plan.splits;
+    rp.kb_total = plan.kb_total;
+    rp.dbg_group = -1;
+    return launch_plan(rp, plan, info, reinterpret_cast<cudaStream_t>(stream));
+}
+
+wqbmm_status wqbmm_debug_unfold(const void *x, int64_t M, int64_t K, int64_t G, int8_t *planes, float *amax,
+                                wqbmm_stream_t stream) {
+    if (!x || !planes || !amax) return WQBMM_ERR_NULLPTR;
+    const Shape s{M, K, 8, G};
+    wqbmm_status st = check_shape(s);
+    if (st != WQBMM_OK) return st;
+    if (!aligned16(x)) return WQBMM_ERR_INVALID;
+    int dev;
+    DeviceInfo *info;
+    if ((st = current_device(&dev, &info)) != WQBMM_OK) return st;
+    constexpr int kWarps = 4;
+    const dim3 grid(static_cast<unsigned>(M), static_cast<unsigned>(ceil_div(ceil_div(K, kKBlock), kWarps)));
+    unfold_debug_kernel<<<grid, kWarps * 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const __half *>(x), static_cast<int>(M), static_cast<int>(K), static_cast<int>(G), planes, amax);
+    return cudaPeekAtLastError() == cudaSuccess ? WQBMM_OK : WQBMM_ERR_CUDA;
+}
+
+wqbmm_status wqbmm_debug_group_partials(const void *x, const void *w_prepacked, int64_t M, int64_t K, int64_t N,
+                                        int64_t G, int64_t g, int32_t *y123, wqbmm_stream_t stream) {
+    if (!x || !w_prepacked || !y123) return WQBMM_ERR_NULLPTR;
+    const Shape s{M, K, N, G};
+    wqbmm_status st = check_shape(s);
+    if (st != WQBMM_OK) return st;
+    if (g < 0 || g >= K / G) return WQBMM_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(w_prepacked)) return WQBMM_ERR_INVALID;
+    int dev;
+    DeviceInfo *info;
+    if ((st = current_device(&dev, &info)) != WQBMM_OK) return st;
+    Plan plan = make_plan(s, info->sms);
+    plan.splits = 1;
+    RunParams rp{};
+    rp.x = static_cast<const __half *>(x);
+    rp.w = static_cast<const uint8_t *>(w_prepacked);
+    rp.dbg_y123 = y123;
+    rp.M = static_cast<int>(M);
+    rp.K = static_cast<int>(K);
+    rp.N = static_cast<int>(N);
+    rp.G = static_cast<int>(G);
+    rp.m_sub = plan.m_sub;
+    rp.n_tiles = plan.n_tiles;
+    rp.m_tiles = plan.m_tiles;
+    rp.splits = 1;
+    rp.kb_total = plan.kb_total;
+    rp.dbg_group = static_cast<int>(g);
+    return launch_plan(rp, plan, info, reinterpret_cast<cudaStream_t>(stream));
+}
+
+wqbmm_status wqbmm_read_device_status(int32_t *code, int clear, wqbmm_stream_t stream) {
+    if (!code) return WQBMM_ERR_NULLPTR;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t host = 0;
+    if (cudaMemcpyFromSymbolAsync(&host, g_status_word, sizeof(host), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return WQBMM_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return WQBMM_ERR_CUDA;
+    if (clear) {
+        const int32_t zero = 0;
+        if (cudaMemcpyToSymbolAsync(g_status_word, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s) !=
+                cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return WQBMM_ERR_CUDA;
+    }
+    *code = host;
+    return WQBMM_OK;
+}
+
+wqbmm_status wqbmm_debug_wait_timeout(int64_t limit_ns, wqbmm_stream_t stream) {
+    if (limit_ns < 1000000 || limit_ns > 2000000000) return WQBMM_ERR_INVALID;
+    int dev;
+    DeviceInfo *info;
+    wqbmm_status st = current_device(&dev, &info);
+    if (st != WQBMM_OK) return st;
+    wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(static_cast<uint64_t>(limit_ns));
+    return cudaPeekAtLastError() == cudaSuccess ? WQBMM_OK : WQBMM_ERR_CUDA;
+}
+
+}  // extern "C"
