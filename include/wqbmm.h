@@ -57,7 +57,8 @@ typedef enum {
     WQBMM_ERR_INVALID = 2,            /* a size, alignment or workspace-size rule below is broken */
     WQBMM_ERR_UNSUPPORTED_ARCH = 3,   /* the current device is not compute capability 10.3 (GB300) */
     WQBMM_ERR_CUDA = 4,               /* a CUDA runtime call failed (no device, launch failure, ...) */
-    WQBMM_ERR_DEVICE_TIMEOUT = 5      /* a kernel gave up a bounded wait (read by wqbmm_read_device_status) */
+    WQBMM_ERR_DEVICE_TIMEOUT = 5,     /* a kernel gave up a bounded wait (read by wqbmm_read_device_status) */
+    WQBMM_ERR_SCRATCH_LIMIT = 6       /* the shape needs more scratch than wqbmm_run_static_scratch holds */
 } wqbmm_status;
 
 /* Shape rules shared by the entry points that take (M, K, N, G):
@@ -140,6 +141,28 @@ WQBMM_API wqbmm_status wqbmm_read_device_status(int32_t *code, int clear, wqbmm_
  * the bounded-wait error path can be checked without a hang. Errors: INVALID, UNSUPPORTED_ARCH, CUDA.
  */
 WQBMM_API wqbmm_status wqbmm_debug_wait_timeout(int64_t limit_ns, wqbmm_stream_t stream);
+
+/*
+ * Same result as wqbmm_run, for callers that cannot allocate device memory: code whose device memory is owned by
+ * another allocator (a framework's caching pool, a plugin interface that hands over only its input and output
+ * buffers) and that therefore has no way to provide wqbmm_run's workspace. (The paper has no counterpart: this is
+ * an interface convenience, not part of the method.)
+ *   x, w_prepacked, antiquant_scale, y   as for wqbmm_run (caller-owned device memory)
+ * Scratch: the split-K partial sums and arrival counters live in one statically sized device array of 2 MiB
+ * (2097152 bytes) inside this library; every GPU that loads the library holds it until the process exits. A shape
+ * whose workspace (as reported by wqbmm_workspace_bytes) exceeds that size is rejected with
+ * WQBMM_ERR_SCRATCH_LIMIT before anything is launched.
+ * Set-up: the first call on each device looks up the array's device address (with that device current) and keeps
+ * it; make that first call before any stream capture. Nothing is allocated by any call: no cudaMalloc, no
+ * cudaFree, no allocating library routine. Each call clears the counters it uses (one cudaMemsetAsync on
+ * `stream`) and then launches the same kernel as wqbmm_run.
+ * All calls share the one array: calls whose executions overlap on the GPU (different streams, or one device
+ * used from several host threads without ordering) race on it and give wrong results. Order them on one stream.
+ * Errors: NULLPTR, INVALID, UNSUPPORTED_ARCH, CUDA, SCRATCH_LIMIT.
+ */
+WQBMM_API wqbmm_status wqbmm_run_static_scratch(const void *x, const void *w_prepacked, const void *antiquant_scale,
+                                                void *y, int64_t M, int64_t K, int64_t N, int64_t G,
+                                                wqbmm_stream_t stream);
 
 /* Static, human-readable name of a status code. */
 WQBMM_API const char *wqbmm_status_string(wqbmm_status status);

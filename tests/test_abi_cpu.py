@@ -49,7 +49,7 @@ def test_build_targets_sm_103a_only():
 
 
 def test_status_strings(lib):
-    for code in range(6):
+    for code in range(7):
         assert wq.wqbmm_status_string(code).startswith("WQBMM_")
     assert "UNKNOWN" in wq.wqbmm_status_string(99)
 
@@ -108,6 +108,11 @@ CASES = [
      INVALID),
     ("partials_negative_group", lambda L: L.wqbmm_debug_group_partials(A, A, 1, 256, 128, 128, -1, A, None),
      INVALID),
+    ("static_scratch_null_y", lambda L: L.wqbmm_run_static_scratch(A, A, A, None, 1, 128, 128, 128, None),
+     NULLPTR),
+    ("static_scratch_misaligned_x", lambda L: L.wqbmm_run_static_scratch(MIS, A, A, A, 1, 128, 128, 128, None),
+     INVALID),
+    ("static_scratch_bad_group", lambda L: L.wqbmm_run_static_scratch(A, A, A, A, 1, 128, 128, 96, None), INVALID),
     ("status_null", lambda L: L.wqbmm_read_device_status(None, 0, None), NULLPTR),
     ("timeout_limit_too_small", lambda L: L.wqbmm_debug_wait_timeout(10, None), INVALID),
     ("timeout_limit_too_large", lambda L: L.wqbmm_debug_wait_timeout(10 ** 10, None), INVALID),

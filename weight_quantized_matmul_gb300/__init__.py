@@ -15,7 +15,7 @@ __all__ = [
     "WqbmmError", "library_path", "load_library", "wqbmm_prepacked_weight_bytes", "wqbmm_prepack_weight",
     "wqbmm_workspace_bytes", "wqbmm_run", "wqbmm_debug_unfold", "wqbmm_debug_group_partials",
     "wqbmm_read_device_status", "wqbmm_debug_wait_timeout", "wqbmm_status_string", "prepack_weight",
-    "allocate_workspace", "msd_matmul", "SYMBOLS",
+    "allocate_workspace", "msd_matmul", "SYMBOLS", "wqbmm_run_static_scratch",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -23,13 +23,13 @@ _LIB_PATH = os.path.join(_PKG, "libwqbmm.so")
 _lock = threading.Lock()
 _lib = None
 
-OK, ERR_NULLPTR, ERR_INVALID, ERR_UNSUPPORTED_ARCH, ERR_CUDA, ERR_DEVICE_TIMEOUT = range(6)
+OK, ERR_NULLPTR, ERR_INVALID, ERR_UNSUPPORTED_ARCH, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_SCRATCH_LIMIT = range(7)
 
 # every entry point include/wqbmm.h declares
 SYMBOLS = (
     "wqbmm_prepacked_weight_bytes", "wqbmm_prepack_weight", "wqbmm_workspace_bytes", "wqbmm_run",
     "wqbmm_debug_unfold", "wqbmm_debug_group_partials", "wqbmm_read_device_status", "wqbmm_debug_wait_timeout",
-    "wqbmm_status_string",
+    "wqbmm_status_string", "wqbmm_run_static_scratch",
 )
 
 
@@ -63,6 +63,7 @@ def load_library():
                 "wqbmm_debug_group_partials": [p, p, i64, i64, i64, i64, i64, p, p],
                 "wqbmm_read_device_status": [ctypes.POINTER(ctypes.c_int32), ctypes.c_int, p],
                 "wqbmm_debug_wait_timeout": [i64, p],
+                "wqbmm_run_static_scratch": [p, p, p, p, i64, i64, i64, i64, p],
             }
             for name, args in sig.items():
                 f = getattr(lib, name)
@@ -123,6 +124,15 @@ def wqbmm_run(x, w_prepacked, antiquant_scale, y, M: int, K: int, N: int, G: int
         workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load_library().wqbmm_run(_ptr(x), _ptr(w_prepacked), _ptr(antiquant_scale), _ptr(y), M, K, N, G,
                                      _ptr(workspace), workspace_bytes, _stream(stream)), "wqbmm_run")
+
+
+def wqbmm_run_static_scratch(x, w_prepacked, antiquant_scale, y, M: int, K: int, N: int, G: int,
+                             stream=None) -> None:
+    """wqbmm_run without a caller workspace: the library's fixed 2 MiB device scratch is used instead (for callers
+    that cannot allocate device memory). Calls must not overlap on the GPU; the first call on a device looks up the
+    scratch address and should come before any stream capture."""
+    _check(load_library().wqbmm_run_static_scratch(_ptr(x), _ptr(w_prepacked), _ptr(antiquant_scale), _ptr(y), M, K,
+                                                    N, G, _stream(stream)), "wqbmm_run_static_scratch")
 
 
 def wqbmm_debug_unfold(x, M: int, K: int, G: int, planes, amax, stream=None) -> None:

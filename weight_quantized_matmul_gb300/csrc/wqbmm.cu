@@ -130,6 +130,25 @@ wqbmm_status launch_plan(const RunParams &rp, const Plan &plan, DeviceInfo *info
     }
 }
 
+// Scratch for wqbmm_run_static_scratch: a fixed device array instead of a caller workspace. Host code must not
+// pass the symbol itself to a kernel (on the host it only names a stand-in); the device address of this array on
+// each device is looked up once with cudaGetSymbolAddress and kept in g_scratch_addr.
+constexpr size_t kStaticScratchBytes = size_t(2) << 20;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+void *g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on `dev` (the current device), found on the first call for that device.
+wqbmm_status static_scratch_address(int dev, void **addr) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return WQBMM_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *addr = g_scratch_addr[dev];
+    return WQBMM_OK;
+}
+
 }  // namespace
 }  // namespace wqbmm
 
@@ -145,6 +164,8 @@ const char *wqbmm_status_string(wqbmm_status status) {
         case WQBMM_ERR_UNSUPPORTED_ARCH: return "WQBMM_ERR_UNSUPPORTED_ARCH: device is not compute capability 10.3";
         case WQBMM_ERR_CUDA: return "WQBMM_ERR_CUDA: a CUDA runtime call failed";
         case WQBMM_ERR_DEVICE_TIMEOUT: return "WQBMM_ERR_DEVICE_TIMEOUT: a kernel gave up a bounded wait";
+        case WQBMM_ERR_SCRATCH_LIMIT:
+            return "WQBMM_ERR_SCRATCH_LIMIT: the shape needs more than the 2 MiB static scratch";
     }
     return "WQBMM_ERR_UNKNOWN";
 }
@@ -222,6 +243,50 @@ wqbmm_status wqbmm_run(const void *x, const void *w_prepacked, const void *antiq
     rp.kb_total = plan.kb_total;
     rp.dbg_group = -1;
     return launch_plan(rp, plan, info, reinterpret_cast<cudaStream_t>(stream));
+}
+
+wqbmm_status wqbmm_run_static_scratch(const void *x, const void *w_prepacked, const void *antiquant_scale, void *y,
+                                      int64_t M, int64_t K, int64_t N, int64_t G, wqbmm_stream_t stream) {
+    if (!x || !w_prepacked || !antiquant_scale || !y) return WQBMM_ERR_NULLPTR;
+    const Shape s{M, K, N, G};
+    wqbmm_status st = check_shape(s);
+    if (st != WQBMM_OK) return st;
+    if (!aligned16(x) || !aligned16(w_prepacked) || !aligned16(antiquant_scale) || !aligned16(y))
+        return WQBMM_ERR_INVALID;
+    int dev;
+    DeviceInfo *info;
+    if ((st = current_device(&dev, &info)) != WQBMM_OK) return st;
+    const Plan plan = make_plan(s, info->sms < kPlanSms ? info->sms : kPlanSms);
+    const size_t need = workspace_for(s, plan);
+    if (need > kStaticScratchBytes) return WQBMM_ERR_SCRATCH_LIMIT;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    RunParams rp{};
+    if (plan.splits > 1) {
+        void *base = nullptr;
+        if ((st = static_scratch_address(dev, &base)) != WQBMM_OK) return st;
+        const size_t counters_at = align256(static_cast<size_t>(plan.splits) * M * N * sizeof(float));
+        const size_t counters_bytes = static_cast<size_t>(plan.m_tiles) * plan.n_tiles * sizeof(uint32_t);
+        // the array keeps whatever the previous call (of any shape) left there: the counters must start at zero
+        if (cudaMemsetAsync(static_cast<uint8_t *>(base) + counters_at, 0, counters_bytes, cs) != cudaSuccess)
+            return WQBMM_ERR_CUDA;
+        rp.ws_part = static_cast<float *>(base);
+        rp.ws_count = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(base) + counters_at);
+    }
+    rp.x = static_cast<const __half *>(x);
+    rp.w = static_cast<const uint8_t *>(w_prepacked);
+    rp.scale = static_cast<const __half *>(antiquant_scale);
+    rp.y = static_cast<__half *>(y);
+    rp.M = static_cast<int>(M);
+    rp.K = static_cast<int>(K);
+    rp.N = static_cast<int>(N);
+    rp.G = static_cast<int>(G);
+    rp.m_sub = plan.m_sub;
+    rp.n_tiles = plan.n_tiles;
+    rp.m_tiles = plan.m_tiles;
+    rp.splits = plan.splits;
+    rp.kb_total = plan.kb_total;
+    rp.dbg_group = -1;
+    return launch_plan(rp, plan, info, cs);
 }
 
 wqbmm_status wqbmm_debug_unfold(const void *x, int64_t M, int64_t K, int64_t G, int8_t *planes, float *amax,
