@@ -61,8 +61,11 @@ def test_prepacked_weight_bytes():
 
 
 def test_workspace_bytes():
-    # decode: 32 column tiles split over K (sized for up to 160 SMs, two CTAs each: 10 slices)
-    assert wq.wqbmm_workspace_bytes(1, 4096, 4096, 128) == 10 * 4096 * 4 + 256
+    # decode: 32 column tiles split over K into 8 slices that reduce inside a thread-block cluster: no workspace
+    assert wq.wqbmm_workspace_bytes(1, 4096, 4096, 128) == 0
+    # two column tiles and a long K: 160 slices (sized for up to 160 SMs, two CTAs each) reduce through the
+    # workspace: 160 x 1 x 256 fp32 partial sums + one 256-byte block of counters
+    assert wq.wqbmm_workspace_bytes(1, 65536, 256, 128) == 160 * 256 * 4 + 256
     # enough tiles to fill the GPU: no split, no workspace
     assert wq.wqbmm_workspace_bytes(2048, 8192, 28672, 64) == 0
     assert wq.wqbmm_workspace_bytes(128, 5120, 13824, 128) == 0
@@ -88,7 +91,7 @@ CASES = [
     ("run_null_w", lambda L: L.wqbmm_run(A, None, A, A, 1, 128, 128, 128, A, 1 << 20, None), NULLPTR),
     ("run_null_scale", lambda L: L.wqbmm_run(A, A, None, A, 1, 128, 128, 128, A, 1 << 20, None), NULLPTR),
     ("run_null_y", lambda L: L.wqbmm_run(A, A, A, None, 1, 128, 128, 128, A, 1 << 20, None), NULLPTR),
-    ("run_null_workspace_needed", lambda L: L.wqbmm_run(A, A, A, A, 1, 4096, 4096, 128, None, 0, None), NULLPTR),
+    ("run_null_workspace_needed", lambda L: L.wqbmm_run(A, A, A, A, 1, 65536, 256, 128, None, 0, None), NULLPTR),
     ("run_zero_m", lambda L: L.wqbmm_run(A, A, A, A, 0, 128, 128, 128, A, 1 << 20, None), INVALID),
     ("run_negative_k", lambda L: L.wqbmm_run(A, A, A, A, 1, -128, 128, 128, A, 1 << 20, None), INVALID),
     ("run_k_not_multiple_of_group", lambda L: L.wqbmm_run(A, A, A, A, 1, 160, 128, 128, A, 1 << 20, None),
@@ -100,7 +103,7 @@ CASES = [
     ("run_misaligned_y", lambda L: L.wqbmm_run(A, A, A, MIS, 1, 128, 128, 128, A, 1 << 20, None), INVALID),
     ("run_misaligned_scale", lambda L: L.wqbmm_run(A, A, MIS, A, 1, 128, 128, 128, A, 1 << 20, None), INVALID),
     ("run_misaligned_weights", lambda L: L.wqbmm_run(A, MIS, A, A, 1, 128, 128, 128, A, 1 << 20, None), INVALID),
-    ("run_misaligned_workspace", lambda L: L.wqbmm_run(A, A, A, A, 1, 4096, 4096, 128, MIS, 1 << 20, None),
+    ("run_misaligned_workspace", lambda L: L.wqbmm_run(A, A, A, A, 1, 65536, 256, 128, MIS, 1 << 20, None),
      INVALID),
     ("unfold_null_planes", lambda L: L.wqbmm_debug_unfold(A, 1, 128, 128, None, A, None), NULLPTR),
     ("unfold_bad_group", lambda L: L.wqbmm_debug_unfold(A, 1, 128, 100, A, A, None), INVALID),

@@ -131,6 +131,31 @@ def test_unfold_bit_exact_special_values(dev, G):
     np.testing.assert_array_equal(amax.cpu().numpy(), a_ref.astype(np.float32))
 
 
+def test_unfold_bit_exact_every_fp16_value(dev):
+    """Every finite fp16 x against 64 values of A_max (each group holds A_max and 127 values with |x| <= A_max),
+    bit-exact against the oracle's binary32 unfold: the quotient step is exact over the whole domain."""
+    allv = np.arange(65536, dtype=np.uint32).astype(np.uint16).view(np.float16)
+    fin = allv[np.isfinite(allv)]
+    pos = np.sort(fin[fin > 0].astype(np.float64))
+    pick = np.unique(np.concatenate([pos[np.linspace(0, pos.size - 1, 60).astype(int)],
+                                     [5.960464477539063e-08, 6.103515625e-05, 1.0, 65504.0]]))[:64]
+    G, K = 128, 65536
+    rows = []
+    for a in pick:
+        vals = fin[np.abs(fin.astype(np.float64)) <= a]
+        reps = -(-(K // G * (G - 1)) // vals.size)
+        body = np.tile(vals, reps)[:K // G * (G - 1)].reshape(K // G, G - 1)
+        rows.append(np.concatenate([np.full((K // G, 1), a, dtype=np.float16), body], axis=1).reshape(-1))
+    x = np.stack(rows).astype(np.float16)
+    M = x.shape[0]
+    planes = torch.empty((3, M, K), dtype=torch.int8, device=dev)
+    amax = torch.empty((M, K // G), dtype=torch.float32, device=dev)
+    wq.wqbmm_debug_unfold(to_dev(x, dev), M, K, G, planes, amax)
+    p_ref, a_ref = oracle.unfold(x, G, oracle.MODE_F)
+    np.testing.assert_array_equal(amax.cpu().numpy(), a_ref.astype(np.float32))
+    np.testing.assert_array_equal(planes.cpu().numpy(), p_ref)
+
+
 # ------------------------------------------------------------------------------------------- step 9
 
 PARTIAL_CASES = [
@@ -188,6 +213,8 @@ RUN_CASES = [
     (17, 640, 392, 64, "normal", "u8", 0.005, 0.02),
     (40, 1280, 520, 128, "t3_clip60", "u8", 0.002, 0.03),
     (130, 512, 256, 64, "normal", "u8", 0.005, 0.02),
+    (1, 65536, 256, 128, "normal", "u8", 0.005, 0.02),     # 160-way split-K through the workspace
+    (4, 4096, 1024, 128, "t3_clip60", "u8", -0.5, 0.5),    # 8 column tiles x 8 cluster slices
 ]
 
 
@@ -212,26 +239,28 @@ def test_run_zero_and_constant_rows(dev):
     assert_within_tolerance(y, oracle.msd_matmul(x, wp, sc, G), "special rows")
 
 
-def test_run_deterministic_and_workspace_left_clean(dev):
-    wl = I.WORKLOADS["decode_m1_k4096_n4096"]
+@pytest.mark.parametrize("wl", [I.WORKLOADS["decode_m1_k4096_n4096"],                  # cluster-reduced split-K
+                                I.small_case(3, 16384, 520, 64, seed=8)])              # workspace split-K
+def test_run_deterministic_and_workspace_left_clean(dev, wl):
     x, wp, sc = I.make_inputs(wl)
     xd, sd = to_dev(x, dev), to_dev(sc, dev)
     w_pre = wq.prepack_weight(to_dev(wp, dev), wl.K, wl.N, wl.G)
     ws = wq.allocate_workspace(wl.M, wl.K, wl.N, wl.G, dev)
-    assert ws is not None
     outs = []
     for _ in range(3):
         y = torch.empty((wl.M, wl.N), dtype=torch.float16, device=dev)
         wq.wqbmm_run(xd, w_pre, sd, y, wl.M, wl.K, wl.N, wl.G, ws)
         outs.append(y.cpu().numpy().view(np.uint16))
     assert all(np.array_equal(outs[0], o) for o in outs[1:])
-    # the arrival counters sit after the partial sums; all must be back at zero
-    counters = ws.cpu().numpy()[-256:].view(np.uint32)
-    assert not counters.any()
+    assert_within_tolerance(outs[0].view(np.float16), oracle.msd_matmul(x, wp, sc, wl.G), wl.name)
+    if ws is not None:
+        # the arrival counters sit after the partial sums; all must be back at zero
+        counters = ws.cpu().numpy()[-256:].view(np.uint32)
+        assert not counters.any()
 
 
 def test_run_errors_leave_output_untouched(dev):
-    M, K, N, G = 1, 4096, 4096, 128
+    M, K, N, G = 1, 65536, 256, 128
     x, wp, sc = I.make_inputs(I.small_case(M, K, N, G, seed=5))
     xd, sd = to_dev(x, dev), to_dev(sc, dev)
     w_pre = wq.prepack_weight(to_dev(wp, dev), K, N, G)

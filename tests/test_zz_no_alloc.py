@@ -39,8 +39,15 @@ def dev():
     return torch.device("cuda:0")
 
 
+# shapes whose split over K goes through the scratch (more K-slices than one thread-block cluster holds)
+SHAPES = {
+    "long_k_m1_k65536_n256": I.small_case(1, 65536, 256, 128, seed=11),
+    "m3_k16384_n520_g64": I.small_case(3, 16384, 520, 64, seed=12),
+}
+
+
 def device_problem(name, dev):
-    wl = I.WORKLOADS[name]
+    wl = SHAPES[name]
     x, wp, sc = I.make_inputs(wl)
     xd = torch.from_numpy(x).to(dev)
     sd = torch.from_numpy(sc).to(dev)
@@ -55,8 +62,8 @@ def reference_run(wl, xd, w_pre, sd, dev):
     return y.cpu().numpy()
 
 
-@pytest.mark.parametrize("order", [("decode_m1_k4096_n4096", "decode_m1_k4096_n4096", "pr1_m16_k1024_n1024"),
-                                   ("pr1_m16_k1024_n1024", "decode_m1_k4096_n4096", "pr1_m16_k1024_n1024")])
+@pytest.mark.parametrize("order", [("long_k_m1_k65536_n256", "long_k_m1_k65536_n256", "m3_k16384_n520_g64"),
+                                   ("m3_k16384_n520_g64", "long_k_m1_k65536_n256", "m3_k16384_n520_g64")])
 def test_static_scratch_matches_run_on_calls_in_a_row(dev, order):
     problems = {name: device_problem(name, dev) for name in set(order)}
     refs = {name: reference_run(*problems[name], dev) for name in problems}
@@ -72,8 +79,8 @@ def test_static_scratch_matches_run_on_calls_in_a_row(dev, order):
 
 
 def test_static_scratch_refuses_shapes_beyond_its_size(dev):
-    # 148 column tiles of 16 rows split over K twice: 2 x 16 x 18944 fp32 partial sums = 2.4 MB > 2 MiB
-    M, K, N, G = 16, 4096, 18944, 128
+    # 16 column tiles of 16 rows split over K 19 times: 19 x 16 x 2048 fp32 partial sums = 2.5 MB > 2 MiB
+    M, K, N, G = 16, 4096, 2048, 128
     assert wq.wqbmm_workspace_bytes(M, K, N, G) > 2 * 1024 * 1024
     x = torch.zeros((M, K), dtype=torch.float16, device=dev)
     s = torch.zeros((K // G, N), dtype=torch.float16, device=dev)

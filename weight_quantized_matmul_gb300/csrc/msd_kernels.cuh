@@ -10,15 +10,21 @@
 // M side is 128 weight columns (so TMEM lane = output column n), its N side is the three stacked residual planes
 // of the row tile (NMMA = 16, 32 or 48 stacked rows), one MMA chain per K-group restarted at every group so the
 // integer partial sums stay exact in FP32. Roles inside a CTA (320 threads):
-//   warp 0      TMA producer: bulk-copies packed weight tiles (8 KB per 128 k) into a 4-stage ring
+//   warp 0      TMA producer: per 128 k, one bulk copy of the packed weight tile (8 KB) plus 2-D tensor copies of
+//               the x tile and the scale tile, into a ring deep enough to hold a decode CTA's whole K-slice
 //   warp 1      TMEM owner and single-thread MMA issuer (tcgen05.mma kind::f8f6f4, E4M3 x E4M3 -> F32)
-//   warps 2-5   weight converters: int4 (offset binary) -> E4M3 bytes in the 128-byte-swizzled K-major layout
-//   warps 6-9   unfold (A_max, three planes as E4M3, per-group constants) one k-block ahead, then the epilogue:
-//               TMEM -> registers, Y_i = D_i - 8 S_i folded into the combine, scale, accumulate over groups
+//   warps 2-5   operand builders, per k-block: int4 (offset binary) -> E4M3 weights in the 128-byte-swizzled
+//               K-major layout, then the unfold of the x tile (A_max, three planes as E4M3, per-group constants,
+//               the scale column of each thread), rows rotating over the warps from one k-block to the next
+//   warps 6-9   epilogue: TMEM -> registers, Y_i = D_i - 8 S_i folded into the combine, scale, accumulate
+// Split-K (when there are too few column tiles to fill the GPU): up to 8 K-slices of a tile form a thread-block
+// cluster and reduce through distributed shared memory; more slices reduce through a global workspace. Either way
+// the slices are summed in slice order, so the result does not depend on timing.
 // Weights are stored as u = w + 8 in [0, 15] so that the int4 -> E4M3 conversion is two byte permutes and an OR;
 // the MMA then yields D_i = sum A_i u = Y_i + 8 S_i with S_i = sum A_i over the group, removed in the combine.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 
 #include <cstdint>
@@ -31,9 +37,8 @@ constexpr int kTileN = 128;                          // output columns per CTA (
 constexpr int kKBlock = 128;                         // k per pipeline stage (one 128-byte E4M3 swizzle row)
 constexpr int kPackedTileBytes = kTileN * kKBlock / 2;  // 8192
 constexpr int kATileBytes = kTileN * kKBlock;        // 16384
-constexpr int kPStages = 4;                          // packed weight ring
 constexpr int kCStages = 3;                          // converted weights / planes / constants ring
-constexpr int kLookahead = kCStages - 1;             // unfold runs this many k-blocks ahead of the epilogue
+constexpr int kSmemBudget = 110 * 1024;              // per CTA, so that two CTAs share an SM
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
@@ -44,7 +49,8 @@ constexpr int kNumEpiWarps = 4;
 constexpr int kEpiBarrierId = 1;
 constexpr int kMaxGroupsPerKBlock = kKBlock / 32;
 constexpr int kConstFloatsPerGroup = 8 * 16;          // a1 a2 a3 corr S1 S2 S3 (pad) x 16 rows
-constexpr int kConstStageFloats = kMaxGroupsPerKBlock * kConstFloatsPerGroup;
+constexpr int kScaleFloatsOffset = kMaxGroupsPerKBlock * kConstFloatsPerGroup;   // then scale[group][128 columns]
+constexpr int kConstStageFloats = kScaleFloatsOffset + kMaxGroupsPerKBlock * kTileN;
 
 // Method constants (page section 4.1): unfold factors and the combine weights 1/7.49, 1/(7.49*14.98), ...
 constexpr float kF1 = 7.49f;
@@ -72,15 +78,24 @@ struct Cfg {
     static constexpr int kBufStride = NMMA <= 16 ? 16 : (NMMA <= 32 ? 32 : 64);   // TMEM columns per buffer
     static constexpr int kTmemCols = 2 * kBufStride < 32 ? 32 : 2 * kBufStride;
     static constexpr int kBTileBytes = NMMA * kKBlock;
+    // one load stage: packed weights, the x tile (rows x 128 k, fp16) and the scale tile (groups x 128 n, fp16)
+    static constexpr int kXOff = kPackedTileBytes;
+    static constexpr int kSOff = kXOff + kMaxM * kKBlock * 2;
+    static constexpr int kStageBytes = kSOff + kMaxGroupsPerKBlock * kTileN * 2;
     // shared memory carve-up (offsets from a 1024-byte aligned base)
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kCStages * kATileBytes;
-    static constexpr int kOffP = kOffB + kCStages * kBTileBytes;
-    static constexpr int kOffConst = kOffP + kPStages * kPackedTileBytes;
-    static constexpr int kOffBar = kOffConst + kCStages * kConstStageFloats * 4;
+    static constexpr int kOffConst = kOffB + kCStages * kBTileBytes;
+    static constexpr int kOffP = kOffConst + kCStages * kConstStageFloats * 4;
+    static constexpr int kFixedBytes = kOffP + 1024 + 256;         // + alignment slack, barriers, flags
+    // as many load stages as fit in the budget that keeps two CTAs per SM (at least 3, at most 8)
+    static constexpr int kPStagesFit = (kSmemBudget - kFixedBytes - 16 * 8) / kStageBytes;
+    static constexpr int kPStages = kPStagesFit < 3 ? 3 : (kPStagesFit > 8 ? 8 : kPStagesFit);
+    static constexpr int kOffBar = kOffP + kPStages * kStageBytes;
     static constexpr int kNumBars = 2 * kPStages + 3 * kCStages + 4;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 64 + 1024;       // + alignment slack
+    static_assert(kStageBytes % 128 == 0, "TMA destinations must stay 128-byte aligned");
 };
 
 struct RunParams {
@@ -93,22 +108,33 @@ struct RunParams {
     int32_t *dbg_y123;          // [3, M, N] integer partials of group dbg_group (debug mode), else null
     int M, K, N, G;
     int m_sub, n_tiles, m_tiles, splits, kb_total;
+    int reduce;                 // kReduceNone, kReduceCluster (splits <= 8, cluster along z) or kReduceGlobal
     int dbg_group;              // -1 in normal runs
 };
+
+constexpr int kReduceNone = 0, kReduceCluster = 1, kReduceGlobal = 2;
+constexpr int kMaxClusterSplits = 8;
 
 // ------------------------------------------------------------------------------------------------ unfold
 
 // Steps 2-7 for four values of one group, IEEE binary32 with every operation rounded on its own (no contraction);
-// rintf rounds half to even. A group whose A_max is 0 gives zero planes.
+// rintf rounds half to even. A group whose A_max is 0 holds only zeros; dividing those by 1 gives zero planes, so no
+// branch is needed.
+// The quotient tmp1 = RN(RN(7.49f x) / A_max) is formed from the correctly rounded reciprocal r = RN(1/A_max),
+// shared by the whole group: q0 = RN(n r), the exact residual e = n - q0 A_max (one fused multiply-add) and
+// q = RN(q0 + e r), the final correction step of Markstein's division sequences (P. Markstein, "IA-64 and Elementary
+// Functions", 2000). Over the whole input domain (every finite fp16 x with every fp16 A_max >= |x|, 1,007,713,278
+// pairs) it was checked on the GPU to equal the IEEE quotient bit for bit; it has no branch, so the four quotients
+// of a lane overlap.
 __device__ __forceinline__ void msd_unfold4(const float (&x)[4], float amax, float (&a1)[4], float (&a2)[4],
                                             float (&a3)[4]) {
+    const float den = amax == 0.0f ? 1.0f : amax;
+    const float rcp = __frcp_rn(den);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        if (amax == 0.0f) {
-            a1[j] = a2[j] = a3[j] = 0.0f;
-            continue;
-        }
-        const float t1 = __fdiv_rn(__fmul_rn(kF1, x[j]), amax);
+        const float n = __fmul_rn(kF1, x[j]);
+        const float q0 = __fmul_rn(n, rcp);
+        const float t1 = __fmaf_rn(__fmaf_rn(-q0, den, n), rcp, q0);
         const float r1 = rintf(t1);
         const float t2 = __fmul_rn(__fsub_rn(t1, r1), kF2);
         const float r2 = rintf(t2);
@@ -134,12 +160,15 @@ __device__ __forceinline__ void load_x4(const __half *x, int M, int K, int row, 
     }
 }
 
-// Max / sum over the lanes that share one group: a group spans G/4 consecutive lanes (4 values per lane).
-__device__ __forceinline__ float group_max(float v, int lanes_per_group) {
+// Max of non-negative values / integer sum over the lanes that share one group: a group spans G/4 consecutive lanes
+// (4 values per lane). A whole-warp group uses one redux instruction (non-negative floats order like their bits).
+__device__ __forceinline__ float group_absmax(float v, int lanes_per_group) {
+    if (lanes_per_group == 32) return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
     for (int off = 1; off < lanes_per_group; off <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
     return v;
 }
-__device__ __forceinline__ float group_sum(float v, int lanes_per_group) {
+__device__ __forceinline__ int group_isum(int v, int lanes_per_group) {
+    if (lanes_per_group == 32) return __reduce_add_sync(0xffffffffu, v);
     for (int off = 1; off < lanes_per_group; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
     return v;
 }
@@ -198,7 +227,7 @@ __global__ void unfold_debug_kernel(const __half *__restrict__ x, int M, int K, 
     load_x4(x, M, K, row, kbase, v);
     const int lpg = G / 4;
     float am = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-    am = group_max(am, lpg);
+    am = group_absmax(am, lpg);
     float a1[4], a2[4], a3[4];
     msd_unfold4(v, am, a1, a2, a3);
     if (!valid) return;
@@ -229,10 +258,80 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns) {
     }
 }
 
+// Unfold of R (1 or 2) rows of one 128-k block by one warp, interleaved for instruction-level parallelism: planes as
+// E4M3 into the B tile (plane i of row m at row i * kMaxM + m), per-group constants c_i A_max, the offset-binary
+// correction 8 sum_i c_i A_max S_i and the plane sums S_i into the constant slot.
+template <int kMaxM, int R>
+__device__ __forceinline__ void unfold_rows(const __half *xs, uint8_t *bt, float *cst, const int (&rows)[R], int lpg,
+                                            int lane) {
+    const int kbyte = lane * 4;
+    float v[R][4];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const uint2 raw = *reinterpret_cast<const uint2 *>(xs + rows[r] * kKBlock + kbyte);
+        const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
+        const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+        v[r][0] = f01.x;
+        v[r][1] = f01.y;
+        v[r][2] = f23.x;
+        v[r][3] = f23.y;
+    }
+    float am[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        am[r] = group_absmax(fmaxf(fmaxf(fabsf(v[r][0]), fabsf(v[r][1])), fmaxf(fabsf(v[r][2]), fabsf(v[r][3]))),
+                             lpg);
+    float a1[R][4], a2[R][4], a3[R][4];
+#pragma unroll
+    for (int r = 0; r < R; ++r) msd_unfold4(v[r], am[r], a1[r], a2[r], a3[r]);
+    // plane sums of a lane (each in [-28, 28]): planes 1 and 2 packed in one word so one reduction serves both
+    // (11-bit fields hold lane sums + 28, at most 32 * 56 = 1792 < 2048 over a whole-warp group), plane 3 alone
+    int packed[R], sum3[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int p1 = __float2int_rn((a1[r][0] + a1[r][1]) + (a1[r][2] + a1[r][3])) + 28;
+        const int p2 = __float2int_rn((a2[r][0] + a2[r][1]) + (a2[r][2] + a2[r][3])) + 28;
+        packed[r] = p1 | (p2 << 11);
+        sum3[r] = __float2int_rn((a3[r][0] + a3[r][1]) + (a3[r][2] + a3[r][3]));
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        packed[r] = group_isum(packed[r], lpg);
+        sum3[r] = group_isum(sum3[r], lpg);
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int m = rows[r];
+        *reinterpret_cast<uint32_t *>(bt + sw128_offset(m, kbyte)) =
+            e4m3x2(a1[r][1], a1[r][0]) | (e4m3x2(a1[r][3], a1[r][2]) << 16);
+        *reinterpret_cast<uint32_t *>(bt + sw128_offset(kMaxM + m, kbyte)) =
+            e4m3x2(a2[r][1], a2[r][0]) | (e4m3x2(a2[r][3], a2[r][2]) << 16);
+        *reinterpret_cast<uint32_t *>(bt + sw128_offset(2 * kMaxM + m, kbyte)) =
+            e4m3x2(a3[r][1], a3[r][0]) | (e4m3x2(a3[r][3], a3[r][2]) << 16);
+        if ((lane & (lpg - 1)) == 0) {
+            const int bias = 28 * lpg;
+            const float s1 = static_cast<float>((packed[r] & 0x7FF) - bias);
+            const float s2 = static_cast<float>(((packed[r] >> 11) & 0x7FF) - bias);
+            const float s3 = static_cast<float>(sum3[r]);
+            float *cg = cst + (lane / lpg) * kConstFloatsPerGroup;
+            const float c1 = kC1 * am[r], c2 = kC2 * am[r], c3 = kC3 * am[r];
+            cg[0 * 16 + m] = c1;
+            cg[1 * 16 + m] = c2;
+            cg[2 * 16 + m] = c3;
+            cg[3 * 16 + m] = 8.0f * (c1 * s1 + c2 * s2 + c3 * s3);
+            cg[4 * 16 + m] = s1;
+            cg[5 * 16 + m] = s2;
+            cg[6 * 16 + m] = s3;
+        }
+    }
+}
+
 template <int NMMA>
-__global__ void __launch_bounds__(kThreads, 2) msd_kernel(const RunParams p) {
+__global__ void __launch_bounds__(kThreads, 2)
+    msd_kernel(const RunParams p, const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_s) {
     using C = Cfg<NMMA>;
     constexpr int kMaxM = C::kMaxM;
+    constexpr int kPStages = C::kPStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *a_ring = smem + C::kOffA;
@@ -240,12 +339,15 @@ __global__ void __launch_bounds__(kThreads, 2) msd_kernel(const RunParams p) {
     uint8_t *p_ring = smem + C::kOffP;
     float *const_ring = reinterpret_cast<float *>(smem + C::kOffConst);
     const uint32_t bar0 = smem_addr(smem + C::kOffBar);
-    // barrier addresses: full_p[P] empty_p[P] full_a[C] full_b[C] empty_o[C] full_t[2] empty_t[2]
+    // barriers: full_p / empty_p  load stage landed / released by the operand builders
+    //           full_o / empty_o  operand slot (A, B, constants) built / consumed by the MMAs
+    //           cempty            constant slot released by the epilogue
+    //           full_t / empty_t  TMEM accumulator buffer written by the MMAs / read by the epilogue
     auto full_p = [&](int s) { return bar0 + 8u * s; };
     auto empty_p = [&](int s) { return bar0 + 8u * (kPStages + s); };
-    auto full_a = [&](int c) { return bar0 + 8u * (2 * kPStages + c); };
-    auto full_b = [&](int c) { return bar0 + 8u * (2 * kPStages + kCStages + c); };
-    auto empty_o = [&](int c) { return bar0 + 8u * (2 * kPStages + 2 * kCStages + c); };
+    auto full_o = [&](int c) { return bar0 + 8u * (2 * kPStages + c); };
+    auto empty_o = [&](int c) { return bar0 + 8u * (2 * kPStages + kCStages + c); };
+    auto cempty = [&](int c) { return bar0 + 8u * (2 * kPStages + 2 * kCStages + c); };
     auto full_t = [&](int b) { return bar0 + 8u * (2 * kPStages + 3 * kCStages + b); };
     auto empty_t = [&](int b) { return bar0 + 8u * (2 * kPStages + 3 * kCStages + 2 + b); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
@@ -256,8 +358,10 @@ __global__ void __launch_bounds__(kThreads, 2) msd_kernel(const RunParams p) {
     const int nt = blockIdx.x, mt = blockIdx.y, sp = blockIdx.z;
     const int M = p.M, K = p.K, N = p.N, G = p.G;
     const int m0 = mt * p.m_sub;
+    const int gpk = kKBlock / G;                         // groups per k-block
+    const bool debug = p.dbg_group >= 0;
     int kb0, kb1;
-    if (p.dbg_group >= 0) {
+    if (debug) {
         kb0 = p.dbg_group * G / kKBlock;
         kb1 = kb0 + 1;
     } else {
@@ -266,16 +370,32 @@ __global__ void __launch_bounds__(kThreads, 2) msd_kernel(const RunParams p) {
     }
     const int nkb = kb1 - kb0;
 
-    // ---- set-up: barriers, TMEM, zeroed plane tiles (rows past the row tile must read as zero)
+    // One load stage: the k-block's packed weight tile, x tile and scale tile, all counted on full_p(s).
+    const uint8_t *w_src = p.w + (static_cast<size_t>(nt) * p.kb_total + kb0) * kPackedTileBytes;
+    const uint32_t stage_tx = kPackedTileBytes + p.m_sub * kKBlock * 2 + (debug ? 0 : gpk * kTileN * 2);
+    auto issue_stage = [&](int i, uint64_t stream_policy, uint64_t keep_policy) {
+        const int s = i % kPStages;
+        const uint32_t dst = smem_addr(p_ring + s * C::kStageBytes);
+        const int kb = kb0 + i;
+        mbar_arrive_expect_tx(full_p(s), stage_tx);
+        bulk_g2s(dst, w_src + static_cast<size_t>(i) * kPackedTileBytes, kPackedTileBytes, full_p(s), stream_policy);
+        tma_load_2d(dst + C::kXOff, &tmap_x, kb * kKBlock, m0, full_p(s), keep_policy);
+        if (!debug) tma_load_2d(dst + C::kSOff, &tmap_s, nt * kTileN, kb * gpk, full_p(s), keep_policy);
+    };
+
+    // ---- set-up. Thread 0 initialises the barriers and at once starts the loads of the first ring's worth of
+    // k-blocks (the slots are free), so the memory latency overlaps the rest of the set-up.
+    const int first_loads = nkb < kPStages ? nkb : kPStages;
+    uint64_t stream_policy = 0, keep_policy = 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kPStages; ++s) {
             mbar_init(full_p(s), 1);
             mbar_init(empty_p(s), kNumConvWarps);
         }
         for (int c = 0; c < kCStages; ++c) {
-            mbar_init(full_a(c), kNumConvWarps);
-            mbar_init(full_b(c), kNumEpiWarps);
+            mbar_init(full_o(c), kNumConvWarps);
             mbar_init(empty_o(c), 1);
+            mbar_init(cempty(c), kNumEpiWarps);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(full_t(b), 1);
@@ -284,6 +404,9 @@ __global__ void __launch_bounds__(kThreads, 2) msd_kernel(const RunParams p) {
         *abort_flag = 0;
         *last_flag = 0;
         mbar_fence_init();
+        stream_policy = l2_policy_evict_first();    // weights: read once per call
+        keep_policy = l2_policy_evict_last();       // x and scale tiles: shared by many CTAs
+        for (int i = 0; i < first_loads; ++i) issue_stage(i, stream_policy, keep_policy);
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
@@ -300,16 +423,11 @@ __global__ void __launch_bounds__(kThreads, 2) msd_kernel(const RunParams p) {
     if (warp == kProducerWarp) {
         // ================================================================ TMA producer
         if (lane == 0) {
-            const uint64_t policy = l2_policy_evict_first();
-            const uint8_t *src = p.w + (static_cast<size_t>(nt) * p.kb_total + kb0) * kPackedTileBytes;
-            int issued = 0;
+            int issued = first_loads;
             for (; issued < nkb; ++issued) {
                 const int s = issued % kPStages;
-                const uint32_t ph = (issued / kPStages) & 1;
-                if (!mbar_wait(empty_p(s), ph ^ 1, abort_flag, kSiteProducerEmpty)) break;
-                mbar_arrive_expect_tx(full_p(s), kPackedTileBytes);
-                bulk_g2s(smem_addr(p_ring + s * kPackedTileBytes), src + static_cast<size_t>(issued) * kPackedTileBytes,
-                         kPackedTileBytes, full_p(s), policy);
+                if (!mbar_wait(empty_p(s), ((issued / kPStages) & 1) ^ 1, abort_flag, kSiteProducerEmpty)) break;
+                issue_stage(issued, stream_policy, keep_policy);
             }
             // no copy may still be writing shared memory when the CTA exits
             for (int j = issued > kPStages ? issued - kPStages : 0; j < issued; ++j)
@@ -323,9 +441,7 @@ __global__ void __launch_bounds__(kThreads, 2) msd_kernel(const RunParams p) {
             int last_j[2] = {-1, -1};
             for (int i = 0; i < nkb; ++i) {
                 const int c = i % kCStages;
-                const uint32_t ph = (i / kCStages) & 1;
-                if (!mbar_wait(full_a(c), ph, abort_flag, kSiteMmaOperands)) break;
-                if (!mbar_wait(full_b(c), ph, abort_flag, kSiteMmaOperands)) break;
+                if (!mbar_wait(full_o(c), (i / kCStages) & 1, abort_flag, kSiteMmaOperands)) break;
                 tc_fence_after_sync();
                 const int kb = kb0 + i;
                 const int kend = min(K, (kb + 1) * kKBlock);
@@ -358,23 +474,22 @@ __global__ void __launch_bounds__(kThreads, 2) msd_kernel(const RunParams p) {
         }
         __syncwarp();
     } else if (warp < kConvWarp0 + kNumConvWarps) {
-        // ================================================================ int4 -> E4M3 converters
-        const int ct = threadIdx.x - kConvWarp0 * 32;
+        // ================================================================ operand builders
+        const int cw = warp - kConvWarp0;               // 0..3
+        const int ct = threadIdx.x - kConvWarp0 * 32;   // 0..127: also this thread's column for the scale copy
+        const int lpg = G / 4;                          // lanes per group in the unfold
         for (int i = 0; i < nkb; ++i) {
             const int s = i % kPStages, c = i % kCStages;
-            bool ok = true;
-            if (lane == 0)
-                ok = mbar_wait(full_p(s), (i / kPStages) & 1, abort_flag, kSiteConvFull) &&
-                     mbar_wait(empty_o(c), ((i / kCStages) & 1) ^ 1, abort_flag, kSiteConvEmpty);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            const uint8_t *src = p_ring + s * kPackedTileBytes;
+            if (!mbar_wait_warp(full_p(s), (i / kPStages) & 1, abort_flag, kSiteConvFull)) break;
+            if (!mbar_wait_warp(empty_o(c), ((i / kCStages) & 1) ^ 1, abort_flag, kSiteConvEmpty)) break;
+            if (!mbar_wait_warp(cempty(c), ((i / kCStages) & 1) ^ 1, abort_flag, kSiteConvEmpty)) break;
+            const uint8_t *stage = p_ring + s * C::kStageBytes;
             uint8_t *dst = a_ring + c * kATileBytes;
 #pragma unroll
             for (int it = 0; it < kPackedTileBytes / 8 / (kNumConvWarps * 32); ++it) {
                 const int q = ct + it * kNumConvWarps * 32;     // 16-k chunk of one weight row
                 const int row = q >> 3, ch = q & 7;
-                const uint2 v = *reinterpret_cast<const uint2 *>(src + q * 8);
+                const uint2 v = *reinterpret_cast<const uint2 *>(stage + q * 8);
                 const uint32_t vx = v.x ^ 0x88888888u, vy = v.y ^ 0x88888888u;
                 uint4 o;
                 o.x = u4x4_to_e4m3(v.x, vx);
@@ -383,87 +498,61 @@ __global__ void __launch_bounds__(kThreads, 2) msd_kernel(const RunParams p) {
                 o.w = u4x4_to_e4m3(v.y >> 16, vy >> 16);
                 *reinterpret_cast<uint4 *>(dst + (row >> 3) * 1024 + (row & 7) * 128 + ((ch ^ (row & 7)) << 4)) = o;
             }
+            // unfold of this k-block's x tile; rows m = base, base + 4, ... rotate over the warps
+            const __half *xs = reinterpret_cast<const __half *>(stage + C::kXOff);
+            uint8_t *bt = b_ring + c * C::kBTileBytes;
+            float *cst = const_ring + c * kConstStageFloats;
+            const int base = (cw - i) & 3;
+#pragma unroll
+            for (int pair = 0; pair < (kMaxM + 7) / 8; ++pair) {
+                const int ma = base + 8 * pair, mb = ma + 4;
+                if (mb < p.m_sub) {
+                    const int rows[2] = {ma, mb};
+                    unfold_rows<kMaxM, 2>(xs, bt, cst, rows, lpg, lane);
+                } else if (ma < p.m_sub) {
+                    const int rows[1] = {ma};
+                    unfold_rows<kMaxM, 1>(xs, bt, cst, rows, lpg, lane);
+                }
+            }
+            if (!debug) {
+                const __half *ss = reinterpret_cast<const __half *>(stage + C::kSOff);
+                for (int gg = 0; gg < gpk; ++gg)
+                    cst[kScaleFloatsOffset + gg * kTileN + ct] = __half2float(ss[gg * kTileN + ct]);
+            }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(empty_p(s));
-                mbar_arrive(full_a(c));
+                mbar_arrive(full_o(c));
             }
         }
     } else {
-        // ================================================================ unfold + epilogue
-        const int ew = warp - kEpiWarp0;                 // unfold row assignment
+        // ================================================================ epilogue
         const int quarter = warp & 3;                    // TMEM lanes this warp may read
         const int et = threadIdx.x - kEpiWarp0 * 32;
-        const int n = nt * kTileN + quarter * 32 + lane;
-        const int lpg = G / 4;                           // lanes per group in the unfold
+        const int n_local = quarter * 32 + lane;
+        const int n = nt * kTileN + n_local;
         const int rows_valid = min(p.m_sub, M - m0);
         float yacc[kMaxM];
 #pragma unroll
         for (int m = 0; m < kMaxM; ++m) yacc[m] = 0.0f;
 
-        auto unfold_kblock = [&](int i) {
-            const int c = i % kCStages;
-            const int kb = kb0 + i;
-            uint8_t *bt = b_ring + c * C::kBTileBytes;
-            float *cst = const_ring + c * kConstStageFloats;
-            const int kbyte = lane * 4;
-            for (int m = ew; m < p.m_sub; m += kNumEpiWarps) {
-                float v[4];
-                load_x4(p.x, M, K, m0 + m, kb * kKBlock + kbyte, v);
-                float am = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-                am = group_max(am, lpg);
-                float a1[4], a2[4], a3[4];
-                msd_unfold4(v, am, a1, a2, a3);
-                const uint32_t w1 = e4m3x2(a1[1], a1[0]) | (e4m3x2(a1[3], a1[2]) << 16);
-                const uint32_t w2 = e4m3x2(a2[1], a2[0]) | (e4m3x2(a2[3], a2[2]) << 16);
-                const uint32_t w3 = e4m3x2(a3[1], a3[0]) | (e4m3x2(a3[3], a3[2]) << 16);
-                *reinterpret_cast<uint32_t *>(bt + sw128_offset(m, kbyte)) = w1;
-                *reinterpret_cast<uint32_t *>(bt + sw128_offset(kMaxM + m, kbyte)) = w2;
-                *reinterpret_cast<uint32_t *>(bt + sw128_offset(2 * kMaxM + m, kbyte)) = w3;
-                const float s1 = group_sum((a1[0] + a1[1]) + (a1[2] + a1[3]), lpg);
-                const float s2 = group_sum((a2[0] + a2[1]) + (a2[2] + a2[3]), lpg);
-                const float s3 = group_sum((a3[0] + a3[1]) + (a3[2] + a3[3]), lpg);
-                if ((lane & (lpg - 1)) == 0) {
-                    float *cg = cst + (lane / lpg) * kConstFloatsPerGroup;
-                    const float c1 = kC1 * am, c2 = kC2 * am, c3 = kC3 * am;
-                    cg[0 * 16 + m] = c1;
-                    cg[1 * 16 + m] = c2;
-                    cg[2 * 16 + m] = c3;
-                    cg[3 * 16 + m] = 8.0f * (c1 * s1 + c2 * s2 + c3 * s3);
-                    cg[4 * 16 + m] = s1;
-                    cg[5 * 16 + m] = s2;
-                    cg[6 * 16 + m] = s3;
-                }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(full_b(c));
-        };
-
-        const int nlook = nkb < kLookahead ? nkb : kLookahead;
-        for (int i = 0; i < nlook; ++i) unfold_kblock(i);        // first uses of the ring slots: no wait
-        named_bar_sync(kEpiBarrierId, kNumEpiWarps * 32);         // constants visible to all epilogue threads
-
         bool ok = true;
         int j = 0;
-        for (int i = 0; i < nkb; ++i) {
-            const int iu = i + kLookahead;
-            if (ok && iu < nkb) {
-                const int c = iu % kCStages;
-                ok = mbar_wait(empty_o(c), ((iu / kCStages) & 1) ^ 1, abort_flag, kSiteEpiOperandsEmpty);
-                if (ok) unfold_kblock(iu);
-            }
+        for (int i = 0; i < nkb && ok; ++i) {
+            const int c = i % kCStages;
+            // the builders' constant writes for this k-block are ordered before this wait (the phase cannot move
+            // on: the next use of slot c waits for cempty(c), which this warp has not released yet)
+            ok = mbar_wait_warp(full_o(c), (i / kCStages) & 1, abort_flag, kSiteEpiOperandsEmpty);
             const int kb = kb0 + i;
-            const int gfirst = kb * kKBlock / G;
+            const int gfirst = kb * gpk;
             const int ng = (min(K, (kb + 1) * kKBlock) - kb * kKBlock) / G;
-            const float *cst = const_ring + (i % kCStages) * kConstStageFloats;
+            const float *cst = const_ring + c * kConstStageFloats;
             for (int gg = 0; gg < ng && ok; ++gg, ++j) {
                 const int b = j & 1;
                 const int g = gfirst + gg;
-                const bool use_scale = p.dbg_group < 0 && n < N;     // debug runs pass no scale
-                const float s_n = use_scale ? __half2float(p.scale[static_cast<size_t>(g) * N + n]) : 0.0f;
-                ok = mbar_wait(full_t(b), (j >> 1) & 1, abort_flag, kSiteEpiTmemFull);
+                const float s_n = cst[kScaleFloatsOffset + gg * kTileN + n_local];
+                ok = mbar_wait_warp(full_t(b), (j >> 1) & 1, abort_flag, kSiteEpiTmemFull);
                 if (!ok) break;
                 tc_fence_after_sync();
                 uint32_t d[3][16];
@@ -480,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 2) msd_kernel(const RunParams p) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_t(b));
                 const float *cg = cst + gg * kConstFloatsPerGroup;
-                if (p.dbg_group >= 0) {
+                if (debug) {
                     if (g == p.dbg_group && n < N) {
 #pragma unroll
                         for (int m = 0; m < kMaxM; ++m) {
@@ -499,25 +588,34 @@ __global__ void __launch_bounds__(kThreads, 2) msd_kernel(const RunParams p) {
                 }
 #pragma unroll
                 for (int m = 0; m < kMaxM; ++m) {
-                    const float d1 = __uint_as_float(d[m >> 4][m & 15]);
-                    const float d2 = __uint_as_float(d[(kMaxM + m) >> 4][(kMaxM + m) & 15]);
-                    const float d3 = __uint_as_float(d[(2 * kMaxM + m) >> 4][(2 * kMaxM + m) & 15]);
-                    float t = fmaf(cg[m], d1, -cg[48 + m]);
-                    t = fmaf(cg[16 + m], d2, t);
-                    t = fmaf(cg[32 + m], d3, t);
-                    yacc[m] = fmaf(s_n, t, yacc[m]);
+                    if (m < rows_valid) {
+                        const float d1 = __uint_as_float(d[m >> 4][m & 15]);
+                        const float d2 = __uint_as_float(d[(kMaxM + m) >> 4][(kMaxM + m) & 15]);
+                        const float d3 = __uint_as_float(d[(2 * kMaxM + m) >> 4][(2 * kMaxM + m) & 15]);
+                        float t = fmaf(cg[m], d1, -cg[48 + m]);
+                        t = fmaf(cg[16 + m], d2, t);
+                        t = fmaf(cg[32 + m], d3, t);
+                        yacc[m] = fmaf(s_n, t, yacc[m]);
+                    }
                 }
             }
-            // one decision for all epilogue threads; also orders the constants of later k-blocks
+            // release the constant slot; one decision for all epilogue threads
+            __syncwarp();
+            if (lane == 0) mbar_arrive(cempty(c));
             ok = !named_bar_or(kEpiBarrierId, kNumEpiWarps * 32, !ok);
-            if (!ok) break;
         }
 
-        if (ok && p.dbg_group < 0) {
-            if (p.splits == 1) {
+        if (ok && !debug) {
+            if (p.reduce == kReduceNone) {
 #pragma unroll
                 for (int m = 0; m < kMaxM; ++m)
                     if (m < rows_valid && n < N) p.y[static_cast<size_t>(m0 + m) * N + n] = __float2half_rn(yacc[m]);
+            } else if (p.reduce == kReduceCluster) {
+                // this slice's partial sums go to shared memory (the converted-weight ring is idle by now); the
+                // cluster reduces them after the cluster barrier below
+                float *red = reinterpret_cast<float *>(a_ring);
+#pragma unroll
+                for (int m = 0; m < kMaxM; ++m) red[m * kTileN + n_local] = yacc[m];
             } else {
                 float *part = p.ws_part + static_cast<size_t>(sp) * M * N;
 #pragma unroll
@@ -532,19 +630,49 @@ __global__ void __launch_bounds__(kThreads, 2) msd_kernel(const RunParams p) {
                 named_bar_sync(kEpiBarrierId, kNumEpiWarps * 32);
                 if (*last_flag) {
                     __threadfence();
+                    for (int m = 0; m < rows_valid; ++m) {
+                        if (n >= N) break;
+                        const float *src = p.ws_part + static_cast<size_t>(m0 + m) * N + n;
+                        const size_t slice = static_cast<size_t>(M) * N;
+                        float acc = 0.0f;
+                        for (int s0 = 0; s0 < p.splits; s0 += 8) {     // eight loads in flight, summed in order
+                            float v[8];
 #pragma unroll
-                    for (int m = 0; m < kMaxM; ++m) {
-                        if (m < rows_valid && n < N) {
-                            float acc = 0.0f;
-                            for (int s = 0; s < p.splits; ++s)
-                                acc += __ldcg(p.ws_part + (static_cast<size_t>(s) * M + m0 + m) * N + n);
-                            p.y[static_cast<size_t>(m0 + m) * N + n] = __float2half_rn(acc);
+                            for (int q = 0; q < 8; ++q) v[q] = s0 + q < p.splits ? __ldcg(src + (s0 + q) * slice) : 0.0f;
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) acc += v[q];
                         }
+                        p.y[static_cast<size_t>(m0 + m) * N + n] = __float2half_rn(acc);
                     }
                     if (et == 0) p.ws_count[static_cast<size_t>(mt) * p.n_tiles + nt] = 0u;
                 }
             }
         }
+    }
+
+    if (p.reduce == kReduceCluster && !debug) {
+        // every thread of every CTA of the cluster takes part in both barriers (warps reconverged first)
+        __syncwarp();
+        cluster_sync_all();                                      // all partial sums are in shared memory
+        if (warp >= kEpiWarp0) {
+            const int n_local = (warp & 3) * 32 + lane;
+            const int n = nt * kTileN + n_local;
+            const int rows_valid = min(p.m_sub, M - m0);
+            const uint32_t red = smem_addr(a_ring);
+            // CTA r of the cluster finishes rows r, r + S, ...; every row sums the slices in slice order
+            for (int m = static_cast<int>(cluster_ctarank()); m < rows_valid && n < N; m += p.splits) {
+                float v[kMaxClusterSplits];
+                const uint32_t off = static_cast<uint32_t>((m * kTileN + n_local) * 4);
+#pragma unroll
+                for (int q = 0; q < kMaxClusterSplits; ++q)
+                    v[q] = q < p.splits ? ld_cluster_f32(cluster_map(red + off, static_cast<uint32_t>(q))) : 0.0f;
+                float acc = 0.0f;
+#pragma unroll
+                for (int q = 0; q < kMaxClusterSplits; ++q) acc += v[q];
+                p.y[static_cast<size_t>(m0 + m) * N + n] = __float2half_rn(acc);
+            }
+        }
+        cluster_sync_all();                                      // peers' shared memory stays alive until read
     }
 
     __syncthreads();

@@ -1,5 +1,6 @@
 // C ABI of the A16W4 per-group MSD matmul for GB300 (declared and documented in include/wqbmm.h).
 // Host code: argument validation (no GPU needed), split-K planning, kernel launches on the caller's stream.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -14,7 +15,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kPlanSms = 160;       // workspace sizing assumes at most this many SMs, so it needs no device
-constexpr int kCtasPerSm = 2;       // shared memory (about 110 KB) and TMEM allow two run CTAs per SM
+constexpr int kCtasPerSm = 2;       // shared memory (at most 110 KB) and TMEM allow two run CTAs per SM
 
 struct DeviceInfo {
     bool probed = false;
@@ -50,11 +51,13 @@ wqbmm_status check_shape(const Shape &s) {
     return WQBMM_OK;
 }
 
-// Rows of x per CTA and the MMA N (three stacked planes padded to 16, 32 or 48 rows).
+// Rows of x per CTA, the MMA N (three stacked planes padded to 16, 32 or 48 rows), and the split over K.
 struct Plan {
-    int m_sub, m_tiles, n_tiles, kb_total, splits, nmma;
+    int m_sub, m_tiles, n_tiles, kb_total, splits, nmma, reduce;
 };
 
+// Splits over K (only when the output tiles alone cannot fill the GPU): aim at two CTAs per SM. Up to 12 wanted
+// slices become at most 8 cluster slices reduced on chip; more go through a global workspace.
 Plan make_plan(const Shape &s, int sms) {
     Plan p{};
     p.m_tiles = static_cast<int>(ceil_div(s.M, 16));
@@ -66,18 +69,55 @@ Plan make_plan(const Shape &s, int sms) {
     const int64_t target = static_cast<int64_t>(kCtasPerSm) * sms;
     int64_t splits = 1;
     if (tiles < sms) splits = target / tiles;
+    if (splits <= 12 && splits > kMaxClusterSplits) splits = kMaxClusterSplits;
     if (splits > p.kb_total) splits = p.kb_total;
     if (splits < 1) splits = 1;
     p.splits = static_cast<int>(splits);
+    p.reduce = p.splits == 1 ? kReduceNone : (p.splits <= kMaxClusterSplits ? kReduceCluster : kReduceGlobal);
     return p;
 }
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 size_t workspace_for(const Shape &s, const Plan &p) {
-    if (p.splits <= 1) return 0;
+    if (p.reduce != kReduceGlobal) return 0;
     return align256(static_cast<size_t>(p.splits) * s.M * s.N * sizeof(float)) +
            align256(static_cast<size_t>(p.m_tiles) * p.n_tiles * sizeof(uint32_t));
+}
+
+// ------------------------------------------------------------------------------------------------ tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool probed = false;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!probed) {
+        probed = true;
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+// Row-major fp16 matrix [rows, cols] with a box of box_rows x box_cols; zeros outside the matrix.
+bool fp16_tensor_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int box_rows, int box_cols) {
+    const EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t elem[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, elem,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Current device must be compute capability 10.3; caches the SM count.
@@ -116,9 +156,25 @@ wqbmm_status launch_msd(const RunParams &rp, const Plan &plan, DeviceInfo *info,
             info->smem_set[idx] = true;
         }
     }
-    const dim3 grid(plan.n_tiles, plan.m_tiles, rp.dbg_group >= 0 ? 1 : plan.splits);
-    msd_kernel<NMMA><<<grid, kThreads, smem, stream>>>(rp);
-    return cudaPeekAtLastError() == cudaSuccess ? WQBMM_OK : WQBMM_ERR_CUDA;
+    // x tiles: m_sub rows x 128 k; scale tiles: (128 / G) groups x 128 columns
+    CUtensorMap tmap_x{}, tmap_s{};
+    if (!fp16_tensor_map(&tmap_x, rp.x, rp.M, rp.K, rp.m_sub, kKBlock)) return WQBMM_ERR_CUDA;
+    if (rp.dbg_group < 0 && !fp16_tensor_map(&tmap_s, rp.scale, rp.K / rp.G, rp.N, kKBlock / rp.G, kTileN))
+        return WQBMM_ERR_CUDA;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(plan.n_tiles, plan.m_tiles, rp.dbg_group >= 0 ? 1 : plan.splits);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = static_cast<unsigned>(plan.splits);
+    cfg.attrs = attr;
+    cfg.numAttrs = rp.reduce == kReduceCluster ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, msd_kernel<NMMA>, rp, tmap_x, tmap_s) != cudaSuccess) return WQBMM_ERR_CUDA;
+    return WQBMM_OK;
 }
 
 wqbmm_status launch_plan(const RunParams &rp, const Plan &plan, DeviceInfo *info, cudaStream_t stream) {
@@ -227,7 +283,7 @@ wqbmm_status wqbmm_run(const void *x, const void *w_prepacked, const void *antiq
     rp.w = static_cast<const uint8_t *>(w_prepacked);
     rp.scale = static_cast<const __half *>(antiquant_scale);
     rp.y = static_cast<__half *>(y);
-    if (plan.splits > 1) {
+    if (plan.reduce == kReduceGlobal) {
         rp.ws_part = static_cast<float *>(workspace);
         rp.ws_count = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) +
                                                    align256(static_cast<size_t>(plan.splits) * M * N * sizeof(float)));
@@ -241,6 +297,7 @@ wqbmm_status wqbmm_run(const void *x, const void *w_prepacked, const void *antiq
     rp.m_tiles = plan.m_tiles;
     rp.splits = plan.splits;
     rp.kb_total = plan.kb_total;
+    rp.reduce = plan.reduce;
     rp.dbg_group = -1;
     return launch_plan(rp, plan, info, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -261,7 +318,7 @@ wqbmm_status wqbmm_run_static_scratch(const void *x, const void *w_prepacked, co
     if (need > kStaticScratchBytes) return WQBMM_ERR_SCRATCH_LIMIT;
     const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     RunParams rp{};
-    if (plan.splits > 1) {
+    if (plan.reduce == kReduceGlobal) {
         void *base = nullptr;
         if ((st = static_scratch_address(dev, &base)) != WQBMM_OK) return st;
         const size_t counters_at = align256(static_cast<size_t>(plan.splits) * M * N * sizeof(float));
@@ -285,6 +342,7 @@ wqbmm_status wqbmm_run_static_scratch(const void *x, const void *w_prepacked, co
     rp.m_tiles = plan.m_tiles;
     rp.splits = plan.splits;
     rp.kb_total = plan.kb_total;
+    rp.reduce = plan.reduce;
     rp.dbg_group = -1;
     return launch_plan(rp, plan, info, cs);
 }
@@ -319,6 +377,7 @@ wqbmm_status wqbmm_debug_group_partials(const void *x, const void *w_prepacked, 
     if ((st = current_device(&dev, &info)) != WQBMM_OK) return st;
     Plan plan = make_plan(s, info->sms);
     plan.splits = 1;
+    plan.reduce = kReduceNone;
     RunParams rp{};
     rp.x = static_cast<const __half *>(x);
     rp.w = static_cast<const uint8_t *>(w_prepacked);
@@ -332,6 +391,7 @@ wqbmm_status wqbmm_debug_group_partials(const void *x, const void *w_prepacked, 
     rp.m_tiles = plan.m_tiles;
     rp.splits = 1;
     rp.kb_total = plan.kb_total;
+    rp.reduce = kReduceNone;
     rp.dbg_group = static_cast<int>(g);
     return launch_plan(rp, plan, info, reinterpret_cast<cudaStream_t>(stream));
 }
