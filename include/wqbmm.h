@@ -101,6 +101,11 @@ WQBMM_API wqbmm_status wqbmm_workspace_bytes(int64_t M, int64_t K, int64_t N, in
  *   y                device, fp16 [M, N] row-major (written; must not overlap the inputs or the workspace)
  *   workspace        device, at least wqbmm_workspace_bytes(M, K, N, G) bytes (may be null when that is 0)
  * The result is deterministic: split-K partial sums are reduced in a fixed order.
+ * The kernel is launched with programmatic stream serialization: it may start while the kernel enqueued just before
+ * it on `stream` is still finishing, and it reads w_prepacked and antiquant_scale before that kernel has ended (x is
+ * read, and y and the workspace are written, only after it has ended). So w_prepacked and antiquant_scale must not be
+ * written by an immediately preceding kernel that itself releases its dependents early (griddepcontrol.
+ * launch_dependents); ordinary kernels, copies and memsets always complete before this kernel starts.
  * Errors: NULLPTR, INVALID (shape, alignment, workspace too small), UNSUPPORTED_ARCH, CUDA (launch failure).
  * A kernel that gives up a bounded internal wait records WQBMM_ERR_DEVICE_TIMEOUT in the device status word.
  */

@@ -13,10 +13,12 @@
 //   warp 0      TMA producer: per 128 k, one bulk copy of the packed weight tile (8 KB) plus 2-D tensor copies of
 //               the x tile and the scale tile, into a ring deep enough to hold a decode CTA's whole K-slice
 //   warp 1      TMEM owner and single-thread MMA issuer (tcgen05.mma kind::f8f6f4, E4M3 x E4M3 -> F32)
-//   warps 2-5   operand builders, per k-block: int4 (offset binary) -> E4M3 weights in the 128-byte-swizzled
-//               K-major layout, then the unfold of the x tile (A_max, three planes as E4M3, per-group constants,
-//               the scale column of each thread), rows rotating over the warps from one k-block to the next
-//   warps 6-9   epilogue: TMEM -> registers, Y_i = D_i - 8 S_i folded into the combine, scale, accumulate
+//   warps 2-5   operand builders, per k-block: int4 (offset binary) -> E4M3 for half of the weight tile (128-byte-
+//               swizzled K-major layout), then the unfold of the x tile (A_max, three planes as E4M3, per-group
+//               constants, the scale column of each thread), rows rotating over the warps from one k-block to the next
+//   warps 6-9   the other half of each weight tile, then the epilogue of the previous k-block: TMEM -> registers,
+//               Y_i = D_i - 8 S_i folded into the combine, scale, accumulate; releasing an operand slot after its
+//               epilogue (which has seen all of that k-block's MMAs complete)
 // Split-K (when there are too few column tiles to fill the GPU): up to 8 K-slices of a tile form a thread-block
 // cluster and reduce through distributed shared memory; more slices reduce through a global workspace. Either way
 // the slices are summed in slice order, so the result does not depend on timing.
@@ -92,7 +94,7 @@ struct Cfg {
     static constexpr int kPStagesFit = (kSmemBudget - kFixedBytes - 16 * 8) / kStageBytes;
     static constexpr int kPStages = kPStagesFit < 3 ? 3 : (kPStagesFit > 8 ? 8 : kPStagesFit);
     static constexpr int kOffBar = kOffP + kPStages * kStageBytes;
-    static constexpr int kNumBars = 2 * kPStages + 3 * kCStages + 4;
+    static constexpr int kNumBars = 2 * kPStages + 2 * kCStages + 4;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 64 + 1024;       // + alignment slack
     static_assert(kStageBytes % 128 == 0, "TMA destinations must stay 128-byte aligned");
@@ -190,6 +192,24 @@ constexpr uint32_t kLut8to11 = 0x53525150u, kLut12to15 = 0x57565554u;
 // the low lookup yields 0 for them. The second lookup runs on the nibbles with msb flipped and covers 8..15.
 __device__ __forceinline__ uint32_t u4x4_to_e4m3(uint32_t sel, uint32_t sel_flipped) {
     return prmt(kLut0to3, kLut4to7, sel) | prmt(kLut8to11, kLut12to15, sel_flipped);
+}
+
+// int4 -> E4M3 for the chunks q = t, t + 128, ... (4 of them) of one half of a packed 128 x 128 weight tile: chunk q
+// is 16 k of weight row q / 8, written to its place in the 128-byte-swizzled K-major A tile.
+__device__ __forceinline__ void convert_half_tile(const uint8_t *src, uint8_t *dst, int t, int half) {
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int q = t + (half * 4 + it) * 128;
+        const int row = q >> 3, ch = q & 7;
+        const uint2 v = *reinterpret_cast<const uint2 *>(src + q * 8);
+        const uint32_t vx = v.x ^ 0x88888888u, vy = v.y ^ 0x88888888u;
+        uint4 o;
+        o.x = u4x4_to_e4m3(v.x, vx);
+        o.y = u4x4_to_e4m3(v.x >> 16, vx >> 16);
+        o.z = u4x4_to_e4m3(v.y, vy);
+        o.w = u4x4_to_e4m3(v.y >> 16, vy >> 16);
+        *reinterpret_cast<uint4 *>(dst + (row >> 3) * 1024 + (row & 7) * 128 + ((ch ^ (row & 7)) << 4)) = o;
+    }
 }
 
 // ------------------------------------------------------------------------------------------------ kernels
@@ -339,17 +359,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint8_t *p_ring = smem + C::kOffP;
     float *const_ring = reinterpret_cast<float *>(smem + C::kOffConst);
     const uint32_t bar0 = smem_addr(smem + C::kOffBar);
-    // barriers: full_p / empty_p  load stage landed / released by the operand builders
-    //           full_o / empty_o  operand slot (A, B, constants) built / consumed by the MMAs
-    //           cempty            constant slot released by the epilogue
+    // barriers: full_p / empty_p  load stage landed / released by the warps that read it
+    //           full_o / sfree    operand slot (A, B, constants) built / released after the k-block's epilogue
     //           full_t / empty_t  TMEM accumulator buffer written by the MMAs / read by the epilogue
     auto full_p = [&](int s) { return bar0 + 8u * s; };
     auto empty_p = [&](int s) { return bar0 + 8u * (kPStages + s); };
     auto full_o = [&](int c) { return bar0 + 8u * (2 * kPStages + c); };
-    auto empty_o = [&](int c) { return bar0 + 8u * (2 * kPStages + kCStages + c); };
-    auto cempty = [&](int c) { return bar0 + 8u * (2 * kPStages + 2 * kCStages + c); };
-    auto full_t = [&](int b) { return bar0 + 8u * (2 * kPStages + 3 * kCStages + b); };
-    auto empty_t = [&](int b) { return bar0 + 8u * (2 * kPStages + 3 * kCStages + 2 + b); };
+    auto sfree = [&](int c) { return bar0 + 8u * (2 * kPStages + kCStages + c); };
+    auto full_t = [&](int b) { return bar0 + 8u * (2 * kPStages + 2 * kCStages + b); };
+    auto empty_t = [&](int b) { return bar0 + 8u * (2 * kPStages + 2 * kCStages + 2 + b); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
     int *last_flag = reinterpret_cast<int *>(smem + C::kOffMisc + 8);
@@ -373,29 +391,35 @@ __global__ void __launch_bounds__(kThreads, 2)
     // One load stage: the k-block's packed weight tile, x tile and scale tile, all counted on full_p(s).
     const uint8_t *w_src = p.w + (static_cast<size_t>(nt) * p.kb_total + kb0) * kPackedTileBytes;
     const uint32_t stage_tx = kPackedTileBytes + p.m_sub * kKBlock * 2 + (debug ? 0 : gpk * kTileN * 2);
-    auto issue_stage = [&](int i, uint64_t stream_policy, uint64_t keep_policy) {
+    // Weights and scales are read-only inputs of the call: they are fetched before waiting for the preceding kernel
+    // on the stream. x may be that kernel's output, so its tiles are fetched only after pdl_wait().
+    auto issue_static = [&](int i, uint64_t stream_policy, uint64_t keep_policy) {
         const int s = i % kPStages;
         const uint32_t dst = smem_addr(p_ring + s * C::kStageBytes);
         const int kb = kb0 + i;
         mbar_arrive_expect_tx(full_p(s), stage_tx);
         bulk_g2s(dst, w_src + static_cast<size_t>(i) * kPackedTileBytes, kPackedTileBytes, full_p(s), stream_policy);
-        tma_load_2d(dst + C::kXOff, &tmap_x, kb * kKBlock, m0, full_p(s), keep_policy);
         if (!debug) tma_load_2d(dst + C::kSOff, &tmap_s, nt * kTileN, kb * gpk, full_p(s), keep_policy);
     };
+    auto issue_x = [&](int i, uint64_t keep_policy) {
+        const int s = i % kPStages;
+        tma_load_2d(smem_addr(p_ring + s * C::kStageBytes) + C::kXOff, &tmap_x, (kb0 + i) * kKBlock, m0, full_p(s),
+                    keep_policy);
+    };
 
-    // ---- set-up. Thread 0 initialises the barriers and at once starts the loads of the first ring's worth of
-    // k-blocks (the slots are free), so the memory latency overlaps the rest of the set-up.
+    // ---- set-up. Thread 0 lets the next kernel on the stream start launching, initialises the barriers and at once
+    // starts the weight loads of the first ring's worth of k-blocks (the slots are free), so the memory latency
+    // overlaps the rest of the set-up and, under programmatic launch, the tail of the preceding kernel.
     const int first_loads = nkb < kPStages ? nkb : kPStages;
     uint64_t stream_policy = 0, keep_policy = 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kPStages; ++s) {
             mbar_init(full_p(s), 1);
-            mbar_init(empty_p(s), kNumConvWarps);
+            mbar_init(empty_p(s), kNumConvWarps + kNumEpiWarps);
         }
         for (int c = 0; c < kCStages; ++c) {
-            mbar_init(full_o(c), kNumConvWarps);
-            mbar_init(empty_o(c), 1);
-            mbar_init(cempty(c), kNumEpiWarps);
+            mbar_init(full_o(c), kNumConvWarps + kNumEpiWarps);
+            mbar_init(sfree(c), kNumEpiWarps);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(full_t(b), 1);
@@ -406,7 +430,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_fence_init();
         stream_policy = l2_policy_evict_first();    // weights: read once per call
         keep_policy = l2_policy_evict_last();       // x and scale tiles: shared by many CTAs
-        for (int i = 0; i < first_loads; ++i) issue_stage(i, stream_policy, keep_policy);
+        pdl_launch_dependents();
+        for (int i = 0; i < first_loads; ++i) issue_static(i, stream_policy, keep_policy);
+        pdl_wait();
+        for (int i = 0; i < first_loads; ++i) issue_x(i, keep_policy);
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
@@ -427,7 +454,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (; issued < nkb; ++issued) {
                 const int s = issued % kPStages;
                 if (!mbar_wait(empty_p(s), ((issued / kPStages) & 1) ^ 1, abort_flag, kSiteProducerEmpty)) break;
-                issue_stage(issued, stream_policy, keep_policy);
+                issue_static(issued, stream_policy, keep_policy);
+                issue_x(issued, keep_policy);
             }
             // no copy may still be writing shared memory when the CTA exits
             for (int j = issued > kPStages ? issued - kPStages : 0; j < issued; ++j)
@@ -466,7 +494,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                     last_j[b] = j;
                 }
                 if (stop) break;
-                umma_commit(empty_o(c));
             }
             // no MMA may still be writing TMEM when it is freed
             for (int b = 0; b < 2; ++b)
@@ -481,23 +508,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int i = 0; i < nkb; ++i) {
             const int s = i % kPStages, c = i % kCStages;
             if (!mbar_wait_warp(full_p(s), (i / kPStages) & 1, abort_flag, kSiteConvFull)) break;
-            if (!mbar_wait_warp(empty_o(c), ((i / kCStages) & 1) ^ 1, abort_flag, kSiteConvEmpty)) break;
-            if (!mbar_wait_warp(cempty(c), ((i / kCStages) & 1) ^ 1, abort_flag, kSiteConvEmpty)) break;
+            if (!mbar_wait_warp(sfree(c), ((i / kCStages) & 1) ^ 1, abort_flag, kSiteConvEmpty)) break;
             const uint8_t *stage = p_ring + s * C::kStageBytes;
-            uint8_t *dst = a_ring + c * kATileBytes;
-#pragma unroll
-            for (int it = 0; it < kPackedTileBytes / 8 / (kNumConvWarps * 32); ++it) {
-                const int q = ct + it * kNumConvWarps * 32;     // 16-k chunk of one weight row
-                const int row = q >> 3, ch = q & 7;
-                const uint2 v = *reinterpret_cast<const uint2 *>(stage + q * 8);
-                const uint32_t vx = v.x ^ 0x88888888u, vy = v.y ^ 0x88888888u;
-                uint4 o;
-                o.x = u4x4_to_e4m3(v.x, vx);
-                o.y = u4x4_to_e4m3(v.x >> 16, vx >> 16);
-                o.z = u4x4_to_e4m3(v.y, vy);
-                o.w = u4x4_to_e4m3(v.y >> 16, vy >> 16);
-                *reinterpret_cast<uint4 *>(dst + (row >> 3) * 1024 + (row & 7) * 128 + ((ch ^ (row & 7)) << 4)) = o;
-            }
+            convert_half_tile(stage, a_ring + c * kATileBytes, ct, 0);
             // unfold of this k-block's x tile; rows m = base, base + 4, ... rotate over the warps
             const __half *xs = reinterpret_cast<const __half *>(stage + C::kXOff);
             uint8_t *bt = b_ring + c * C::kBTileBytes;
@@ -528,6 +541,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     } else {
         // ================================================================ epilogue
+        pdl_wait();                                      // outputs are written after the preceding kernel ended
         const int quarter = warp & 3;                    // TMEM lanes this warp may read
         const int et = threadIdx.x - kEpiWarp0 * 32;
         const int n_local = quarter * 32 + lane;
@@ -537,71 +551,90 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int m = 0; m < kMaxM; ++m) yacc[m] = 0.0f;
 
+        // Iteration i converts the second half of k-block i's weight tile, then runs the epilogue of k-block i - 1.
         bool ok = true;
         int j = 0;
-        for (int i = 0; i < nkb && ok; ++i) {
-            const int c = i % kCStages;
-            // the builders' constant writes for this k-block are ordered before this wait (the phase cannot move
-            // on: the next use of slot c waits for cempty(c), which this warp has not released yet)
-            ok = mbar_wait_warp(full_o(c), (i / kCStages) & 1, abort_flag, kSiteEpiOperandsEmpty);
-            const int kb = kb0 + i;
-            const int gfirst = kb * gpk;
-            const int ng = (min(K, (kb + 1) * kKBlock) - kb * kKBlock) / G;
-            const float *cst = const_ring + c * kConstStageFloats;
-            for (int gg = 0; gg < ng && ok; ++gg, ++j) {
-                const int b = j & 1;
-                const int g = gfirst + gg;
-                const float s_n = cst[kScaleFloatsOffset + gg * kTileN + n_local];
-                ok = mbar_wait_warp(full_t(b), (j >> 1) & 1, abort_flag, kSiteEpiTmemFull);
-                if (!ok) break;
-                tc_fence_after_sync();
-                uint32_t d[3][16];
-                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                       static_cast<uint32_t>(b * C::kBufStride);
-                tmem_ld16(taddr, d[0]);
-                if (NMMA > 16) tmem_ld16(taddr + 16, d[1]);
-                if (NMMA > 32) tmem_ld16(taddr + 32, d[2]);
-                tmem_wait_ld();
-                reg_fence16(d[0]);
-                if (NMMA > 16) reg_fence16(d[1]);
-                if (NMMA > 32) reg_fence16(d[2]);
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty_t(b));
-                const float *cg = cst + gg * kConstFloatsPerGroup;
-                if (debug) {
-                    if (g == p.dbg_group && n < N) {
-#pragma unroll
-                        for (int m = 0; m < kMaxM; ++m) {
-                            if (m < rows_valid) {
-#pragma unroll
-                                for (int pl = 0; pl < 3; ++pl) {
-                                    const int col = pl * kMaxM + m;
-                                    const float dv = __uint_as_float(d[col >> 4][col & 15]);
-                                    const float yi = dv - 8.0f * cg[(4 + pl) * 16 + m];
-                                    p.dbg_y123[(static_cast<size_t>(pl) * M + m0 + m) * N + n] = __float2int_rn(yi);
-                                }
-                            }
-                        }
-                    }
-                    continue;
-                }
-#pragma unroll
-                for (int m = 0; m < kMaxM; ++m) {
-                    if (m < rows_valid) {
-                        const float d1 = __uint_as_float(d[m >> 4][m & 15]);
-                        const float d2 = __uint_as_float(d[(kMaxM + m) >> 4][(kMaxM + m) & 15]);
-                        const float d3 = __uint_as_float(d[(2 * kMaxM + m) >> 4][(2 * kMaxM + m) & 15]);
-                        float t = fmaf(cg[m], d1, -cg[48 + m]);
-                        t = fmaf(cg[16 + m], d2, t);
-                        t = fmaf(cg[32 + m], d3, t);
-                        yacc[m] = fmaf(s_n, t, yacc[m]);
+        for (int i = 0; i <= nkb && ok; ++i) {
+            if (i < nkb) {
+                const int s = i % kPStages, c = i % kCStages;
+                ok = mbar_wait_warp(full_p(s), (i / kPStages) & 1, abort_flag, kSiteConvFull) &&
+                     mbar_wait_warp(sfree(c), ((i / kCStages) & 1) ^ 1, abort_flag, kSiteConvEmpty);
+                if (ok) {
+                    convert_half_tile(p_ring + s * C::kStageBytes, a_ring + c * kATileBytes, et, 1);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(empty_p(s));
+                        mbar_arrive(full_o(c));
                     }
                 }
             }
-            // release the constant slot; one decision for all epilogue threads
-            __syncwarp();
-            if (lane == 0) mbar_arrive(cempty(c));
+            const int ie = i - 1;                        // k-block whose epilogue runs now
+            if (ok && ie >= 0) {
+                const int c = ie % kCStages;
+                // the builders' constant writes for this k-block are ordered before this wait (the phase cannot
+                // move on: the next use of slot c waits for sfree(c), which is released below)
+                ok = mbar_wait_warp(full_o(c), (ie / kCStages) & 1, abort_flag, kSiteEpiOperandsEmpty);
+                const int kb = kb0 + ie;
+                const int gfirst = kb * gpk;
+                const int ng = (min(K, (kb + 1) * kKBlock) - kb * kKBlock) / G;
+                const float *cst = const_ring + c * kConstStageFloats;
+                for (int gg = 0; gg < ng && ok; ++gg, ++j) {
+                    const int b = j & 1;
+                    const int g = gfirst + gg;
+                    const float s_n = cst[kScaleFloatsOffset + gg * kTileN + n_local];
+                    ok = mbar_wait_warp(full_t(b), (j >> 1) & 1, abort_flag, kSiteEpiTmemFull);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    uint32_t d[3][16];
+                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                           static_cast<uint32_t>(b * C::kBufStride);
+                    tmem_ld16(taddr, d[0]);
+                    if (NMMA > 16) tmem_ld16(taddr + 16, d[1]);
+                    if (NMMA > 32) tmem_ld16(taddr + 32, d[2]);
+                    tmem_wait_ld();
+                    reg_fence16(d[0]);
+                    if (NMMA > 16) reg_fence16(d[1]);
+                    if (NMMA > 32) reg_fence16(d[2]);
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(empty_t(b));
+                    const float *cg = cst + gg * kConstFloatsPerGroup;
+                    if (debug) {
+                        if (g == p.dbg_group && n < N) {
+#pragma unroll
+                            for (int m = 0; m < kMaxM; ++m) {
+                                if (m < rows_valid) {
+#pragma unroll
+                                    for (int pl = 0; pl < 3; ++pl) {
+                                        const int col = pl * kMaxM + m;
+                                        const float dv = __uint_as_float(d[col >> 4][col & 15]);
+                                        const float yi = dv - 8.0f * cg[(4 + pl) * 16 + m];
+                                        p.dbg_y123[(static_cast<size_t>(pl) * M + m0 + m) * N + n] =
+                                            __float2int_rn(yi);
+                                    }
+                                }
+                            }
+                        }
+                        continue;
+                    }
+#pragma unroll
+                    for (int m = 0; m < kMaxM; ++m) {
+                        if (m < rows_valid) {
+                            const float d1 = __uint_as_float(d[m >> 4][m & 15]);
+                            const float d2 = __uint_as_float(d[(kMaxM + m) >> 4][(kMaxM + m) & 15]);
+                            const float d3 = __uint_as_float(d[(2 * kMaxM + m) >> 4][(2 * kMaxM + m) & 15]);
+                            float t = fmaf(cg[m], d1, -cg[48 + m]);
+                            t = fmaf(cg[16 + m], d2, t);
+                            t = fmaf(cg[32 + m], d3, t);
+                            yacc[m] = fmaf(s_n, t, yacc[m]);
+                        }
+                    }
+                }
+                // this k-block's MMAs have all completed (the last full_t wait saw them): release the slot
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sfree(c));
+            }
             ok = !named_bar_or(kEpiBarrierId, kNumEpiWarps * 32, !ok);
         }
 

@@ -121,6 +121,19 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, boo
     return r != 0;
 }
 
+// ------------------------------------------------------------------------------------------------ dependent launch
+
+// Lets the next kernel on the stream (if it was launched with programmatic serialization) start launching.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the kernels this one depends on have completed and their memory is visible (no-op without a
+// programmatic dependency).
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------------------------------ clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

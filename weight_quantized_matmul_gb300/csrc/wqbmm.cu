@@ -166,13 +166,17 @@ wqbmm_status launch_msd(const RunParams &rp, const Plan &plan, DeviceInfo *info,
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = static_cast<unsigned>(plan.splits);
+    // programmatic launch: this kernel may start while the preceding kernel on the stream finishes; it fetches only
+    // weights and scales before griddepcontrol.wait (see msd_kernel)
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = static_cast<unsigned>(plan.splits);
     cfg.attrs = attr;
-    cfg.numAttrs = rp.reduce == kReduceCluster ? 1 : 0;
+    cfg.numAttrs = rp.reduce == kReduceCluster ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, msd_kernel<NMMA>, rp, tmap_x, tmap_s) != cudaSuccess) return WQBMM_ERR_CUDA;
     return WQBMM_OK;
 }
