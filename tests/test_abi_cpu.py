@@ -66,9 +66,13 @@ def test_workspace_bytes():
     # two column tiles and a long K: 160 slices (sized for up to 160 SMs, two CTAs each) reduce through the
     # workspace: 160 x 1 x 256 fp32 partial sums + one 256-byte block of counters
     assert wq.wqbmm_workspace_bytes(1, 65536, 256, 128) == 160 * 256 * 4 + 256
-    # enough tiles to fill the GPU: no split, no workspace
-    assert wq.wqbmm_workspace_bytes(2048, 8192, 28672, 64) == 0
-    assert wq.wqbmm_workspace_bytes(128, 5120, 13824, 128) == 0
+    # M >= 64: x unfolded once into three planes of 128-row tiles (3 bytes per element of x, rows padded to 128)
+    # plus 16 bytes of combine constants per padded row and group
+    assert wq.wqbmm_workspace_bytes(2048, 8192, 28672, 64) == 3 * 2048 * 8192 + 16 * 2048 * 128
+    assert wq.wqbmm_workspace_bytes(128, 5120, 13824, 128) == 3 * 128 * 5120 + 16 * 128 * 40
+    assert wq.wqbmm_workspace_bytes(64, 320, 136, 64) == 3 * 128 * 384 + 16 * 128 * 5
+    # 63 rows is still the fused small-M path: enough column tiles, no split, no workspace
+    assert wq.wqbmm_workspace_bytes(63, 4096, 28672, 64) == 0
 
 
 # (entry, args, expected status) — table-driven error paths
@@ -107,10 +111,14 @@ CASES = [
      INVALID),
     ("unfold_null_planes", lambda L: L.wqbmm_debug_unfold(A, 1, 128, 128, None, A, None), NULLPTR),
     ("unfold_bad_group", lambda L: L.wqbmm_debug_unfold(A, 1, 128, 100, A, A, None), INVALID),
-    ("partials_group_out_of_range", lambda L: L.wqbmm_debug_group_partials(A, A, 1, 256, 128, 128, 2, A, None),
-     INVALID),
-    ("partials_negative_group", lambda L: L.wqbmm_debug_group_partials(A, A, 1, 256, 128, 128, -1, A, None),
-     INVALID),
+    ("partials_group_out_of_range",
+     lambda L: L.wqbmm_debug_group_partials(A, A, 1, 256, 128, 128, 2, A, None, 0, None), INVALID),
+    ("partials_negative_group",
+     lambda L: L.wqbmm_debug_group_partials(A, A, 1, 256, 128, 128, -1, A, None, 0, None), INVALID),
+    ("partials_large_m_needs_workspace",
+     lambda L: L.wqbmm_debug_group_partials(A, A, 64, 256, 128, 128, 0, A, None, 0, None), NULLPTR),
+    ("partials_large_m_workspace_too_small",
+     lambda L: L.wqbmm_debug_group_partials(A, A, 64, 256, 128, 128, 0, A, A, 1024, None), INVALID),
     ("static_scratch_null_y", lambda L: L.wqbmm_run_static_scratch(A, A, A, None, 1, 128, 128, 128, None),
      NULLPTR),
     ("static_scratch_misaligned_x", lambda L: L.wqbmm_run_static_scratch(MIS, A, A, A, 1, 128, 128, 128, None),
@@ -137,4 +145,5 @@ def test_no_device_is_a_cuda_error(lib):
     if torch.cuda.is_available():
         pytest.skip("a CUDA device is present")
     # valid arguments, but no GPU: the device check fails with a CUDA error and nothing is launched
-    assert lib.wqbmm_run(A, A, A, A, 2048, 8192, 28672, 64, None, 0, None) == wq.ERR_CUDA
+    assert lib.wqbmm_run(A, A, A, A, 16, 8192, 28672, 64, None, 0, None) == wq.ERR_CUDA
+    assert lib.wqbmm_run(A, A, A, A, 2048, 8192, 28672, 64, A, 1 << 30, None) == wq.ERR_CUDA

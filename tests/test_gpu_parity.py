@@ -167,6 +167,11 @@ PARTIAL_CASES = [
     (16, 640, 136, 64, [9], "uniform3", "u7"),
     (17, 384, 256, 128, [2], "normal", "u8"),
     (40, 256, 128, 32, [0, 7], "normal", "u8"),
+    # M >= 64: the unfold pre-pass and the 128 x 128 tile kernel
+    (64, 512, 264, 64, [0, 5, 7], "t3_clip60", "u8"),
+    (130, 384, 256, 128, [0, 2], "normal", "u8"),
+    (200, 96, 1000, 32, [0, 2], "uniform3", "u7"),
+    (256, 320, 136, 64, [4], "normal_cols20", "pm1_mix"),
 ]
 
 
@@ -175,27 +180,30 @@ def test_group_partials_bit_exact(dev, M, K, N, G, groups, xd, wd):
     x, wp, _ = I.make_inputs(I.small_case(M, K, N, G, seed=M * 7 + K, x_dist=xd, w_dist=wd))
     w_pre = wq.prepack_weight(to_dev(wp, dev), K, N, G)
     xdv = to_dev(x, dev)
+    ws = wq.allocate_workspace(M, K, N, G, dev)
     for g in groups:
         y123 = torch.full((3, M, N), -12345, dtype=torch.int32, device=dev)
-        wq.wqbmm_debug_group_partials(xdv, w_pre, M, K, N, G, g, y123)
+        wq.wqbmm_debug_group_partials(xdv, w_pre, M, K, N, G, g, y123, ws)
         np.testing.assert_array_equal(y123.cpu().numpy(), oracle.group_partials(x, wp, N, G, g, oracle.MODE_F),
                                       err_msg=f"group {g}")
 
 
+@pytest.mark.parametrize("M", [4, 128])
 @pytest.mark.parametrize("wval", [7, -8, 1, -1])
-def test_group_partials_exact_at_extreme_magnitudes(dev, wval):
+def test_group_partials_exact_at_extreme_magnitudes(dev, wval, M):
     """x constant per group gives planes (7, 7, 5) everywhere; with constant weights the integer sums reach the
     largest magnitudes the format allows (|Y| up to 7 * 8 * G), where inexact FP32 accumulation would show."""
-    M, K, N, G = 4, 256, 128, 128
+    K, N, G = 256, 128, 128
     x = np.ones((M, K), dtype=np.float16)
     x[1] = -2.0
     x[2, :128] = 0.25
     w = np.full((K, N), wval, dtype=np.int8)
     wp = I.pack_int4_along_k(w)
     w_pre = wq.prepack_weight(to_dev(wp, dev), K, N, G)
+    ws = wq.allocate_workspace(M, K, N, G, dev)
     for g in range(2):
         y123 = torch.zeros((3, M, N), dtype=torch.int32, device=dev)
-        wq.wqbmm_debug_group_partials(to_dev(x, dev), w_pre, M, K, N, G, g, y123)
+        wq.wqbmm_debug_group_partials(to_dev(x, dev), w_pre, M, K, N, G, g, y123, ws)
         ref = oracle.group_partials(x, wp, N, G, g, oracle.MODE_F)
         np.testing.assert_array_equal(y123.cpu().numpy(), ref)
 
@@ -212,7 +220,11 @@ RUN_CASES = [
     (12, 2048, 640, 128, "normal_cols20", "pm1_mix", 0.005, 0.02),
     (17, 640, 392, 64, "normal", "u8", 0.005, 0.02),
     (40, 1280, 520, 128, "t3_clip60", "u8", 0.002, 0.03),
+    (64, 256, 128, 128, "normal", "u8", 0.005, 0.02),      # M >= 64: unfold pre-pass + 128 x 128 tiles
     (130, 512, 256, 64, "normal", "u8", 0.005, 0.02),
+    (200, 96, 1000, 32, "uniform3", "u7", -3.0, 3.0),
+    (256, 320, 392, 64, "t3_clip60", "u8", -1.0, 1.0),
+    (300, 1280, 520, 128, "normal_cols20", "pm1_mix", 0.002, 0.03),
     (1, 65536, 256, 128, "normal", "u8", 0.005, 0.02),     # 160-way split-K through the workspace
     (4, 4096, 1024, 128, "t3_clip60", "u8", -0.5, 0.5),    # 8 column tiles x 8 cluster slices
 ]
@@ -240,7 +252,8 @@ def test_run_zero_and_constant_rows(dev):
 
 
 @pytest.mark.parametrize("wl", [I.WORKLOADS["decode_m1_k4096_n4096"],                  # cluster-reduced split-K
-                                I.small_case(3, 16384, 520, 64, seed=8)])              # workspace split-K
+                                I.small_case(3, 16384, 520, 64, seed=8),               # workspace split-K
+                                I.small_case(200, 1024, 392, 128, seed=9)])            # unfold pre-pass
 def test_run_deterministic_and_workspace_left_clean(dev, wl):
     x, wp, sc = I.make_inputs(wl)
     xd, sd = to_dev(x, dev), to_dev(sc, dev)
@@ -253,7 +266,7 @@ def test_run_deterministic_and_workspace_left_clean(dev, wl):
         outs.append(y.cpu().numpy().view(np.uint16))
     assert all(np.array_equal(outs[0], o) for o in outs[1:])
     assert_within_tolerance(outs[0].view(np.float16), oracle.msd_matmul(x, wp, sc, wl.G), wl.name)
-    if ws is not None:
+    if ws is not None and wl.M < 64:
         # the arrival counters sit after the partial sums; all must be back at zero
         counters = ws.cpu().numpy()[-256:].view(np.uint32)
         assert not counters.any()
@@ -310,6 +323,7 @@ def test_workload_sampled_rows(dev, name, nrows):
     g = wl.groups // 2
     y123 = torch.empty((3, wl.M, wl.N), dtype=torch.int32, device=dev)
     w_pre = wq.prepack_weight(to_dev(wp, dev), wl.K, wl.N, wl.G)
-    wq.wqbmm_debug_group_partials(to_dev(x, dev), w_pre, wl.M, wl.K, wl.N, wl.G, g, y123)
+    ws = wq.allocate_workspace(wl.M, wl.K, wl.N, wl.G, dev)
+    wq.wqbmm_debug_group_partials(to_dev(x, dev), w_pre, wl.M, wl.K, wl.N, wl.G, g, y123, ws)
     got = y123.cpu().numpy()[:, rows]
     np.testing.assert_array_equal(got, oracle.group_partials(x, wp, wl.N, wl.G, g, oracle.MODE_F, rows=rows))

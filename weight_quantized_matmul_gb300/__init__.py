@@ -60,7 +60,7 @@ def load_library():
                 "wqbmm_workspace_bytes": [i64, i64, i64, i64, ctypes.POINTER(sz)],
                 "wqbmm_run": [p, p, p, p, i64, i64, i64, i64, p, sz, p],
                 "wqbmm_debug_unfold": [p, i64, i64, i64, p, p, p],
-                "wqbmm_debug_group_partials": [p, p, i64, i64, i64, i64, i64, p, p],
+                "wqbmm_debug_group_partials": [p, p, i64, i64, i64, i64, i64, p, p, sz, p],
                 "wqbmm_read_device_status": [ctypes.POINTER(ctypes.c_int32), ctypes.c_int, p],
                 "wqbmm_debug_wait_timeout": [i64, p],
                 "wqbmm_run_static_scratch": [p, p, p, p, i64, i64, i64, i64, p],
@@ -140,9 +140,13 @@ def wqbmm_debug_unfold(x, M: int, K: int, G: int, planes, amax, stream=None) -> 
            "wqbmm_debug_unfold")
 
 
-def wqbmm_debug_group_partials(x, w_prepacked, M: int, K: int, N: int, G: int, g: int, y123, stream=None) -> None:
+def wqbmm_debug_group_partials(x, w_prepacked, M: int, K: int, N: int, G: int, g: int, y123, workspace=None,
+                               workspace_bytes: int | None = None, stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load_library().wqbmm_debug_group_partials(_ptr(x), _ptr(w_prepacked), M, K, N, G, g, _ptr(y123),
-                                                     _stream(stream)), "wqbmm_debug_group_partials")
+                                                     _ptr(workspace), workspace_bytes, _stream(stream)),
+           "wqbmm_debug_group_partials")
 
 
 def wqbmm_read_device_status(clear: bool = False, stream=None) -> int:

@@ -1,0 +1,382 @@
+// Large-M path of the A16W4 per-group MSD matmul (WeightQuantBatchMatmulExperiment page, section 4.1).
+//
+// When x has many rows, unfolding x inside every column-tile CTA would repeat the same work N/128 times, so the
+// path is split in two kernels:
+//   unfold_planes_kernel  steps 1-8 once per (row, k): the three residual planes as E4M3 bytes, written directly in
+//                         the tensor-core operand layout (128-row x 128-k tiles, 128-byte swizzle, K-major), plus
+//                         per-(row, group) constants {c1 A_max, c2 A_max, c3 A_max, 8 sum_i c_i A_max S_i}
+//   msd_gemm_kernel       steps 9-11 for one 128-row x 128-column output tile per CTA: the planes are the MMA's A
+//                         operand (M = 128 rows of x), the int4 weights converted to E4M3 the B operand (N = 128
+//                         columns); each plane of each K-group accumulates in its own 128-column TMEM slot (four
+//                         slots rotate, so the next group's first plane overlaps the epilogue of this group)
+// Roles in msd_gemm_kernel (448 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA issuer, warps 2-5 int4 ->
+// E4M3 converters, warps 6-13 epilogue (two warps per TMEM lane quarter, 64 columns each, packed FP32x2 math).
+#pragma once
+
+#include "msd_kernels.cuh"
+
+namespace wqbmm {
+
+constexpr int kGemmTileM = 128;
+constexpr int kGemmTileN = 128;
+constexpr int kGemmThreads = 448;
+constexpr int kGemmConvWarp0 = 2;
+constexpr int kGemmEpiWarp0 = 6;
+constexpr int kGemmNumEpiWarps = 8;
+constexpr int kGemmBStages = 2;
+constexpr int kGemmSlots = 4;                                  // TMEM accumulator slots of 128 columns
+constexpr int kPlaneImageBytes = kGemmTileM * kKBlock;         // 16384: one plane of one k-block
+constexpr int kGemmConstRowBytes = 16;                         // float4 per (row, group)
+constexpr int kGemmSmemLimit = 232448;                         // opt-in shared memory per CTA on sm_103
+
+// Shared-memory layout of msd_gemm_kernel (depends on the group size through the groups per k-block).
+struct GemmLayout {
+    int gpk, const_bytes, scale_bytes, stage_bytes, p_stages;
+    int off_const, off_scale, off_p, off_b, off_bar, off_misc, smem_bytes;
+    __host__ __device__ static int align(int v, int a) { return (v + a - 1) / a * a; }
+    __host__ __device__ explicit GemmLayout(int G) {
+        gpk = kKBlock / G;
+        const_bytes = gpk * kGemmTileM * kGemmConstRowBytes;
+        scale_bytes = gpk * kGemmTileN * 2;
+        // stage: three plane images | packed weight tile | constants | scale tile
+        off_const = 3 * kPlaneImageBytes + kPackedTileBytes;
+        off_scale = off_const + const_bytes;
+        stage_bytes = align(off_scale + scale_bytes, 1024);
+        off_b = 0;                                             // converted weights ring first (1024-aligned)
+        off_p = kGemmBStages * (kGemmTileN * kKBlock);
+        const int fixed = off_p + 1024 /*align slack*/ + 512 /*barriers and flags*/;
+        p_stages = (kGemmSmemLimit - fixed) / stage_bytes;
+        if (p_stages > 3) p_stages = 3;
+        off_bar = off_p + p_stages * stage_bytes;
+        off_misc = off_bar + 8 * (2 * 3 + 2 * kGemmBStages + 2 * kGemmSlots);
+        smem_bytes = off_misc + 64 + 1024;
+    }
+};
+
+struct GemmParams {
+    const uint8_t *w;           // prepacked tiles
+    const uint8_t *planes;      // [m_tiles][kb_total][3][16 KB] from unfold_planes_kernel
+    const float4 *consts;       // [m_tiles][K/G][128 rows]
+    __half *y;
+    int32_t *dbg_y123;          // debug: integer partials of group dbg_group, else null
+    int M, K, N, G;
+    int m_tiles, n_tiles, kb_total;
+    int dbg_group;              // -1 in normal runs
+};
+
+// Steps 1-8 for one row and one 128-k block per warp. Planes go to the operand images, constants to the table; rows
+// past M (padding of the last 128-row tile) get zero planes and zero constants. In debug mode the constant record
+// holds the plane sums {S1, S2, S3, 0} instead.
+__global__ void __launch_bounds__(256) unfold_planes_kernel(const __half *__restrict__ x, int M, int K, int G,
+                                                            int kb_total, uint8_t *__restrict__ planes,
+                                                            float4 *__restrict__ consts, int debug) {
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);        // row within the padded rows
+    const int kb = blockIdx.y;
+    const int mt = row / kGemmTileM, r = row % kGemmTileM;
+    const int kbase = kb * kKBlock + lane * 4;
+    const int lpg = G / 4;
+    const int Gn = K / G;
+    float v[4];
+    load_x4(x, M, K, row, kbase, v);
+    float am = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    am = group_absmax(am, lpg);
+    float a1[4], a2[4], a3[4];
+    msd_unfold4(v, am, a1, a2, a3);
+    const int s1 = group_isum(__float2int_rn((a1[0] + a1[1]) + (a1[2] + a1[3])), lpg);
+    const int s2 = group_isum(__float2int_rn((a2[0] + a2[1]) + (a2[2] + a2[3])), lpg);
+    const int s3 = group_isum(__float2int_rn((a3[0] + a3[1]) + (a3[2] + a3[3])), lpg);
+    uint8_t *img = planes + (static_cast<size_t>(mt) * kb_total + kb) * 3 * kPlaneImageBytes;
+    const uint32_t off = sw128_offset(r, lane * 4);
+    *reinterpret_cast<uint32_t *>(img + off) = e4m3x2(a1[1], a1[0]) | (e4m3x2(a1[3], a1[2]) << 16);
+    *reinterpret_cast<uint32_t *>(img + kPlaneImageBytes + off) = e4m3x2(a2[1], a2[0]) | (e4m3x2(a2[3], a2[2]) << 16);
+    *reinterpret_cast<uint32_t *>(img + 2 * kPlaneImageBytes + off) =
+        e4m3x2(a3[1], a3[0]) | (e4m3x2(a3[3], a3[2]) << 16);
+    const int g = kb * (kKBlock / G) + lane / lpg;
+    if ((lane & (lpg - 1)) == 0 && g < Gn) {
+        float4 rec;
+        if (debug) {
+            rec = make_float4(static_cast<float>(s1), static_cast<float>(s2), static_cast<float>(s3), 0.0f);
+        } else {
+            const float c1 = kC1 * am, c2 = kC2 * am, c3 = kC3 * am;
+            rec = make_float4(c1, c2, c3, 8.0f * (c1 * s1 + c2 * s2 + c3 * s3));
+        }
+        consts[(static_cast<size_t>(mt) * Gn + g) * kGemmTileM + r] = rec;
+    }
+}
+
+__device__ __forceinline__ float2 ld_scale2(const uint8_t *p) {
+    return __half22float2(*reinterpret_cast<const __half2 *>(p));
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float2 v) {
+    const __half2 h = __float22half2_rn(v);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    msd_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmap_s) {
+    const GemmLayout L(p.G);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *b_ring = smem + L.off_b;
+    uint8_t *p_ring = smem + L.off_p;
+    const int P = L.p_stages;
+    const uint32_t bar0 = smem_addr(smem + L.off_bar);
+    // barriers: full_p / empty_p  load stage landed / released (MMAs done with the planes, converters with the
+    //                             weights, epilogue with constants and scales)
+    //           bfull / bfree     converted weight tile ready / consumed by the MMAs
+    //           tfull / tfree     TMEM slot written by the MMAs / read by the epilogue
+    auto full_p = [&](int s) { return bar0 + 8u * s; };
+    auto empty_p = [&](int s) { return bar0 + 8u * (3 + s); };
+    auto bfull = [&](int c) { return bar0 + 8u * (6 + c); };
+    auto bfree = [&](int c) { return bar0 + 8u * (6 + kGemmBStages + c); };
+    auto tfull = [&](int t) { return bar0 + 8u * (6 + 2 * kGemmBStages + t); };
+    auto tfree = [&](int t) { return bar0 + 8u * (6 + 2 * kGemmBStages + kGemmSlots + t); };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.off_misc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.off_misc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nt = blockIdx.x, mt = blockIdx.y;
+    const int K = p.K, N = p.N, G = p.G, M = p.M;
+    const int gpk = L.gpk;
+    const int Gn = K / G;
+    const bool debug = p.dbg_group >= 0;
+    const int kb0 = debug ? p.dbg_group * G / kKBlock : 0;
+    const int nkb = debug ? 1 : p.kb_total;
+
+    auto groups_in = [&](int kb) { return (min(K, (kb + 1) * kKBlock) - kb * kKBlock) / G; };
+    auto stage_tx = [&](int kb) {
+        return static_cast<uint32_t>(3 * kPlaneImageBytes + kPackedTileBytes + groups_in(kb) * kGemmTileM * 16 +
+                                     (debug ? 0 : gpk * kGemmTileN * 2));
+    };
+    // read-only inputs of the call (weights, scales) may be fetched before the preceding kernel (the unfold) ends
+    auto issue_static = [&](int i, uint64_t pol_stream, uint64_t pol_keep) {
+        const int s = i % P, kb = kb0 + i;
+        const uint32_t dst = smem_addr(p_ring + s * L.stage_bytes);
+        mbar_arrive_expect_tx(full_p(s), stage_tx(kb));
+        bulk_g2s(dst + 3 * kPlaneImageBytes, p.w + (static_cast<size_t>(nt) * p.kb_total + kb) * kPackedTileBytes,
+                 kPackedTileBytes, full_p(s), pol_stream);
+        if (!debug) tma_load_2d(dst + L.off_scale, &tmap_s, nt * kGemmTileN, kb * gpk, full_p(s), pol_keep);
+    };
+    auto issue_dynamic = [&](int i, uint64_t pol_keep) {
+        const int s = i % P, kb = kb0 + i;
+        const uint32_t dst = smem_addr(p_ring + s * L.stage_bytes);
+        bulk_g2s(dst, p.planes + (static_cast<size_t>(mt) * p.kb_total + kb) * 3 * kPlaneImageBytes,
+                 3 * kPlaneImageBytes, full_p(s), pol_keep);
+        bulk_g2s(dst + L.off_const, p.consts + (static_cast<size_t>(mt) * Gn + kb * gpk) * kGemmTileM,
+                 groups_in(kb) * kGemmTileM * 16, full_p(s), pol_keep);
+    };
+
+    const int first = nkb < P ? nkb : P;
+    uint64_t pol_stream = 0, pol_keep = 0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P; ++s) {
+            mbar_init(full_p(s), 1);
+            mbar_init(empty_p(s), 1 + 4 + kGemmNumEpiWarps);
+        }
+        for (int c = 0; c < kGemmBStages; ++c) {
+            mbar_init(bfull(c), 4);
+            mbar_init(bfree(c), 1);
+        }
+        for (int t = 0; t < kGemmSlots; ++t) {
+            mbar_init(tfull(t), 1);
+            mbar_init(tfree(t), kGemmNumEpiWarps);
+        }
+        *abort_flag = 0;
+        mbar_fence_init();
+        pol_stream = l2_policy_evict_first();
+        pol_keep = l2_policy_evict_last();
+        prefetch_tensormap(&tmap_s);
+        pdl_launch_dependents();
+        for (int i = 0; i < first; ++i) issue_static(i, pol_stream, pol_keep);
+        pdl_wait();
+        for (int i = 0; i < first; ++i) issue_dynamic(i, pol_keep);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), 512);
+        tmem_relinquish();
+        tc_fence_before_sync();
+    }
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ================================================================ TMA producer
+        if (lane == 0) {
+            int issued = first;
+            for (; issued < nkb; ++issued) {
+                const int s = issued % P;
+                if (!mbar_wait(empty_p(s), ((issued / P) & 1) ^ 1, abort_flag, kSiteProducerEmpty)) break;
+                issue_static(issued, pol_stream, pol_keep);
+                issue_dynamic(issued, pol_keep);
+            }
+            for (int j = issued > P ? issued - P : 0; j < issued; ++j) mbar_wait_drain(full_p(j % P), (j / P) & 1);
+        }
+    } else if (warp == 1) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = (1u << 4) | (static_cast<uint32_t>(kGemmTileN >> 3) << 17) |
+                                       (static_cast<uint32_t>(kGemmTileM >> 4) << 24);
+            int u = 0;                                   // plane-accumulation unit counter (3 per group)
+            int last_u[kGemmSlots] = {-1, -1, -1, -1};
+            bool stop = false;
+            for (int i = 0; i < nkb && !stop; ++i) {
+                const int s = i % P, cb = i % kGemmBStages;
+                if (!mbar_wait(full_p(s), (i / P) & 1, abort_flag, kSiteMmaOperands)) break;
+                if (!mbar_wait(bfull(cb), (i / kGemmBStages) & 1, abort_flag, kSiteMmaOperands)) break;
+                tc_fence_after_sync();
+                const uint32_t plane_base = smem_addr(p_ring + s * L.stage_bytes);
+                const uint32_t w_base = smem_addr(b_ring + cb * (kGemmTileN * kKBlock));
+                const int ng = groups_in(kb0 + i);
+                for (int gg = 0; gg < ng && !stop; ++gg) {
+                    for (int pl = 0; pl < 3; ++pl, ++u) {
+                        const int t = u % kGemmSlots;
+                        if (!mbar_wait(tfree(t), ((u / kGemmSlots) & 1) ^ 1, abort_flag, kSiteMmaTmemEmpty)) {
+                            stop = true;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const uint32_t d = tmem_base + static_cast<uint32_t>(t * kGemmTileN);
+                        for (int ks = 0; ks < G / 32; ++ks) {
+                            const uint32_t kofs = static_cast<uint32_t>(gg * G + ks * 32);
+                            umma_f8f6f4(d, sdesc_kmajor_sw128(plane_base + pl * kPlaneImageBytes + kofs),
+                                        sdesc_kmajor_sw128(w_base + kofs), idesc, ks > 0 ? 1u : 0u);
+                        }
+                        umma_commit(tfull(t));
+                        last_u[t] = u;
+                    }
+                }
+                if (stop) break;
+                umma_commit(bfree(cb));
+                umma_commit(empty_p(s));
+            }
+            for (int t = 0; t < kGemmSlots; ++t)
+                if (last_u[t] >= 0) mbar_wait_drain(tfull(t), (last_u[t] / kGemmSlots) & 1);
+        }
+        __syncwarp();
+    } else if (warp < kGemmEpiWarp0) {
+        // ================================================================ int4 -> E4M3 converters
+        const int ct = threadIdx.x - kGemmConvWarp0 * 32;
+        for (int i = 0; i < nkb; ++i) {
+            const int s = i % P, cb = i % kGemmBStages;
+            if (!mbar_wait_warp(full_p(s), (i / P) & 1, abort_flag, kSiteConvFull)) break;
+            if (!mbar_wait_warp(bfree(cb), ((i / kGemmBStages) & 1) ^ 1, abort_flag, kSiteConvEmpty)) break;
+            const uint8_t *src = p_ring + s * L.stage_bytes + 3 * kPlaneImageBytes;
+            uint8_t *dst = b_ring + cb * (kGemmTileN * kKBlock);
+            convert_half_tile(src, dst, ct, 0);
+            convert_half_tile(src, dst, ct, 1);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bfull(cb));
+                mbar_arrive(empty_p(s));
+            }
+        }
+    } else {
+        // ================================================================ epilogue
+        pdl_wait();
+        const int ew = warp - kGemmEpiWarp0;             // 0..7
+        const int quarter = warp & 3;                    // TMEM lanes (rows) this warp may read
+        const int half = ew >> 2;                        // columns [64 half, 64 half + 64) of each slot
+        const int r = quarter * 32 + lane;               // row within the tile
+        const int m = mt * kGemmTileM + r;
+        float2 yacc[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) yacc[q] = make_float2(0.0f, 0.0f);
+        bool ok = true;
+        int u = 0;
+        for (int i = 0; i < nkb && ok; ++i) {
+            const int s = i % P, kb = kb0 + i;
+            if (!mbar_wait_warp(full_p(s), (i / P) & 1, abort_flag, kSiteEpiOperandsEmpty)) {
+                ok = false;
+                break;
+            }
+            const uint8_t *stage = p_ring + s * L.stage_bytes;
+            const int ng = groups_in(kb);
+            for (int gg = 0; gg < ng && ok; ++gg, u += 3) {
+                const float4 cr = reinterpret_cast<const float4 *>(stage + L.off_const)[gg * kGemmTileM + r];
+                const float2 a1 = make_float2(cr.x, cr.x), a2 = make_float2(cr.y, cr.y);
+                const float2 a3 = make_float2(cr.z, cr.z), nc = make_float2(-cr.w, -cr.w);
+                const uint8_t *srow = stage + L.off_scale + gg * kGemmTileN * 2;
+                int t[3];
+                for (int pl = 0; pl < 3 && ok; ++pl) {
+                    t[pl] = (u + pl) % kGemmSlots;
+                    ok = mbar_wait_warp(tfull(t[pl]), ((u + pl) / kGemmSlots) & 1, abort_flag, kSiteEpiTmemFull);
+                }
+                if (!ok) break;
+                tc_fence_after_sync();
+                const bool dbg_here = debug && kb * gpk + gg == p.dbg_group;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    const uint32_t col = static_cast<uint32_t>(half * 64 + ch * 16);
+                    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+                    uint32_t d1[16], d2[16], d3[16];
+                    tmem_ld16(tmem_base + lane_off + static_cast<uint32_t>(t[0] * kGemmTileN) + col, d1);
+                    tmem_ld16(tmem_base + lane_off + static_cast<uint32_t>(t[1] * kGemmTileN) + col, d2);
+                    tmem_ld16(tmem_base + lane_off + static_cast<uint32_t>(t[2] * kGemmTileN) + col, d3);
+                    tmem_wait_ld();
+                    reg_fence16(d1);
+                    reg_fence16(d2);
+                    reg_fence16(d3);
+                    if (debug) {
+                        if (dbg_here && m < M) {
+                            for (int q = 0; q < 16; ++q) {
+                                const int n = nt * kGemmTileN + col + q;
+                                if (n < N) {
+                                    // in debug runs the constant record holds the plane sums
+                                    p.dbg_y123[(static_cast<size_t>(0) * M + m) * N + n] =
+                                        __float2int_rn(__uint_as_float(d1[q]) - 8.0f * cr.x);
+                                    p.dbg_y123[(static_cast<size_t>(1) * M + m) * N + n] =
+                                        __float2int_rn(__uint_as_float(d2[q]) - 8.0f * cr.y);
+                                    p.dbg_y123[(static_cast<size_t>(2) * M + m) * N + n] =
+                                        __float2int_rn(__uint_as_float(d3[q]) - 8.0f * cr.z);
+                                }
+                            }
+                        }
+                        continue;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float2 sc = ld_scale2(srow + (col + 2 * q) * 2);
+                        const float2 v1 = make_float2(__uint_as_float(d1[2 * q]), __uint_as_float(d1[2 * q + 1]));
+                        const float2 v2 = make_float2(__uint_as_float(d2[2 * q]), __uint_as_float(d2[2 * q + 1]));
+                        const float2 v3 = make_float2(__uint_as_float(d3[2 * q]), __uint_as_float(d3[2 * q + 1]));
+                        float2 acc = __ffma2_rn(a1, v1, nc);
+                        acc = __ffma2_rn(a2, v2, acc);
+                        acc = __ffma2_rn(a3, v3, acc);
+                        yacc[ch * 8 + q] = __ffma2_rn(sc, acc, yacc[ch * 8 + q]);
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    for (int pl = 0; pl < 3; ++pl) mbar_arrive(tfree(t[pl]));
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_p(s));
+        }
+        if (ok && !debug && m < M) {
+            __half *yrow = p.y + static_cast<size_t>(m) * N;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                const int n = nt * kGemmTileN + half * 64 + c8 * 8;
+                if (n < N) {
+                    const uint4 o = make_uint4(pack_half2(yacc[c8 * 4 + 0]), pack_half2(yacc[c8 * 4 + 1]),
+                                               pack_half2(yacc[c8 * 4 + 2]), pack_half2(yacc[c8 * 4 + 3]));
+                    *reinterpret_cast<uint4 *>(yrow + n) = o;
+                }
+            }
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+}  // namespace wqbmm

@@ -1,5 +1,6 @@
 // C ABI of the A16W4 per-group MSD matmul for GB300 (declared and documented in include/wqbmm.h).
-// Host code: argument validation (no GPU needed), split-K planning, kernel launches on the caller's stream.
+// Host code: argument validation (no GPU needed), planning (small-M fused kernel with split-K, or large-M pre-pass
+// plus GEMM kernel), kernel launches on the caller's stream.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -7,6 +8,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "msd_gemm.cuh"
 #include "msd_kernels.cuh"
 #include "wqbmm.h"
 
@@ -22,6 +24,7 @@ struct DeviceInfo {
     bool supported = false;
     int sms = 0;
     bool smem_set[3] = {false, false, false};
+    bool gemm_smem_set = false;
 };
 
 std::mutex g_mutex;
@@ -51,8 +54,12 @@ wqbmm_status check_shape(const Shape &s) {
     return WQBMM_OK;
 }
 
-// Rows of x per CTA, the MMA N (three stacked planes padded to 16, 32 or 48 rows), and the split over K.
+constexpr int64_t kLargeM = 64;     // from this many rows on, x is unfolded once by a pre-pass (large-M path)
+
+// Small-M path: rows of x per CTA, the MMA N (three stacked planes padded to 16, 32 or 48 rows), the split over K.
+// Large-M path: 128-row x 128-column tiles, no split.
 struct Plan {
+    bool large;
     int m_sub, m_tiles, n_tiles, kb_total, splits, nmma, reduce;
 };
 
@@ -60,11 +67,19 @@ struct Plan {
 // slices become at most 8 cluster slices reduced on chip; more go through a global workspace.
 Plan make_plan(const Shape &s, int sms) {
     Plan p{};
+    p.n_tiles = static_cast<int>(ceil_div(s.N, kTileN));
+    p.kb_total = static_cast<int>(ceil_div(s.K, kKBlock));
+    if (s.M >= kLargeM) {
+        p.large = true;
+        p.m_tiles = static_cast<int>(ceil_div(s.M, kGemmTileM));
+        p.m_sub = kGemmTileM;
+        p.splits = 1;
+        p.reduce = kReduceNone;
+        return p;
+    }
     p.m_tiles = static_cast<int>(ceil_div(s.M, 16));
     p.m_sub = static_cast<int>(ceil_div(s.M, p.m_tiles));
     p.nmma = p.m_sub <= 5 ? 16 : (p.m_sub <= 10 ? 32 : 48);
-    p.n_tiles = static_cast<int>(ceil_div(s.N, kTileN));
-    p.kb_total = static_cast<int>(ceil_div(s.K, kKBlock));
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     const int64_t target = static_cast<int64_t>(kCtasPerSm) * sms;
     int64_t splits = 1;
@@ -79,7 +94,14 @@ Plan make_plan(const Shape &s, int sms) {
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
+// Large-M workspace: the plane tiles [m_tiles][kb][3][16 KB], then the constants [m_tiles][K/G][128] (float4).
+size_t planes_bytes(const Plan &p) { return static_cast<size_t>(p.m_tiles) * p.kb_total * 3 * kPlaneImageBytes; }
+size_t consts_bytes(const Shape &s, const Plan &p) {
+    return static_cast<size_t>(p.m_tiles) * (s.K / s.G) * kGemmTileM * kGemmConstRowBytes;
+}
+
 size_t workspace_for(const Shape &s, const Plan &p) {
+    if (p.large) return align256(planes_bytes(p)) + align256(consts_bytes(s, p));
     if (p.reduce != kReduceGlobal) return 0;
     return align256(static_cast<size_t>(p.splits) * s.M * s.N * sizeof(float)) +
            align256(static_cast<size_t>(p.m_tiles) * p.n_tiles * sizeof(uint32_t));
@@ -181,13 +203,101 @@ wqbmm_status launch_msd(const RunParams &rp, const Plan &plan, DeviceInfo *info,
     return WQBMM_OK;
 }
 
-wqbmm_status launch_plan(const RunParams &rp, const Plan &plan, DeviceInfo *info, cudaStream_t stream) {
+wqbmm_status launch_small(const RunParams &rp, const Plan &plan, DeviceInfo *info, cudaStream_t stream) {
     if (plan.m_tiles > 65535 || plan.splits > 65535) return WQBMM_ERR_INVALID;
     switch (plan.nmma) {
         case 16: return launch_msd<16>(rp, plan, info, stream);
         case 32: return launch_msd<32>(rp, plan, info, stream);
         default: return launch_msd<48>(rp, plan, info, stream);
     }
+}
+
+// Large-M path: the unfold pre-pass writes plane tiles and constants into the workspace, then the GEMM kernel runs
+// under programmatic launch (it fetches weights and scales while the pre-pass finishes).
+wqbmm_status launch_large(const Shape &s, const Plan &plan, const void *x, const void *w, const void *scale, void *y,
+                          void *workspace, int dbg_group, int32_t *dbg_y123, DeviceInfo *info, cudaStream_t stream) {
+    if (plan.m_tiles > 65535) return WQBMM_ERR_INVALID;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (!info->gemm_smem_set) {
+            if (cudaFuncSetAttribute(msd_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemLimit) !=
+                cudaSuccess)
+                return WQBMM_ERR_CUDA;
+            info->gemm_smem_set = true;
+        }
+    }
+    uint8_t *planes = static_cast<uint8_t *>(workspace);
+    float4 *consts = reinterpret_cast<float4 *>(planes + align256(planes_bytes(plan)));
+    const dim3 ugrid(static_cast<unsigned>(plan.m_tiles * kGemmTileM / 8), static_cast<unsigned>(plan.kb_total));
+    unfold_planes_kernel<<<ugrid, 256, 0, stream>>>(static_cast<const __half *>(x), static_cast<int>(s.M),
+                                                    static_cast<int>(s.K), static_cast<int>(s.G), plan.kb_total,
+                                                    planes, consts, dbg_group >= 0 ? 1 : 0);
+    if (cudaPeekAtLastError() != cudaSuccess) return WQBMM_ERR_CUDA;
+    CUtensorMap tmap_s{};
+    if (dbg_group < 0 &&
+        !fp16_tensor_map(&tmap_s, scale, s.K / s.G, s.N, static_cast<int>(kKBlock / s.G), kGemmTileN))
+        return WQBMM_ERR_CUDA;
+    GemmParams gp{};
+    gp.w = static_cast<const uint8_t *>(w);
+    gp.planes = planes;
+    gp.consts = consts;
+    gp.y = static_cast<__half *>(y);
+    gp.dbg_y123 = dbg_y123;
+    gp.M = static_cast<int>(s.M);
+    gp.K = static_cast<int>(s.K);
+    gp.N = static_cast<int>(s.N);
+    gp.G = static_cast<int>(s.G);
+    gp.m_tiles = plan.m_tiles;
+    gp.n_tiles = plan.n_tiles;
+    gp.kb_total = plan.kb_total;
+    gp.dbg_group = dbg_group;
+    const GemmLayout L(gp.G);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(plan.n_tiles, plan.m_tiles, 1);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = L.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, msd_gemm_kernel, gp, tmap_s) == cudaSuccess ? WQBMM_OK : WQBMM_ERR_CUDA;
+}
+
+// Launches one product (or, with dbg_group >= 0, the integer partials of one group) planned by `plan` on the current
+// device. `workspace` holds workspace_for(shape, plan) bytes; `clear_counters` clears the split-K counters first.
+wqbmm_status dispatch(const void *x, const void *w, const void *scale, void *y, const Shape &s, const Plan &plan,
+                      void *workspace, bool clear_counters, int dbg_group, int32_t *dbg_y123, DeviceInfo *info,
+                      cudaStream_t stream) {
+    if (plan.large) return launch_large(s, plan, x, w, scale, y, workspace, dbg_group, dbg_y123, info, stream);
+    RunParams rp{};
+    rp.x = static_cast<const __half *>(x);
+    rp.w = static_cast<const uint8_t *>(w);
+    rp.scale = static_cast<const __half *>(scale);
+    rp.y = static_cast<__half *>(y);
+    rp.dbg_y123 = dbg_y123;
+    if (plan.reduce == kReduceGlobal) {
+        const size_t counters_at = align256(static_cast<size_t>(plan.splits) * s.M * s.N * sizeof(float));
+        rp.ws_part = static_cast<float *>(workspace);
+        rp.ws_count = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) + counters_at);
+        if (clear_counters &&
+            cudaMemsetAsync(rp.ws_count, 0, static_cast<size_t>(plan.m_tiles) * plan.n_tiles * sizeof(uint32_t),
+                            stream) != cudaSuccess)
+            return WQBMM_ERR_CUDA;
+    }
+    rp.M = static_cast<int>(s.M);
+    rp.K = static_cast<int>(s.K);
+    rp.N = static_cast<int>(s.N);
+    rp.G = static_cast<int>(s.G);
+    rp.m_sub = plan.m_sub;
+    rp.n_tiles = plan.n_tiles;
+    rp.m_tiles = plan.m_tiles;
+    rp.splits = plan.splits;
+    rp.kb_total = plan.kb_total;
+    rp.reduce = plan.reduce;
+    rp.dbg_group = dbg_group;
+    return launch_small(rp, plan, info, stream);
 }
 
 // Scratch for wqbmm_run_static_scratch: a fixed device array instead of a caller workspace. Host code must not
@@ -272,38 +382,16 @@ wqbmm_status wqbmm_run(const void *x, const void *w_prepacked, const void *antiq
     if (st != WQBMM_OK) return st;
     if (!aligned16(x) || !aligned16(w_prepacked) || !aligned16(antiquant_scale) || !aligned16(y))
         return WQBMM_ERR_INVALID;
+    // the plan for this device never needs more workspace than wqbmm_workspace_bytes reports
+    if (workspace_for(s, make_plan(s, kPlanSms)) > 0 && !workspace) return WQBMM_ERR_NULLPTR;
+    if (workspace && !aligned16(workspace)) return WQBMM_ERR_INVALID;
     int dev;
     DeviceInfo *info;
-    // the plan for this device never needs more workspace than wqbmm_workspace_bytes reports
-    const Plan worst = make_plan(s, kPlanSms);
-    if (workspace_for(s, worst) > 0 && !workspace) return WQBMM_ERR_NULLPTR;
-    if (workspace && !aligned16(workspace)) return WQBMM_ERR_INVALID;
     if ((st = current_device(&dev, &info)) != WQBMM_OK) return st;
     const Plan plan = make_plan(s, info->sms < kPlanSms ? info->sms : kPlanSms);
-    const size_t need = workspace_for(s, plan);
-    if (workspace_bytes < need) return WQBMM_ERR_INVALID;
-    RunParams rp{};
-    rp.x = static_cast<const __half *>(x);
-    rp.w = static_cast<const uint8_t *>(w_prepacked);
-    rp.scale = static_cast<const __half *>(antiquant_scale);
-    rp.y = static_cast<__half *>(y);
-    if (plan.reduce == kReduceGlobal) {
-        rp.ws_part = static_cast<float *>(workspace);
-        rp.ws_count = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) +
-                                                   align256(static_cast<size_t>(plan.splits) * M * N * sizeof(float)));
-    }
-    rp.M = static_cast<int>(M);
-    rp.K = static_cast<int>(K);
-    rp.N = static_cast<int>(N);
-    rp.G = static_cast<int>(G);
-    rp.m_sub = plan.m_sub;
-    rp.n_tiles = plan.n_tiles;
-    rp.m_tiles = plan.m_tiles;
-    rp.splits = plan.splits;
-    rp.kb_total = plan.kb_total;
-    rp.reduce = plan.reduce;
-    rp.dbg_group = -1;
-    return launch_plan(rp, plan, info, reinterpret_cast<cudaStream_t>(stream));
+    if (workspace_bytes < workspace_for(s, plan)) return WQBMM_ERR_INVALID;
+    return dispatch(x, w_prepacked, antiquant_scale, y, s, plan, workspace, false, -1, nullptr, info,
+                    reinterpret_cast<cudaStream_t>(stream));
 }
 
 wqbmm_status wqbmm_run_static_scratch(const void *x, const void *w_prepacked, const void *antiquant_scale, void *y,
@@ -320,35 +408,11 @@ wqbmm_status wqbmm_run_static_scratch(const void *x, const void *w_prepacked, co
     const Plan plan = make_plan(s, info->sms < kPlanSms ? info->sms : kPlanSms);
     const size_t need = workspace_for(s, plan);
     if (need > kStaticScratchBytes) return WQBMM_ERR_SCRATCH_LIMIT;
-    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    RunParams rp{};
-    if (plan.reduce == kReduceGlobal) {
-        void *base = nullptr;
-        if ((st = static_scratch_address(dev, &base)) != WQBMM_OK) return st;
-        const size_t counters_at = align256(static_cast<size_t>(plan.splits) * M * N * sizeof(float));
-        const size_t counters_bytes = static_cast<size_t>(plan.m_tiles) * plan.n_tiles * sizeof(uint32_t);
-        // the array keeps whatever the previous call (of any shape) left there: the counters must start at zero
-        if (cudaMemsetAsync(static_cast<uint8_t *>(base) + counters_at, 0, counters_bytes, cs) != cudaSuccess)
-            return WQBMM_ERR_CUDA;
-        rp.ws_part = static_cast<float *>(base);
-        rp.ws_count = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(base) + counters_at);
-    }
-    rp.x = static_cast<const __half *>(x);
-    rp.w = static_cast<const uint8_t *>(w_prepacked);
-    rp.scale = static_cast<const __half *>(antiquant_scale);
-    rp.y = static_cast<__half *>(y);
-    rp.M = static_cast<int>(M);
-    rp.K = static_cast<int>(K);
-    rp.N = static_cast<int>(N);
-    rp.G = static_cast<int>(G);
-    rp.m_sub = plan.m_sub;
-    rp.n_tiles = plan.n_tiles;
-    rp.m_tiles = plan.m_tiles;
-    rp.splits = plan.splits;
-    rp.kb_total = plan.kb_total;
-    rp.reduce = plan.reduce;
-    rp.dbg_group = -1;
-    return launch_plan(rp, plan, info, cs);
+    void *base = nullptr;
+    if (need > 0 && (st = static_scratch_address(dev, &base)) != WQBMM_OK) return st;
+    // the array keeps whatever the previous call (of any shape) left there: split-K counters are cleared first
+    return dispatch(x, w_prepacked, antiquant_scale, y, s, plan, base, true, -1, nullptr, info,
+                    reinterpret_cast<cudaStream_t>(stream));
 }
 
 wqbmm_status wqbmm_debug_unfold(const void *x, int64_t M, int64_t K, int64_t G, int8_t *planes, float *amax,
@@ -369,35 +433,29 @@ wqbmm_status wqbmm_debug_unfold(const void *x, int64_t M, int64_t K, int64_t G, 
 }
 
 wqbmm_status wqbmm_debug_group_partials(const void *x, const void *w_prepacked, int64_t M, int64_t K, int64_t N,
-                                        int64_t G, int64_t g, int32_t *y123, wqbmm_stream_t stream) {
+                                        int64_t G, int64_t g, int32_t *y123, void *workspace, size_t workspace_bytes,
+                                        wqbmm_stream_t stream) {
     if (!x || !w_prepacked || !y123) return WQBMM_ERR_NULLPTR;
     const Shape s{M, K, N, G};
     wqbmm_status st = check_shape(s);
     if (st != WQBMM_OK) return st;
     if (g < 0 || g >= K / G) return WQBMM_ERR_INVALID;
     if (!aligned16(x) || !aligned16(w_prepacked)) return WQBMM_ERR_INVALID;
+    if (workspace && !aligned16(workspace)) return WQBMM_ERR_INVALID;
+    if (M >= kLargeM) {                                 // the large-M plan does not depend on the SM count
+        if (!workspace) return WQBMM_ERR_NULLPTR;
+        if (workspace_bytes < workspace_for(s, make_plan(s, kPlanSms))) return WQBMM_ERR_INVALID;
+    }
     int dev;
     DeviceInfo *info;
     if ((st = current_device(&dev, &info)) != WQBMM_OK) return st;
-    Plan plan = make_plan(s, info->sms);
-    plan.splits = 1;
-    plan.reduce = kReduceNone;
-    RunParams rp{};
-    rp.x = static_cast<const __half *>(x);
-    rp.w = static_cast<const uint8_t *>(w_prepacked);
-    rp.dbg_y123 = y123;
-    rp.M = static_cast<int>(M);
-    rp.K = static_cast<int>(K);
-    rp.N = static_cast<int>(N);
-    rp.G = static_cast<int>(G);
-    rp.m_sub = plan.m_sub;
-    rp.n_tiles = plan.n_tiles;
-    rp.m_tiles = plan.m_tiles;
-    rp.splits = 1;
-    rp.kb_total = plan.kb_total;
-    rp.reduce = kReduceNone;
-    rp.dbg_group = static_cast<int>(g);
-    return launch_plan(rp, plan, info, reinterpret_cast<cudaStream_t>(stream));
+    Plan plan = make_plan(s, info->sms < kPlanSms ? info->sms : kPlanSms);
+    if (!plan.large) {                                  // the group's own k-block only, no split
+        plan.splits = 1;
+        plan.reduce = kReduceNone;
+    }
+    return dispatch(x, w_prepacked, nullptr, nullptr, s, plan, workspace, false, static_cast<int>(g), y123, info,
+                    reinterpret_cast<cudaStream_t>(stream));
 }
 
 wqbmm_status wqbmm_read_device_status(int32_t *code, int clear, wqbmm_stream_t stream) {
