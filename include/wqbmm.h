@@ -68,9 +68,9 @@ typedef enum {
 /*
  * Size in bytes of the prepacked weight buffer for a K x N int4 weight. Host only; no GPU needed.
  * Layout (for reference; callers treat it as opaque): tiles of 128 output columns x 128 k, tile (nt, kb) at byte
- * offset (nt * ceil(K/128) + kb) * 8192; inside a tile, row r (column n = 128 nt + r) holds 64 bytes with k = 128 kb
- * + 2j in the low nibble and k + 1 in the high nibble of byte j, each stored as w + 8 (offset binary, 0..15); padding
- * holds w = 0. Total = ceil(N/128) * ceil(K/128) * 8192 bytes.
+ * offset (nt * ceil(K/128) + kb) * 8192; inside a tile, row r (column n = 128 nt + r) holds 64 bytes, byte 4q + b
+ * (q = 0..15, b = 0..3) with k = 128 kb + 8q + b in the low nibble and k + 4 in the high nibble, each stored as w + 8
+ * (offset binary, 0..15); padding holds w = 0. Total = ceil(N/128) * ceil(K/128) * 8192 bytes.
  * Errors: WQBMM_ERR_NULLPTR if bytes is null; WQBMM_ERR_INVALID if the shape rules fail.
  */
 WQBMM_API wqbmm_status wqbmm_prepacked_weight_bytes(int64_t K, int64_t N, int64_t G, size_t *bytes);

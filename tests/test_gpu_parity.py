@@ -71,7 +71,10 @@ def prepack_layout(wp, K, N):
     padded = np.zeros((kb * 64, nt * 128), dtype=np.uint8)
     padded[:K // 2, :N] = wp
     padded ^= 0x88
-    return padded.reshape(kb, 64, nt, 128).transpose(2, 0, 3, 1).reshape(-1)
+    u = np.stack([padded & 0xF, padded >> 4], axis=1).reshape(kb * 128, nt * 128)      # u[k, n] = w + 8
+    u = u.reshape(kb, 16, 2, 4, nt, 128)                                               # k = 128 kb + 8q + 4h + b
+    byte = u[:, :, 0] | (u[:, :, 1] << 4)                                              # [kb, q, b, nt, 128]
+    return byte.reshape(kb, 64, nt, 128).transpose(2, 0, 3, 1).reshape(-1)
 
 
 # ------------------------------------------------------------------------------------------- prepack

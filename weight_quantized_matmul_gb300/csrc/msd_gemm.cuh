@@ -9,8 +9,9 @@
 //                         operand (M = 128 rows of x), the int4 weights converted to E4M3 the B operand (N = 128
 //                         columns); each plane of each K-group accumulates in its own 128-column TMEM slot (four
 //                         slots rotate, so the next group's first plane overlaps the epilogue of this group)
-// Roles in msd_gemm_kernel (448 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA issuer, warps 2-5 int4 ->
-// E4M3 converters, warps 6-13 epilogue (two warps per TMEM lane quarter, 64 columns each, packed FP32x2 math).
+// Roles in msd_gemm_kernel (384 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA issuer, warps 2-3 int4 ->
+// E4M3 converters (and fp16 -> fp32 scales), warps 4-11 epilogue (two warps per TMEM lane quarter, 64 columns each,
+// packed FP32x2 math).
 #pragma once
 
 #include "msd_kernels.cuh"
@@ -19,9 +20,10 @@ namespace wqbmm {
 
 constexpr int kGemmTileM = 128;
 constexpr int kGemmTileN = 128;
-constexpr int kGemmThreads = 448;
+constexpr int kGemmThreads = 384;                              // 12 warps: 3 per SM sub-partition, 168 registers
 constexpr int kGemmConvWarp0 = 2;
-constexpr int kGemmEpiWarp0 = 6;
+constexpr int kGemmNumConvWarps = 2;
+constexpr int kGemmEpiWarp0 = 4;
 constexpr int kGemmNumEpiWarps = 8;
 constexpr int kGemmBStages = 2;
 constexpr int kGemmSlots = 4;                                  // TMEM accumulator slots of 128 columns
@@ -32,23 +34,24 @@ constexpr int kGemmSmemLimit = 232448;                         // opt-in shared 
 // Shared-memory layout of msd_gemm_kernel (depends on the group size through the groups per k-block).
 struct GemmLayout {
     int gpk, const_bytes, scale_bytes, stage_bytes, p_stages;
-    int off_const, off_scale, off_p, off_b, off_bar, off_misc, smem_bytes;
+    int off_const, off_scale, off_scale32, off_p, off_b, off_bar, off_misc, smem_bytes;
     __host__ __device__ static int align(int v, int a) { return (v + a - 1) / a * a; }
     __host__ __device__ explicit GemmLayout(int G) {
         gpk = kKBlock / G;
         const_bytes = gpk * kGemmTileM * kGemmConstRowBytes;
         scale_bytes = gpk * kGemmTileN * 2;
-        // stage: three plane images | packed weight tile | constants | scale tile
+        // stage: three plane images | packed weight tile | constants | scale tile (fp16, as loaded) | scale (fp32)
         off_const = 3 * kPlaneImageBytes + kPackedTileBytes;
         off_scale = off_const + const_bytes;
-        stage_bytes = align(off_scale + scale_bytes, 1024);
+        off_scale32 = off_scale + scale_bytes;
+        stage_bytes = align(off_scale32 + 2 * scale_bytes, 1024);
         off_b = 0;                                             // converted weights ring first (1024-aligned)
         off_p = kGemmBStages * (kGemmTileN * kKBlock);
         const int fixed = off_p + 1024 /*align slack*/ + 512 /*barriers and flags*/;
         p_stages = (kGemmSmemLimit - fixed) / stage_bytes;
         if (p_stages > 3) p_stages = 3;
         off_bar = off_p + p_stages * stage_bytes;
-        off_misc = off_bar + 8 * (2 * 3 + 2 * kGemmBStages + 2 * kGemmSlots);
+        off_misc = off_bar + 8 * (3 * 3 + 2 * kGemmBStages + 2 * kGemmSlots);
         smem_bytes = off_misc + 64 + 1024;
     }
 };
@@ -100,7 +103,7 @@ __global__ void __launch_bounds__(256) unfold_planes_kernel(const __half *__rest
             rec = make_float4(static_cast<float>(s1), static_cast<float>(s2), static_cast<float>(s3), 0.0f);
         } else {
             const float c1 = kC1 * am, c2 = kC2 * am, c3 = kC3 * am;
-            rec = make_float4(c1, c2, c3, 8.0f * (c1 * s1 + c2 * s2 + c3 * s3));
+            rec = make_float4(kMmaUnit * c1, kMmaUnit * c2, kMmaUnit * c3, 8.0f * (c1 * s1 + c2 * s2 + c3 * s3));
         }
         consts[(static_cast<size_t>(mt) * Gn + g) * kGemmTileM + r] = rec;
     }
@@ -115,6 +118,9 @@ __device__ __forceinline__ uint32_t pack_half2(float2 v) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// kDebug: only the k-block of group p.dbg_group runs, the constant records hold the plane sums, and the epilogue
+// writes that group's integer partials instead of y.
+template <bool kDebug>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     msd_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmap_s) {
     const GemmLayout L(p.G);
@@ -126,14 +132,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t bar0 = smem_addr(smem + L.off_bar);
     // barriers: full_p / empty_p  load stage landed / released (MMAs done with the planes, converters with the
     //                             weights, epilogue with constants and scales)
+    //           sready            scales of the stage converted to fp32 (the epilogue's view of the stage)
     //           bfull / bfree     converted weight tile ready / consumed by the MMAs
     //           tfull / tfree     TMEM slot written by the MMAs / read by the epilogue
     auto full_p = [&](int s) { return bar0 + 8u * s; };
     auto empty_p = [&](int s) { return bar0 + 8u * (3 + s); };
-    auto bfull = [&](int c) { return bar0 + 8u * (6 + c); };
-    auto bfree = [&](int c) { return bar0 + 8u * (6 + kGemmBStages + c); };
-    auto tfull = [&](int t) { return bar0 + 8u * (6 + 2 * kGemmBStages + t); };
-    auto tfree = [&](int t) { return bar0 + 8u * (6 + 2 * kGemmBStages + kGemmSlots + t); };
+    auto sready = [&](int s) { return bar0 + 8u * (6 + s); };
+    auto bfull = [&](int c) { return bar0 + 8u * (9 + c); };
+    auto bfree = [&](int c) { return bar0 + 8u * (9 + kGemmBStages + c); };
+    auto tfull = [&](int t) { return bar0 + 8u * (9 + 2 * kGemmBStages + t); };
+    auto tfree = [&](int t) { return bar0 + 8u * (9 + 2 * kGemmBStages + kGemmSlots + t); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.off_misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.off_misc + 4);
 
@@ -142,14 +150,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int K = p.K, N = p.N, G = p.G, M = p.M;
     const int gpk = L.gpk;
     const int Gn = K / G;
-    const bool debug = p.dbg_group >= 0;
-    const int kb0 = debug ? p.dbg_group * G / kKBlock : 0;
-    const int nkb = debug ? 1 : p.kb_total;
+    const int kb0 = kDebug ? p.dbg_group * G / kKBlock : 0;
+    const int nkb = kDebug ? 1 : p.kb_total;
 
     auto groups_in = [&](int kb) { return (min(K, (kb + 1) * kKBlock) - kb * kKBlock) / G; };
     auto stage_tx = [&](int kb) {
         return static_cast<uint32_t>(3 * kPlaneImageBytes + kPackedTileBytes + groups_in(kb) * kGemmTileM * 16 +
-                                     (debug ? 0 : gpk * kGemmTileN * 2));
+                                     (kDebug ? 0 : gpk * kGemmTileN * 2));
     };
     // read-only inputs of the call (weights, scales) may be fetched before the preceding kernel (the unfold) ends
     auto issue_static = [&](int i, uint64_t pol_stream, uint64_t pol_keep) {
@@ -158,7 +165,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mbar_arrive_expect_tx(full_p(s), stage_tx(kb));
         bulk_g2s(dst + 3 * kPlaneImageBytes, p.w + (static_cast<size_t>(nt) * p.kb_total + kb) * kPackedTileBytes,
                  kPackedTileBytes, full_p(s), pol_stream);
-        if (!debug) tma_load_2d(dst + L.off_scale, &tmap_s, nt * kGemmTileN, kb * gpk, full_p(s), pol_keep);
+        if (!kDebug) tma_load_2d(dst + L.off_scale, &tmap_s, nt * kGemmTileN, kb * gpk, full_p(s), pol_keep);
     };
     auto issue_dynamic = [&](int i, uint64_t pol_keep) {
         const int s = i % P, kb = kb0 + i;
@@ -174,10 +181,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < P; ++s) {
             mbar_init(full_p(s), 1);
-            mbar_init(empty_p(s), 1 + 4 + kGemmNumEpiWarps);
+            mbar_init(empty_p(s), 1 + kGemmNumConvWarps + kGemmNumEpiWarps);
+            mbar_init(sready(s), kGemmNumConvWarps);
         }
         for (int c = 0; c < kGemmBStages; ++c) {
-            mbar_init(bfull(c), 4);
+            mbar_init(bfull(c), kGemmNumConvWarps);
             mbar_init(bfree(c), 1);
         }
         for (int t = 0; t < kGemmSlots; ++t) {
@@ -258,16 +266,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         __syncwarp();
     } else if (warp < kGemmEpiWarp0) {
-        // ================================================================ int4 -> E4M3 converters
+        // ================================================================ int4 -> E4M3 converters, scales to fp32
         const int ct = threadIdx.x - kGemmConvWarp0 * 32;
+        constexpr int kConvThreads = kGemmNumConvWarps * 32;
         for (int i = 0; i < nkb; ++i) {
             const int s = i % P, cb = i % kGemmBStages;
             if (!mbar_wait_warp(full_p(s), (i / P) & 1, abort_flag, kSiteConvFull)) break;
+            uint8_t *stage = p_ring + s * L.stage_bytes;
+            if (!kDebug) {
+                const __half2 *s16 = reinterpret_cast<const __half2 *>(stage + L.off_scale);
+                float2 *s32 = reinterpret_cast<float2 *>(stage + L.off_scale32);
+                for (int j = ct; j < gpk * kGemmTileN / 2; j += kConvThreads) s32[j] = __half22float2(s16[j]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sready(s));
+            }
             if (!mbar_wait_warp(bfree(cb), ((i / kGemmBStages) & 1) ^ 1, abort_flag, kSiteConvEmpty)) break;
-            const uint8_t *src = p_ring + s * L.stage_bytes + 3 * kPlaneImageBytes;
-            uint8_t *dst = b_ring + cb * (kGemmTileN * kKBlock);
-            convert_half_tile(src, dst, ct, 0);
-            convert_half_tile(src, dst, ct, 1);
+            convert_tile(stage + 3 * kPlaneImageBytes, b_ring + cb * (kGemmTileN * kKBlock), ct, kConvThreads);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -283,6 +297,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int half = ew >> 2;                        // columns [64 half, 64 half + 64) of each slot
         const int r = quarter * 32 + lane;               // row within the tile
         const int m = mt * kGemmTileM + r;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         float2 yacc[32];
 #pragma unroll
         for (int q = 0; q < 32; ++q) yacc[q] = make_float2(0.0f, 0.0f);
@@ -290,75 +305,89 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int u = 0;
         for (int i = 0; i < nkb && ok; ++i) {
             const int s = i % P, kb = kb0 + i;
-            if (!mbar_wait_warp(full_p(s), (i / P) & 1, abort_flag, kSiteEpiOperandsEmpty)) {
-                ok = false;
-                break;
-            }
+            // the epilogue reads constants (landed with the stage) and fp32 scales (written by the converters)
+            ok = kDebug ? mbar_wait_warp(full_p(s), (i / P) & 1, abort_flag, kSiteEpiOperandsEmpty)
+                        : mbar_wait_warp(sready(s), (i / P) & 1, abort_flag, kSiteEpiOperandsEmpty);
+            if (!ok) break;
             const uint8_t *stage = p_ring + s * L.stage_bytes;
             const int ng = groups_in(kb);
-            for (int gg = 0; gg < ng && ok; ++gg, u += 3) {
+            for (int gg = 0; gg < ng; ++gg, u += 3) {
                 const float4 cr = reinterpret_cast<const float4 *>(stage + L.off_const)[gg * kGemmTileM + r];
-                const float2 a1 = make_float2(cr.x, cr.x), a2 = make_float2(cr.y, cr.y);
-                const float2 a3 = make_float2(cr.z, cr.z), nc = make_float2(-cr.w, -cr.w);
-                const uint8_t *srow = stage + L.off_scale + gg * kGemmTileN * 2;
-                int t[3];
-                for (int pl = 0; pl < 3 && ok; ++pl) {
-                    t[pl] = (u + pl) % kGemmSlots;
-                    ok = mbar_wait_warp(tfull(t[pl]), ((u + pl) / kGemmSlots) & 1, abort_flag, kSiteEpiTmemFull);
-                }
+                const int t0 = u % kGemmSlots, t1 = (u + 1) % kGemmSlots, t2 = (u + 2) % kGemmSlots;
+                // the three planes were committed in order: the last one's completion covers all three
+                ok = mbar_wait_warp(tfull(t2), ((u + 2) / kGemmSlots) & 1, abort_flag, kSiteEpiTmemFull);
                 if (!ok) break;
                 tc_fence_after_sync();
-                const bool dbg_here = debug && kb * gpk + gg == p.dbg_group;
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    const uint32_t col = static_cast<uint32_t>(half * 64 + ch * 16);
-                    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-                    uint32_t d1[16], d2[16], d3[16];
-                    tmem_ld16(tmem_base + lane_off + static_cast<uint32_t>(t[0] * kGemmTileN) + col, d1);
-                    tmem_ld16(tmem_base + lane_off + static_cast<uint32_t>(t[1] * kGemmTileN) + col, d2);
-                    tmem_ld16(tmem_base + lane_off + static_cast<uint32_t>(t[2] * kGemmTileN) + col, d3);
-                    tmem_wait_ld();
-                    reg_fence16(d1);
-                    reg_fence16(d2);
-                    reg_fence16(d3);
-                    if (debug) {
-                        if (dbg_here && m < M) {
-                            for (int q = 0; q < 16; ++q) {
-                                const int n = nt * kGemmTileN + col + q;
-                                if (n < N) {
-                                    // in debug runs the constant record holds the plane sums
-                                    p.dbg_y123[(static_cast<size_t>(0) * M + m) * N + n] =
-                                        __float2int_rn(__uint_as_float(d1[q]) - 8.0f * cr.x);
-                                    p.dbg_y123[(static_cast<size_t>(1) * M + m) * N + n] =
-                                        __float2int_rn(__uint_as_float(d2[q]) - 8.0f * cr.y);
-                                    p.dbg_y123[(static_cast<size_t>(2) * M + m) * N + n] =
-                                        __float2int_rn(__uint_as_float(d3[q]) - 8.0f * cr.z);
+                const uint32_t a0 = tmem_base + lane_off + static_cast<uint32_t>(t0 * kGemmTileN + half * 64);
+                const uint32_t a1p = tmem_base + lane_off + static_cast<uint32_t>(t1 * kGemmTileN + half * 64);
+                const uint32_t a2p = tmem_base + lane_off + static_cast<uint32_t>(t2 * kGemmTileN + half * 64);
+                if (kDebug) {
+                    if (kb * gpk + gg == p.dbg_group) {
+#pragma unroll 1
+                        for (int ch = 0; ch < 4; ++ch) {
+                            uint32_t d1[16], d2[16], d3[16];
+                            tmem_ld16(a0 + ch * 16, d1);
+                            tmem_ld16(a1p + ch * 16, d2);
+                            tmem_ld16(a2p + ch * 16, d3);
+                            tmem_wait_ld();
+                            if (m < M) {
+                                for (int q = 0; q < 16; ++q) {
+                                    const int n = nt * kGemmTileN + half * 64 + ch * 16 + q;
+                                    if (n < N) {
+                                        // in debug runs the constant record holds the plane sums
+                                        p.dbg_y123[(static_cast<size_t>(0) * M + m) * N + n] =
+                                            __float2int_rn(kMmaUnit * __uint_as_float(d1[q]) - 8.0f * cr.x);
+                                        p.dbg_y123[(static_cast<size_t>(1) * M + m) * N + n] =
+                                            __float2int_rn(kMmaUnit * __uint_as_float(d2[q]) - 8.0f * cr.y);
+                                        p.dbg_y123[(static_cast<size_t>(2) * M + m) * N + n] =
+                                            __float2int_rn(kMmaUnit * __uint_as_float(d3[q]) - 8.0f * cr.z);
+                                    }
                                 }
                             }
                         }
-                        continue;
                     }
+                } else {
+                    const float2 c1 = make_float2(cr.x, cr.x), c2 = make_float2(cr.y, cr.y);
+                    const float2 c3 = make_float2(cr.z, cr.z), nc = make_float2(-cr.w, -cr.w);
+                    const float4 *srow =
+                        reinterpret_cast<const float4 *>(stage + L.off_scale32) + (gg * kGemmTileN + half * 64) / 4;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float2 sc = ld_scale2(srow + (col + 2 * q) * 2);
-                        const float2 v1 = make_float2(__uint_as_float(d1[2 * q]), __uint_as_float(d1[2 * q + 1]));
-                        const float2 v2 = make_float2(__uint_as_float(d2[2 * q]), __uint_as_float(d2[2 * q + 1]));
-                        const float2 v3 = make_float2(__uint_as_float(d3[2 * q]), __uint_as_float(d3[2 * q + 1]));
-                        float2 acc = __ffma2_rn(a1, v1, nc);
-                        acc = __ffma2_rn(a2, v2, acc);
-                        acc = __ffma2_rn(a3, v3, acc);
-                        yacc[ch * 8 + q] = __ffma2_rn(sc, acc, yacc[ch * 8 + q]);
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint32_t d1[16], d2[16], d3[16];
+                        tmem_ld16(a0 + ch * 16, d1);
+                        tmem_ld16(a1p + ch * 16, d2);
+                        tmem_ld16(a2p + ch * 16, d3);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const float4 sc = srow[ch * 4 + q4];           // same address in every lane: broadcast
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int q = q4 * 2 + h;
+                                const float2 scv = h == 0 ? make_float2(sc.x, sc.y) : make_float2(sc.z, sc.w);
+                                const float2 v1 = make_float2(__uint_as_float(d1[2 * q]), __uint_as_float(d1[2 * q + 1]));
+                                const float2 v2 = make_float2(__uint_as_float(d2[2 * q]), __uint_as_float(d2[2 * q + 1]));
+                                const float2 v3 = make_float2(__uint_as_float(d3[2 * q]), __uint_as_float(d3[2 * q + 1]));
+                                float2 acc = __ffma2_rn(c1, v1, nc);
+                                acc = __ffma2_rn(c2, v2, acc);
+                                acc = __ffma2_rn(c3, v3, acc);
+                                yacc[ch * 8 + q] = __ffma2_rn(scv, acc, yacc[ch * 8 + q]);
+                            }
+                        }
                     }
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0)
-                    for (int pl = 0; pl < 3; ++pl) mbar_arrive(tfree(t[pl]));
+                if (lane == 0) {
+                    mbar_arrive(tfree(t0));
+                    mbar_arrive(tfree(t1));
+                    mbar_arrive(tfree(t2));
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_p(s));
         }
-        if (ok && !debug && m < M) {
+        if (!kDebug && ok && m < M) {
             __half *yrow = p.y + static_cast<size_t>(m) * N;
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) {

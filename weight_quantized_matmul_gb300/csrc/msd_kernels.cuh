@@ -183,31 +183,35 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int kbyte) {
 
 // ------------------------------------------------------------------------------------------------ int4 -> e4m3
 
-// E4M3 encodings of 0..7 and 8..15 (bytes little-endian in each word)
-constexpr uint32_t kLut0to3 = 0x44403800u, kLut4to7 = 0x4E4C4A48u;
-constexpr uint32_t kLut8to11 = 0x53525150u, kLut12to15 = 0x57565554u;
+// The tensor cores read each weight as one E4M3 byte whose bits are the offset-binary nibble u = w + 8 (0..15): the
+// bytes 0..7 are the E4M3 subnormals u * 2^-9 and 8..15 the first normal binade, also u * 2^-9, so the byte stands
+// for u exactly and the MMA yields 2^-9 * sum_k A_i[k] (w[k] + 8). The combine multiplies by 2^9 (folded into its
+// coefficients) and subtracts 8 S_i. Turning packed nibbles into these bytes needs no table: the prepacked layout
+// puts k .. k+3 in the low nibbles and k+4 .. k+7 in the high nibbles of each 32-bit word.
+constexpr float kMmaUnit = 512.0f;     // 2^9: one MMA unit of the weight operand
 
-// Four offset-binary nibbles (sel bits 15..0, nibble j -> output byte j) to four E4M3 bytes. Nibbles 0..7 select
-// from the low table; 8..15 have their msb set, which makes prmt emit the (zero) sign of a positive table byte, so
-// the low lookup yields 0 for them. The second lookup runs on the nibbles with msb flipped and covers 8..15.
-__device__ __forceinline__ uint32_t u4x4_to_e4m3(uint32_t sel, uint32_t sel_flipped) {
-    return prmt(kLut0to3, kLut4to7, sel) | prmt(kLut8to11, kLut12to15, sel_flipped);
+__device__ __forceinline__ uint4 expand_nibbles16(uint2 v) {
+    return make_uint4(v.x & 0x0F0F0F0Fu, (v.x >> 4) & 0x0F0F0F0Fu, v.y & 0x0F0F0F0Fu, (v.y >> 4) & 0x0F0F0F0Fu);
 }
 
-// int4 -> E4M3 for the chunks q = t, t + 128, ... (4 of them) of one half of a packed 128 x 128 weight tile: chunk q
-// is 16 k of weight row q / 8, written to its place in the 128-byte-swizzled K-major A tile.
+// Weight bytes for the chunks q = t, t + 128, ... (4 of them) of one half of a packed 128 x 128 weight tile: chunk
+// q is 16 k of weight row q / 8, written to its place in the 128-byte-swizzled K-major operand tile.
 __device__ __forceinline__ void convert_half_tile(const uint8_t *src, uint8_t *dst, int t, int half) {
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
         const int q = t + (half * 4 + it) * 128;
         const int row = q >> 3, ch = q & 7;
-        const uint2 v = *reinterpret_cast<const uint2 *>(src + q * 8);
-        const uint32_t vx = v.x ^ 0x88888888u, vy = v.y ^ 0x88888888u;
-        uint4 o;
-        o.x = u4x4_to_e4m3(v.x, vx);
-        o.y = u4x4_to_e4m3(v.x >> 16, vx >> 16);
-        o.z = u4x4_to_e4m3(v.y, vy);
-        o.w = u4x4_to_e4m3(v.y >> 16, vy >> 16);
+        const uint4 o = expand_nibbles16(*reinterpret_cast<const uint2 *>(src + q * 8));
+        *reinterpret_cast<uint4 *>(dst + (row >> 3) * 1024 + (row & 7) * 128 + ((ch ^ (row & 7)) << 4)) = o;
+    }
+}
+
+// The same for a whole tile by `nthreads` threads (nthreads divides 1024): chunks q = t, t + nthreads, ...
+__device__ __forceinline__ void convert_tile(const uint8_t *src, uint8_t *dst, int t, int nthreads) {
+#pragma unroll 4
+    for (int q = t; q < 1024; q += nthreads) {
+        const int row = q >> 3, ch = q & 7;
+        const uint4 o = expand_nibbles16(*reinterpret_cast<const uint2 *>(src + q * 8));
         *reinterpret_cast<uint4 *>(dst + (row >> 3) * 1024 + (row & 7) * 128 + ((ch ^ (row & 7)) << 4)) = o;
     }
 }
@@ -227,10 +231,13 @@ __global__ void prepack_kernel(const uint8_t *__restrict__ in, uint8_t *__restri
         tile[kk][c] = static_cast<uint8_t>(v ^ 0x88u);               // w -> w + 8 in both nibbles
     }
     __syncthreads();
+    // row r of the tile: byte 4q + b holds k = 8q + b (low nibble) and k + 4 (high nibble)
     uint8_t *dst = out + (static_cast<size_t>(nt) * kb_total + kb) * kPackedTileBytes;
     for (int idx = threadIdx.x; idx < kPackedTileBytes; idx += blockDim.x) {
         const int r = idx / (kKBlock / 2), j = idx % (kKBlock / 2);
-        dst[idx] = tile[j][r];
+        const int k0 = 8 * (j >> 2) + (j & 3), k1 = k0 + 4;
+        const int lo = (tile[k0 >> 1][r] >> (4 * (k0 & 1))) & 0xF, hi = (tile[k1 >> 1][r] >> (4 * (k1 & 1))) & 0xF;
+        dst[idx] = static_cast<uint8_t>(lo | (hi << 4));
     }
 }
 
@@ -335,9 +342,9 @@ __device__ __forceinline__ void unfold_rows(const __half *xs, uint8_t *bt, float
             const float s3 = static_cast<float>(sum3[r]);
             float *cg = cst + (lane / lpg) * kConstFloatsPerGroup;
             const float c1 = kC1 * am[r], c2 = kC2 * am[r], c3 = kC3 * am[r];
-            cg[0 * 16 + m] = c1;
-            cg[1 * 16 + m] = c2;
-            cg[2 * 16 + m] = c3;
+            cg[0 * 16 + m] = kMmaUnit * c1;                  // exact: power-of-two scaling
+            cg[1 * 16 + m] = kMmaUnit * c2;
+            cg[2 * 16 + m] = kMmaUnit * c3;
             cg[3 * 16 + m] = 8.0f * (c1 * s1 + c2 * s2 + c3 * s3);
             cg[4 * 16 + m] = s1;
             cg[5 * 16 + m] = s2;
@@ -609,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                                     for (int pl = 0; pl < 3; ++pl) {
                                         const int col = pl * kMaxM + m;
                                         const float dv = __uint_as_float(d[col >> 4][col & 15]);
-                                        const float yi = dv - 8.0f * cg[(4 + pl) * 16 + m];
+                                        const float yi = kMmaUnit * dv - 8.0f * cg[(4 + pl) * 16 + m];
                                         p.dbg_y123[(static_cast<size_t>(pl) * M + m0 + m) * N + n] =
                                             __float2int_rn(yi);
                                     }

@@ -220,8 +220,10 @@ wqbmm_status launch_large(const Shape &s, const Plan &plan, const void *x, const
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         if (!info->gemm_smem_set) {
-            if (cudaFuncSetAttribute(msd_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemLimit) !=
-                cudaSuccess)
+            if (cudaFuncSetAttribute(msd_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kGemmSmemLimit) != cudaSuccess ||
+                cudaFuncSetAttribute(msd_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kGemmSmemLimit) != cudaSuccess)
                 return WQBMM_ERR_CUDA;
             info->gemm_smem_set = true;
         }
@@ -262,7 +264,9 @@ wqbmm_status launch_large(const Shape &s, const Plan &plan, const void *x, const
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, msd_gemm_kernel, gp, tmap_s) == cudaSuccess ? WQBMM_OK : WQBMM_ERR_CUDA;
+    const cudaError_t e = dbg_group >= 0 ? cudaLaunchKernelEx(&cfg, msd_gemm_kernel<true>, gp, tmap_s)
+                                         : cudaLaunchKernelEx(&cfg, msd_gemm_kernel<false>, gp, tmap_s);
+    return e == cudaSuccess ? WQBMM_OK : WQBMM_ERR_CUDA;
 }
 
 // Launches one product (or, with dbg_group >= 0, the integer partials of one group) planned by `plan` on the current
