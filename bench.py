@@ -338,8 +338,8 @@ def main():
             torch.distributed.destroy_process_group()
         return
 
-    # M >= 64 runs the unfold pre-pass and then the tile kernel; below that one fused kernel
-    launches_per_step = 2 if wl.M >= 64 else 1
+    # M <= 2 and M >= 64 run an unfold pre-pass and then the main kernel; in between one fused kernel
+    launches_per_step = 1 if 2 < wl.M < 64 else 2
     peaks, peak_kind = measured_peaks()
     alg_bytes = wl.algorithmic_bytes()
     if wl.M <= 16:

@@ -86,9 +86,11 @@ WQBMM_API wqbmm_status wqbmm_prepack_weight(const uint8_t *w_packed, void *w_pre
 
 /*
  * Workspace bytes wqbmm_run needs for this shape on any GB300 (0 when the shape needs none). Host only.
- * For M < 64 the workspace holds split-K partial sums and per-tile arrival counters (only shapes whose split over K
- * is wider than one thread-block cluster need any); for M >= 64 it holds the unfolded planes of x (3 bytes per
- * element of x, rows padded to a multiple of 128) and, per row and group, four floats of combine constants.
+ * For M <= 2 the workspace holds the unfolded planes of x as int8 (3 bytes per element, K padded to a multiple of
+ * 128) and, per row and group, four floats of combine constants; for 3 <= M < 64 it holds split-K partial sums and
+ * per-tile arrival counters (only shapes whose split over K is wider than one thread-block cluster need any); for
+ * M >= 64 it holds the unfolded planes of x (3 bytes per element of x, rows padded to a multiple of 128) and the
+ * constants.
  * It must be zero-filled once before its first use; every successful run leaves the counters at zero again, so the
  * same workspace can be reused by later runs on the same stream without clearing. Runs that execute concurrently must
  * use different workspaces.
@@ -130,7 +132,7 @@ WQBMM_API wqbmm_status wqbmm_debug_unfold(const void *x, int64_t M, int64_t K, i
  * Exposes step 9 for one group g as the run kernel's tensor-core path computes it (for bit-exact checks): the
  * kernel wqbmm_run would pick for this M, restricted to the k-block that holds group g.
  *   y123       device, int32 [3, M, N]: Y_i[m, n] of group g at y123[(i * M + m) * N + n]
- *   workspace  device, wqbmm_workspace_bytes(M, K, N, G) bytes when M >= 64 (ignored, may be null, below)
+ *   workspace  device, wqbmm_workspace_bytes(M, K, N, G) bytes when M <= 2 or M >= 64 (else ignored, may be null)
  * 0 <= g < K/G. Errors: NULLPTR, INVALID (also a workspace too small for M >= 64), UNSUPPORTED_ARCH, CUDA.
  */
 WQBMM_API wqbmm_status wqbmm_debug_group_partials(const void *x, const void *w_prepacked, int64_t M, int64_t K,

@@ -269,7 +269,7 @@ def test_run_deterministic_and_workspace_left_clean(dev, wl):
         outs.append(y.cpu().numpy().view(np.uint16))
     assert all(np.array_equal(outs[0], o) for o in outs[1:])
     assert_within_tolerance(outs[0].view(np.float16), oracle.msd_matmul(x, wp, sc, wl.G), wl.name)
-    if ws is not None and wl.M < 64:
+    if ws is not None and 2 < wl.M < 64:
         # the arrival counters sit after the partial sums; all must be back at zero
         counters = ws.cpu().numpy()[-256:].view(np.uint32)
         assert not counters.any()

@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "msd_gemm.cuh"
+#include "msd_gemv.cuh"
 #include "msd_kernels.cuh"
 #include "wqbmm.h"
 
@@ -55,11 +56,12 @@ wqbmm_status check_shape(const Shape &s) {
 }
 
 constexpr int64_t kLargeM = 64;     // from this many rows on, x is unfolded once by a pre-pass (large-M path)
+constexpr int64_t kGemvMaxM = kGemvMaxRows;   // up to this many rows: the dp4a matrix-vector path
 
 // Small-M path: rows of x per CTA, the MMA N (three stacked planes padded to 16, 32 or 48 rows), the split over K.
 // Large-M path: 128-row x 128-column tiles, no split.
 struct Plan {
-    bool large;
+    bool large, gemv;
     int m_sub, m_tiles, n_tiles, kb_total, splits, nmma, reduce;
 };
 
@@ -69,6 +71,14 @@ Plan make_plan(const Shape &s, int sms) {
     Plan p{};
     p.n_tiles = static_cast<int>(ceil_div(s.N, kTileN));
     p.kb_total = static_cast<int>(ceil_div(s.K, kKBlock));
+    if (s.M <= kGemvMaxM) {
+        p.gemv = true;
+        p.m_tiles = 1;
+        p.m_sub = static_cast<int>(s.M);
+        p.splits = 1;
+        p.reduce = kReduceNone;
+        return p;
+    }
     if (s.M >= kLargeM) {
         p.large = true;
         p.m_tiles = static_cast<int>(ceil_div(s.M, kGemmTileM));
@@ -100,7 +110,13 @@ size_t consts_bytes(const Shape &s, const Plan &p) {
     return static_cast<size_t>(p.m_tiles) * (s.K / s.G) * kGemmTileM * kGemmConstRowBytes;
 }
 
+// Decode workspace: int8 planes [M][kb][384 B], then the constants [M][K/G] (float4).
+size_t gemv_planes_bytes(const Shape &s, const Plan &p) {
+    return static_cast<size_t>(s.M) * p.kb_total * kGemvPlaneBytes;
+}
+
 size_t workspace_for(const Shape &s, const Plan &p) {
+    if (p.gemv) return align256(gemv_planes_bytes(s, p)) + align256(static_cast<size_t>(s.M) * (s.K / s.G) * 16);
     if (p.large) return align256(planes_bytes(p)) + align256(consts_bytes(s, p));
     if (p.reduce != kReduceGlobal) return 0;
     return align256(static_cast<size_t>(p.splits) * s.M * s.N * sizeof(float)) +
@@ -269,11 +285,58 @@ wqbmm_status launch_large(const Shape &s, const Plan &plan, const void *x, const
     return e == cudaSuccess ? WQBMM_OK : WQBMM_ERR_CUDA;
 }
 
+// Decode path: the unfold of the one or two rows, then the dp4a matrix-vector kernel, both under programmatic launch
+// (the GEMV kernel streams its weights while the unfold runs).
+wqbmm_status launch_gemv(const Shape &s, const Plan &plan, const void *x, const void *w, const void *scale, void *y,
+                         void *workspace, int dbg_group, int32_t *dbg_y123, cudaStream_t stream) {
+    int8_t *planes = static_cast<int8_t *>(workspace);
+    float4 *consts = reinterpret_cast<float4 *>(static_cast<uint8_t *>(workspace) +
+                                                align256(gemv_planes_bytes(s, plan)));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(plan.kb_total, 4)), static_cast<unsigned>(s.M), 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, gemv_unfold_kernel, static_cast<const __half *>(x), static_cast<int>(s.M),
+                           static_cast<int>(s.K), static_cast<int>(s.G), plan.kb_total, planes, consts,
+                           dbg_group >= 0 ? 1 : 0) != cudaSuccess)
+        return WQBMM_ERR_CUDA;
+    GemvParams gp{};
+    gp.w = static_cast<const uint8_t *>(w);
+    gp.scale = static_cast<const __half *>(scale);
+    gp.planes = planes;
+    gp.consts = consts;
+    gp.y = static_cast<__half *>(y);
+    gp.dbg_y123 = dbg_y123;
+    gp.M = static_cast<int>(s.M);
+    gp.K = static_cast<int>(s.K);
+    gp.N = static_cast<int>(s.N);
+    gp.G = static_cast<int>(s.G);
+    gp.kb_total = plan.kb_total;
+    gp.dbg_group = dbg_group;
+    cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(s.N, kGemvCols)), 1, 1);
+    cfg.blockDim = dim3(kGemvThreads, 1, 1);
+    const bool dbg = dbg_group >= 0;
+    cudaError_t e;
+    if (s.M == 1)
+        e = dbg ? cudaLaunchKernelEx(&cfg, msd_gemv_kernel<1, true>, gp)
+                : cudaLaunchKernelEx(&cfg, msd_gemv_kernel<1, false>, gp);
+    else
+        e = dbg ? cudaLaunchKernelEx(&cfg, msd_gemv_kernel<2, true>, gp)
+                : cudaLaunchKernelEx(&cfg, msd_gemv_kernel<2, false>, gp);
+    return e == cudaSuccess ? WQBMM_OK : WQBMM_ERR_CUDA;
+}
+
 // Launches one product (or, with dbg_group >= 0, the integer partials of one group) planned by `plan` on the current
 // device. `workspace` holds workspace_for(shape, plan) bytes; `clear_counters` clears the split-K counters first.
 wqbmm_status dispatch(const void *x, const void *w, const void *scale, void *y, const Shape &s, const Plan &plan,
                       void *workspace, bool clear_counters, int dbg_group, int32_t *dbg_y123, DeviceInfo *info,
                       cudaStream_t stream) {
+    if (plan.gemv) return launch_gemv(s, plan, x, w, scale, y, workspace, dbg_group, dbg_y123, stream);
     if (plan.large) return launch_large(s, plan, x, w, scale, y, workspace, dbg_group, dbg_y123, info, stream);
     RunParams rp{};
     rp.x = static_cast<const __half *>(x);
@@ -446,7 +509,7 @@ wqbmm_status wqbmm_debug_group_partials(const void *x, const void *w_prepacked, 
     if (g < 0 || g >= K / G) return WQBMM_ERR_INVALID;
     if (!aligned16(x) || !aligned16(w_prepacked)) return WQBMM_ERR_INVALID;
     if (workspace && !aligned16(workspace)) return WQBMM_ERR_INVALID;
-    if (M >= kLargeM) {                                 // the large-M plan does not depend on the SM count
+    if (M >= kLargeM || M <= kGemvMaxM) {               // these plans do not depend on the SM count
         if (!workspace) return WQBMM_ERR_NULLPTR;
         if (workspace_bytes < workspace_for(s, make_plan(s, kPlanSms))) return WQBMM_ERR_INVALID;
     }
@@ -454,7 +517,7 @@ wqbmm_status wqbmm_debug_group_partials(const void *x, const void *w_prepacked, 
     DeviceInfo *info;
     if ((st = current_device(&dev, &info)) != WQBMM_OK) return st;
     Plan plan = make_plan(s, info->sms < kPlanSms ? info->sms : kPlanSms);
-    if (!plan.large) {                                  // the group's own k-block only, no split
+    if (!plan.large && !plan.gemv) {                    // the group's own k-block only, no split
         plan.splits = 1;
         plan.reduce = kReduceNone;
     }
