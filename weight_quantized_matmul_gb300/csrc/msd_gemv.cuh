@@ -25,6 +25,7 @@ constexpr int kGemvWarps = 8;
 constexpr int kGemvThreads = kGemvWarps * 32;
 constexpr int kGemvKbPerPass = 8;                   // k-blocks per warp held in registers at a time
 constexpr int kGemvPlaneBytes = 3 * kKBlock;        // one row, one k-block: [chunk 4][plane 3][32 bytes]
+constexpr float kDotUnitInv = 1.0f / 16.0f;          // the dot products come out as 16 sum_k A_i u
 
 // Steps 1-8 for one row and one 128-k block per warp (lane: 4 k). Planes to [row][kb][chunk][plane][32 B] as int8,
 // constants to [row][group] (float4).
@@ -47,11 +48,14 @@ __global__ void __launch_bounds__(128) gemv_unfold_kernel(const __half *__restri
     const int s1 = group_isum(__float2int_rn((a1[0] + a1[1]) + (a1[2] + a1[3])), lpg);
     const int s2 = group_isum(__float2int_rn((a2[0] + a2[1]) + (a2[2] + a2[3])), lpg);
     const int s3 = group_isum(__float2int_rn((a3[0] + a3[1]) + (a3[2] + a3[3])), lpg);
-    auto pack4 = [](const float (&a)[4]) {
-        return (static_cast<uint32_t>(static_cast<int>(a[0])) & 0xFFu) |
-               ((static_cast<uint32_t>(static_cast<int>(a[1])) & 0xFFu) << 8) |
-               ((static_cast<uint32_t>(static_cast<int>(a[2])) & 0xFFu) << 16) |
-               (static_cast<uint32_t>(static_cast<int>(a[3])) << 24);
+    // k = 8q .. 8q + 3 meet the low nibbles of a weight word, k = 8q + 4 .. 8q + 7 the high nibbles (16 u as a
+    // byte): the former planes are stored x16 (|16 A| <= 112 fits int8), so every product is 16 A u
+    const int mul = (lane & 1) ? 1 : 16;
+    auto pack4 = [mul](const float (&a)[4]) {
+        return (static_cast<uint32_t>(mul * static_cast<int>(a[0])) & 0xFFu) |
+               ((static_cast<uint32_t>(mul * static_cast<int>(a[1])) & 0xFFu) << 8) |
+               ((static_cast<uint32_t>(mul * static_cast<int>(a[2])) & 0xFFu) << 16) |
+               (static_cast<uint32_t>(mul * static_cast<int>(a[3])) << 24);
     };
     int8_t *dst = planes + (static_cast<size_t>(row) * kb_total + kb) * kGemvPlaneBytes + (lane >> 3) * 96 +
                   (lane & 7) * 4;
@@ -66,7 +70,7 @@ __global__ void __launch_bounds__(128) gemv_unfold_kernel(const __half *__restri
             rec = make_float4(static_cast<float>(s1), static_cast<float>(s2), static_cast<float>(s3), 0.0f);
         } else {
             const float c1 = kC1 * am, c2 = kC2 * am, c3 = kC3 * am;
-            rec = make_float4(c1, c2, c3,
+            rec = make_float4(c1 * kDotUnitInv, c2 * kDotUnitInv, c3 * kDotUnitInv,        // exact: 1/16
                               8.0f * (c1 * static_cast<float>(s1) + c2 * static_cast<float>(s2) +
                                       c3 * static_cast<float>(s3)));
         }
@@ -92,34 +96,65 @@ __device__ __forceinline__ uint4 ldg_stream16(const void *p, uint64_t policy) {
     return v;
 }
 
-// dp4a of the eight widened words of a 16-byte weight piece (32 k) against 32 plane bytes.
+__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// 16 sum_k A[k] u[k] over a 16-byte weight piece (32 k) and its 32 plane bytes: the low nibbles meet the x16 plane
+// bytes, the high nibbles (masked in place, worth 16 u) the plain ones.
 __device__ __forceinline__ int dot32(const uint4 w, const int4 pa, const int4 pb, int acc) {
-    acc = __dp4a(static_cast<int>(w.x & 0x0F0F0F0Fu), pa.x, acc);
-    acc = __dp4a(static_cast<int>((w.x >> 4) & 0x0F0F0F0Fu), pa.y, acc);
-    acc = __dp4a(static_cast<int>(w.y & 0x0F0F0F0Fu), pa.z, acc);
-    acc = __dp4a(static_cast<int>((w.y >> 4) & 0x0F0F0F0Fu), pa.w, acc);
-    acc = __dp4a(static_cast<int>(w.z & 0x0F0F0F0Fu), pb.x, acc);
-    acc = __dp4a(static_cast<int>((w.z >> 4) & 0x0F0F0F0Fu), pb.y, acc);
-    acc = __dp4a(static_cast<int>(w.w & 0x0F0F0F0Fu), pb.z, acc);
-    acc = __dp4a(static_cast<int>((w.w >> 4) & 0x0F0F0F0Fu), pb.w, acc);
+    acc = dp4a_us(w.x & 0x0F0F0F0Fu, pa.x, acc);
+    acc = dp4a_us(w.x & 0xF0F0F0F0u, pa.y, acc);
+    acc = dp4a_us(w.y & 0x0F0F0F0Fu, pa.z, acc);
+    acc = dp4a_us(w.y & 0xF0F0F0F0u, pa.w, acc);
+    acc = dp4a_us(w.z & 0x0F0F0F0Fu, pb.x, acc);
+    acc = dp4a_us(w.z & 0xF0F0F0F0u, pb.y, acc);
+    acc = dp4a_us(w.w & 0x0F0F0F0Fu, pb.z, acc);
+    acc = dp4a_us(w.w & 0xF0F0F0F0u, pb.w, acc);
     return acc;
 }
 
-// One CTA: columns [16 c, 16 c + 16) (rows r0 .. r0 + 15 of weight tile nt), all of K. Warp w: k-blocks
-// [w kb_total / 8, (w + 1) kb_total / 8). Lane l: weight rows r0 + l / 4 and r0 + 8 + l / 4, 32 k at (l % 4) * 32.
+// int -> float for |v| < 2^22 with one integer add and one float subtract (1.5 * 2^23 as the bias)
+__device__ __forceinline__ float small_int_to_float(int v) {
+    return __int_as_float(v + 0x4B400000) - 12582912.0f;
+}
+
+// One CTA: columns [16 c, 16 c + 16) (rows r0 .. r0 + 15 of weight tile nt), all of K, in passes of at most 64
+// k-blocks. In a pass, warp w takes an eighth of the pass's k-blocks; lane l reads weight rows r0 + l / 4 and
+// r0 + 8 + l / 4, 32 k at (l % 4) * 32. The pass's planes and constants are copied into shared memory in one bulk
+// copy each (the planes of a k-block are read by every warp of every CTA).
+constexpr int kGemvPassKb = kGemvWarps * kGemvKbPerPass;      // 64
+
+template <int MR>
+struct GemvSmem {
+    int8_t planes[MR][kGemvPassKb * kGemvPlaneBytes];
+    float4 consts[MR][kGemvPassKb * 4];
+    float red[kGemvWarps][MR][kGemvCols];
+    uint64_t bar;
+    int abort_flag;
+};
+
 template <int MR, bool kDebug>
 __global__ void __launch_bounds__(kGemvThreads) msd_gemv_kernel(const GemvParams p) {
-    __shared__ float red[kGemvWarps][MR][kGemvCols];
+    extern __shared__ __align__(128) uint8_t gemv_smem_raw[];
+    GemvSmem<MR> &sm = *reinterpret_cast<GemvSmem<MR> *>(gemv_smem_raw);
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = p.N, K = p.K, G = p.G, kb_total = p.kb_total;
-    const int Gn = K / G;
+    const int Gn = K / G, gpk = kKBlock / G;
     const int col0 = blockIdx.x * kGemvCols;
     const int nt = col0 / kTileN, r0 = col0 % kTileN;
     const int chunk = lane & 3;
     const int lpg_chunks = G / 32;                     // lanes (chunks of 32 k) per group: 1, 2 or 4
-    const int kbw0 = static_cast<int>(static_cast<int64_t>(warp) * kb_total / kGemvWarps);
-    const int kbw1 = static_cast<int>(static_cast<int64_t>(warp + 1) * kb_total / kGemvWarps);
+    const uint32_t bar = smem_addr(&sm.bar);
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        sm.abort_flag = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
     const uint64_t policy = l2_policy_evict_first();
     const uint8_t *wbase = p.w + static_cast<size_t>(nt) * kb_total * kPackedTileBytes + (r0 + (lane >> 2)) * 64 +
                            chunk * 16;
@@ -127,116 +162,136 @@ __global__ void __launch_bounds__(kGemvThreads) msd_gemv_kernel(const GemvParams
     float yacc[MR][2];
 #pragma unroll
     for (int m = 0; m < MR; ++m) yacc[m][0] = yacc[m][1] = 0.0f;
-    bool waited = false;
+    bool ok = true;
 
-    for (int kp = kbw0; kp < kbw1; kp += kGemvKbPerPass) {
-        const int nkb = min(kGemvKbPerPass, kbw1 - kp);
-        // weights of the pass: rows a and b of each k-block, 16 bytes each, all requested before any use
+    int pass = 0;
+    for (int pb = 0; pb < kb_total; pb += kGemvPassKb, ++pass) {
+        const int pn = min(kGemvPassKb, kb_total - pb);
+        const int kw0 = pb + warp * pn / kGemvWarps, kw1 = pb + (warp + 1) * pn / kGemvWarps;
+        const int nkb = kw1 - kw0;
+        // weights and scales of the warp's k-blocks, all requested before any use
         uint4 wa[kGemvKbPerPass], wb[kGemvKbPerPass];
         float sa[kGemvKbPerPass], sb[kGemvKbPerPass];
 #pragma unroll
         for (int j = 0; j < kGemvKbPerPass; ++j) {
             if (j < nkb) {
-                const uint8_t *src = wbase + static_cast<size_t>(kp + j) * kPackedTileBytes;
+                const uint8_t *src = wbase + static_cast<size_t>(kw0 + j) * kPackedTileBytes;
                 wa[j] = ldg_stream16(src, policy);
                 wb[j] = ldg_stream16(src + 8 * 64, policy);
-                const int g = ((kp + j) * kKBlock + chunk * 32) / G;
+                const int g = ((kw0 + j) * kKBlock + chunk * 32) / G;
                 if (!kDebug) {
                     sa[j] = g < Gn && n_a < N ? __half2float(__ldg(p.scale + static_cast<size_t>(g) * N + n_a)) : 0.0f;
                     sb[j] = g < Gn && n_b < N ? __half2float(__ldg(p.scale + static_cast<size_t>(g) * N + n_b)) : 0.0f;
                 }
             }
         }
-        if (!waited) {
-            pdl_wait();                                // the planes come from the unfold kernel
-            waited = true;
-        }
-#pragma unroll
-        for (int j = 0; j < kGemvKbPerPass; ++j) {
-            if (j >= nkb) break;
-            const int kb = kp + j;
-            const int k0 = kb * kKBlock + chunk * 32;
-            const int g = k0 / G;
-            const bool live = k0 < K;                   // a ragged last k-block: chunks past K hold zeros
+        if (threadIdx.x == 0) {
+            if (pass == 0) pdl_wait();                 // the planes come from the unfold kernel
+            const int groups = min((pb + pn) * gpk, Gn) - pb * gpk;
+            const uint32_t bytes = static_cast<uint32_t>(MR * pn * kGemvPlaneBytes + MR * groups * 16);
+            mbar_arrive_expect_tx(bar, bytes);
+            const uint64_t keep = l2_policy_evict_last();   // every CTA reads the same planes
 #pragma unroll
             for (int m = 0; m < MR; ++m) {
-                const int8_t *pl = p.planes + (static_cast<size_t>(m) * kb_total + kb) * kGemvPlaneBytes + chunk * 96;
-                int da[3], db[3];
-#pragma unroll
-                for (int q = 0; q < 3; ++q) {
-                    const int4 pa = __ldg(reinterpret_cast<const int4 *>(pl + q * 32));
-                    const int4 pb = __ldg(reinterpret_cast<const int4 *>(pl + q * 32 + 16));
-                    da[q] = dot32(wa[j], pa, pb, 0);
-                    db[q] = dot32(wb[j], pa, pb, 0);
-                }
-                // lanes of one group (same weight row, consecutive chunks) add their dots
-#pragma unroll
-                for (int q = 0; q < 3; ++q) {
-                    if (lpg_chunks >= 2) {
-                        da[q] += __shfl_xor_sync(0xffffffffu, da[q], 1);
-                        db[q] += __shfl_xor_sync(0xffffffffu, db[q], 1);
-                    }
-                    if (lpg_chunks >= 4) {
-                        da[q] += __shfl_xor_sync(0xffffffffu, da[q], 2);
-                        db[q] += __shfl_xor_sync(0xffffffffu, db[q], 2);
-                    }
-                }
-                if (!live) continue;
-                const float4 cr = __ldg(p.consts + static_cast<size_t>(m) * Gn + g);
-                if (kDebug) {
-                    // the constant record holds the plane sums: Y_i = dot_i - 8 S_i
-                    if (g == p.dbg_group && (chunk & (lpg_chunks - 1)) == 0 && m < p.M) {
-                        const float sv[3] = {cr.x, cr.y, cr.z};
-#pragma unroll
-                        for (int q = 0; q < 3; ++q) {
-                            const int sq = __float2int_rn(sv[q]);
-                            if (n_a < N) p.dbg_y123[(static_cast<size_t>(q) * p.M + m) * N + n_a] = da[q] - 8 * sq;
-                            if (n_b < N) p.dbg_y123[(static_cast<size_t>(q) * p.M + m) * N + n_b] = db[q] - 8 * sq;
-                        }
-                    }
-                    continue;
-                }
-                float ta = fmaf(cr.x, static_cast<float>(da[0]), -cr.w);
-                ta = fmaf(cr.y, static_cast<float>(da[1]), ta);
-                ta = fmaf(cr.z, static_cast<float>(da[2]), ta);
-                float tb = fmaf(cr.x, static_cast<float>(db[0]), -cr.w);
-                tb = fmaf(cr.y, static_cast<float>(db[1]), tb);
-                tb = fmaf(cr.z, static_cast<float>(db[2]), tb);
-                yacc[m][0] = fmaf(sa[j], ta, yacc[m][0]);
-                yacc[m][1] = fmaf(sb[j], tb, yacc[m][1]);
+                bulk_g2s(smem_addr(sm.planes[m]), p.planes + (static_cast<size_t>(m) * kb_total + pb) * kGemvPlaneBytes,
+                         static_cast<uint32_t>(pn * kGemvPlaneBytes), bar, keep);
+                bulk_g2s(smem_addr(sm.consts[m]), p.consts + static_cast<size_t>(m) * Gn + pb * gpk,
+                         static_cast<uint32_t>(groups * 16), bar, keep);
             }
         }
-    }
-    if (!waited) pdl_wait();
-    if constexpr (!kDebug) {
-    // one value per group: the lanes of a group hold equal sums, so add one lane per group (fixed order)
+        if (pass == 0 && threadIdx.x != 0) pdl_wait();
+        ok = ok && mbar_wait_warp(bar, pass & 1, &sm.abort_flag, kSiteConvFull);
+        if (ok) {
 #pragma unroll
-    for (int m = 0; m < MR; ++m) {
+            for (int j = 0; j < kGemvKbPerPass; ++j) {
+                if (j >= nkb) break;
+                const int kb = kw0 + j, kbl = kb - pb;
+                const int k0 = kb * kKBlock + chunk * 32;
+                const int g = k0 / G;
+                const bool live = k0 < K;               // a ragged last k-block: chunks past K hold zeros
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            float v = yacc[m][h];
-            if (lpg_chunks == 1) v += __shfl_xor_sync(0xffffffffu, v, 1);
-            if (lpg_chunks <= 2) v += __shfl_xor_sync(0xffffffffu, v, 2);
-            yacc[m][h] = v;
+                for (int m = 0; m < MR; ++m) {
+                    const int4 *pl = reinterpret_cast<const int4 *>(sm.planes[m] + kbl * kGemvPlaneBytes + chunk * 96);
+                    int da[3], db[3];
+#pragma unroll
+                    for (int q = 0; q < 3; ++q) {
+                        const int4 pa = pl[2 * q], pbv = pl[2 * q + 1];
+                        da[q] = dot32(wa[j], pa, pbv, 0);
+                        db[q] = dot32(wb[j], pa, pbv, 0);
+                    }
+                    if (kDebug) {
+                        // lanes of one group (same weight row, consecutive chunks) add their dots
+#pragma unroll
+                        for (int q = 0; q < 3; ++q) {
+                            for (int off = 1; off < lpg_chunks; off <<= 1) {
+                                da[q] += __shfl_xor_sync(0xffffffffu, da[q], off);
+                                db[q] += __shfl_xor_sync(0xffffffffu, db[q], off);
+                            }
+                        }
+                    }
+                    if (!live) continue;
+                    const float4 cr = sm.consts[m][g - pb * gpk];
+                    if (kDebug) {
+                        // the constant record holds the plane sums: Y_i = dot_i / 16 - 8 S_i
+                        if (g == p.dbg_group && (chunk & (lpg_chunks - 1)) == 0 && m < p.M) {
+                            const float sv[3] = {cr.x, cr.y, cr.z};
+#pragma unroll
+                            for (int q = 0; q < 3; ++q) {
+                                const int sq = __float2int_rn(sv[q]);
+                                if (n_a < N) p.dbg_y123[(static_cast<size_t>(q) * p.M + m) * N + n_a] = da[q] / 16 - 8 * sq;
+                                if (n_b < N) p.dbg_y123[(static_cast<size_t>(q) * p.M + m) * N + n_b] = db[q] / 16 - 8 * sq;
+                            }
+                        }
+                        continue;
+                    }
+                    // this lane's share of the group: c_i times its own dots; the group's first chunk also takes
+                    // the offset correction (the combine is linear, the lanes are added at the end)
+                    const float corr = (chunk & (lpg_chunks - 1)) == 0 ? -cr.w : 0.0f;
+                    float ta = fmaf(cr.x, small_int_to_float(da[0]), corr);
+                    ta = fmaf(cr.y, small_int_to_float(da[1]), ta);
+                    ta = fmaf(cr.z, small_int_to_float(da[2]), ta);
+                    float tb = fmaf(cr.x, small_int_to_float(db[0]), corr);
+                    tb = fmaf(cr.y, small_int_to_float(db[1]), tb);
+                    tb = fmaf(cr.z, small_int_to_float(db[2]), tb);
+                    yacc[m][0] = fmaf(sa[j], ta, yacc[m][0]);
+                    yacc[m][1] = fmaf(sb[j], tb, yacc[m][1]);
+                }
+            }
         }
+        __syncthreads();                               // the next pass overwrites the planes
     }
-    if (chunk == 0) {
+    if (kb_total == 0) pdl_wait();
+    if constexpr (!kDebug) {
+        // the four chunk lanes of a weight row hold partial sums: add them (fixed order)
 #pragma unroll
         for (int m = 0; m < MR; ++m) {
-            red[warp][m][lane >> 2] = yacc[m][0];
-            red[warp][m][8 + (lane >> 2)] = yacc[m][1];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float v = yacc[m][h];
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                yacc[m][h] = v;
+            }
+        }
+        if (chunk == 0) {
+#pragma unroll
+            for (int m = 0; m < MR; ++m) {
+                sm.red[warp][m][lane >> 2] = yacc[m][0];
+                sm.red[warp][m][8 + (lane >> 2)] = yacc[m][1];
+            }
+        }
+        __syncthreads();
+        if (ok && threadIdx.x < MR * kGemvCols) {
+            const int m = threadIdx.x / kGemvCols, c = threadIdx.x % kGemvCols;
+            float acc = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kGemvWarps; ++w) acc += sm.red[w][m][c];
+            const int n = col0 + c;
+            if (m < p.M && n < N) p.y[static_cast<size_t>(m) * N + n] = __float2half_rn(acc);
         }
     }
-    __syncthreads();
-    if (threadIdx.x < MR * kGemvCols) {
-        const int m = threadIdx.x / kGemvCols, c = threadIdx.x % kGemvCols;
-        float acc = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kGemvWarps; ++w) acc += red[w][m][c];
-        const int n = col0 + c;
-        if (m < p.M && n < N) p.y[static_cast<size_t>(m) * N + n] = __float2half_rn(acc);
-    }
-    }
+    // no bulk copy may still be writing shared memory when the CTA exits
+    if (threadIdx.x == 0 && !ok) mbar_wait_drain(bar, (pass - 1) & 1);
 }
 
 }  // namespace wqbmm

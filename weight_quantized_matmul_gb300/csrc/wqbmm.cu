@@ -26,6 +26,7 @@ struct DeviceInfo {
     int sms = 0;
     bool smem_set[3] = {false, false, false};
     bool gemm_smem_set = false;
+    bool gemv_smem_set = false;
 };
 
 std::mutex g_mutex;
@@ -288,7 +289,23 @@ wqbmm_status launch_large(const Shape &s, const Plan &plan, const void *x, const
 // Decode path: the unfold of the one or two rows, then the dp4a matrix-vector kernel, both under programmatic launch
 // (the GEMV kernel streams its weights while the unfold runs).
 wqbmm_status launch_gemv(const Shape &s, const Plan &plan, const void *x, const void *w, const void *scale, void *y,
-                         void *workspace, int dbg_group, int32_t *dbg_y123, cudaStream_t stream) {
+                         void *workspace, int dbg_group, int32_t *dbg_y123, DeviceInfo *info, cudaStream_t stream) {
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (!info->gemv_smem_set) {
+            const int s1 = static_cast<int>(sizeof(GemvSmem<1>)), s2 = static_cast<int>(sizeof(GemvSmem<2>));
+            if (cudaFuncSetAttribute(msd_gemv_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, s1) !=
+                    cudaSuccess ||
+                cudaFuncSetAttribute(msd_gemv_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s1) !=
+                    cudaSuccess ||
+                cudaFuncSetAttribute(msd_gemv_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, s2) !=
+                    cudaSuccess ||
+                cudaFuncSetAttribute(msd_gemv_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s2) !=
+                    cudaSuccess)
+                return WQBMM_ERR_CUDA;
+            info->gemv_smem_set = true;
+        }
+    }
     int8_t *planes = static_cast<int8_t *>(workspace);
     float4 *consts = reinterpret_cast<float4 *>(static_cast<uint8_t *>(workspace) +
                                                 align256(gemv_planes_bytes(s, plan)));
@@ -321,13 +338,15 @@ wqbmm_status launch_gemv(const Shape &s, const Plan &plan, const void *x, const 
     cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(s.N, kGemvCols)), 1, 1);
     cfg.blockDim = dim3(kGemvThreads, 1, 1);
     const bool dbg = dbg_group >= 0;
+    auto go = [&](auto kernel, size_t smem) {
+        cfg.dynamicSmemBytes = smem;
+        return cudaLaunchKernelEx(&cfg, kernel, gp);
+    };
     cudaError_t e;
     if (s.M == 1)
-        e = dbg ? cudaLaunchKernelEx(&cfg, msd_gemv_kernel<1, true>, gp)
-                : cudaLaunchKernelEx(&cfg, msd_gemv_kernel<1, false>, gp);
+        e = dbg ? go(msd_gemv_kernel<1, true>, sizeof(GemvSmem<1>)) : go(msd_gemv_kernel<1, false>, sizeof(GemvSmem<1>));
     else
-        e = dbg ? cudaLaunchKernelEx(&cfg, msd_gemv_kernel<2, true>, gp)
-                : cudaLaunchKernelEx(&cfg, msd_gemv_kernel<2, false>, gp);
+        e = dbg ? go(msd_gemv_kernel<2, true>, sizeof(GemvSmem<2>)) : go(msd_gemv_kernel<2, false>, sizeof(GemvSmem<2>));
     return e == cudaSuccess ? WQBMM_OK : WQBMM_ERR_CUDA;
 }
 
@@ -336,7 +355,7 @@ wqbmm_status launch_gemv(const Shape &s, const Plan &plan, const void *x, const 
 wqbmm_status dispatch(const void *x, const void *w, const void *scale, void *y, const Shape &s, const Plan &plan,
                       void *workspace, bool clear_counters, int dbg_group, int32_t *dbg_y123, DeviceInfo *info,
                       cudaStream_t stream) {
-    if (plan.gemv) return launch_gemv(s, plan, x, w, scale, y, workspace, dbg_group, dbg_y123, stream);
+    if (plan.gemv) return launch_gemv(s, plan, x, w, scale, y, workspace, dbg_group, dbg_y123, info, stream);
     if (plan.large) return launch_large(s, plan, x, w, scale, y, workspace, dbg_group, dbg_y123, info, stream);
     RunParams rp{};
     rp.x = static_cast<const __half *>(x);
