@@ -164,6 +164,8 @@ def test_unfold_bit_exact_every_fp16_value(dev):
 PARTIAL_CASES = [
     # M, K, N, G, groups to check, x dist, w dist
     (1, 256, 128, 128, [0, 1], "normal", "u8"),
+    (2, 512, 264, 32, [3, 15], "t3_clip60", "u8"),
+    (2, 8320, 136, 64, [0, 129], "normal", "pm1_mix"),     # K > 8192: unfold kernel + streaming kernel
     (3, 512, 264, 64, [0, 5, 7], "t3_clip60", "u8"),
     (5, 96, 1000, 32, [0, 2], "normal", "u8"),
     (8, 1024, 384, 128, [3], "normal_cols20", "pm1_mix"),
@@ -228,7 +230,10 @@ RUN_CASES = [
     (200, 96, 1000, 32, "uniform3", "u7", -3.0, 3.0),
     (256, 320, 392, 64, "t3_clip60", "u8", -1.0, 1.0),
     (300, 1280, 520, 128, "normal_cols20", "pm1_mix", 0.002, 0.03),
-    (1, 65536, 256, 128, "normal", "u8", 0.005, 0.02),     # 160-way split-K through the workspace
+    (1, 65536, 256, 128, "normal", "u8", 0.005, 0.02),     # M <= 2, K > 8192: unfold kernel + streaming kernel
+    (2, 8320, 264, 64, "t3_clip60", "u8", -1.0, 1.0),
+    (2, 1024, 1000, 32, "uniform3", "u7", -3.0, 3.0),      # M <= 2, K <= 8192: one persistent kernel
+    (3, 65536, 256, 128, "normal", "u8", 0.005, 0.02),     # 160-way split-K through the workspace
     (4, 4096, 1024, 128, "t3_clip60", "u8", -0.5, 0.5),    # 8 column tiles x 8 cluster slices
 ]
 

@@ -137,7 +137,7 @@ struct GemvSmem {
 };
 
 template <int MR, bool kDebug>
-__global__ void __launch_bounds__(kGemvThreads) msd_gemv_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvParams p) {
     extern __shared__ __align__(128) uint8_t gemv_smem_raw[];
     GemvSmem<MR> &sm = *reinterpret_cast<GemvSmem<MR> *>(gemv_smem_raw);
     pdl_launch_dependents();
@@ -169,20 +169,16 @@ __global__ void __launch_bounds__(kGemvThreads) msd_gemv_kernel(const GemvParams
         const int pn = min(kGemvPassKb, kb_total - pb);
         const int kw0 = pb + warp * pn / kGemvWarps, kw1 = pb + (warp + 1) * pn / kGemvWarps;
         const int nkb = kw1 - kw0;
-        // weights and scales of the warp's k-blocks, all requested before any use
+        // weights and scales of the warp's k-blocks, all requested before any use (the scales stay fp16 until
+        // they are used, so no instruction waits for them here)
         uint4 wa[kGemvKbPerPass], wb[kGemvKbPerPass];
-        float sa[kGemvKbPerPass], sb[kGemvKbPerPass];
+        __half sa[kGemvKbPerPass], sb[kGemvKbPerPass];
 #pragma unroll
         for (int j = 0; j < kGemvKbPerPass; ++j) {
             if (j < nkb) {
                 const uint8_t *src = wbase + static_cast<size_t>(kw0 + j) * kPackedTileBytes;
                 wa[j] = ldg_stream16(src, policy);
                 wb[j] = ldg_stream16(src + 8 * 64, policy);
-                const int g = ((kw0 + j) * kKBlock + chunk * 32) / G;
-                if (!kDebug) {
-                    sa[j] = g < Gn && n_a < N ? __half2float(__ldg(p.scale + static_cast<size_t>(g) * N + n_a)) : 0.0f;
-                    sb[j] = g < Gn && n_b < N ? __half2float(__ldg(p.scale + static_cast<size_t>(g) * N + n_b)) : 0.0f;
-                }
             }
         }
         if (threadIdx.x == 0) {
@@ -197,6 +193,15 @@ __global__ void __launch_bounds__(kGemvThreads) msd_gemv_kernel(const GemvParams
                          static_cast<uint32_t>(pn * kGemvPlaneBytes), bar, keep);
                 bulk_g2s(smem_addr(sm.consts[m]), p.consts + static_cast<size_t>(m) * Gn + pb * gpk,
                          static_cast<uint32_t>(groups * 16), bar, keep);
+            }
+        }
+        if (!kDebug) {
+#pragma unroll
+            for (int j = 0; j < kGemvKbPerPass; ++j) {
+                const int g = ((kw0 + j) * kKBlock + chunk * 32) / G;
+                const bool in = j < nkb && g < Gn;
+                sa[j] = in && n_a < N ? __ldg(p.scale + static_cast<size_t>(g) * N + n_a) : __half(0.0f);
+                sb[j] = in && n_b < N ? __ldg(p.scale + static_cast<size_t>(g) * N + n_b) : __half(0.0f);
             }
         }
         if (pass == 0 && threadIdx.x != 0) pdl_wait();
@@ -253,8 +258,8 @@ __global__ void __launch_bounds__(kGemvThreads) msd_gemv_kernel(const GemvParams
                     float tb = fmaf(cr.x, small_int_to_float(db[0]), corr);
                     tb = fmaf(cr.y, small_int_to_float(db[1]), tb);
                     tb = fmaf(cr.z, small_int_to_float(db[2]), tb);
-                    yacc[m][0] = fmaf(sa[j], ta, yacc[m][0]);
-                    yacc[m][1] = fmaf(sb[j], tb, yacc[m][1]);
+                    yacc[m][0] = fmaf(__half2float(sa[j]), ta, yacc[m][0]);
+                    yacc[m][1] = fmaf(__half2float(sb[j]), tb, yacc[m][1]);
                 }
             }
         }
