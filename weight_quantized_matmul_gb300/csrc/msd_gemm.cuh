@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (lane == 0) mbar_arrive(sready(s));
             }
             if (!mbar_wait_warp(bfree(cb), ((i / kGemmBStages) & 1) ^ 1, abort_flag, kSiteConvEmpty)) break;
-            convert_tile(stage + 3 * kPlaneImageBytes, b_ring + cb * (kGemmTileN * kKBlock), ct, kConvThreads);
+            convert_tile<kConvThreads>(stage + 3 * kPlaneImageBytes, b_ring + cb * (kGemmTileN * kKBlock), ct);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {

@@ -206,13 +206,21 @@ __device__ __forceinline__ void convert_half_tile(const uint8_t *src, uint8_t *d
     }
 }
 
-// The same for a whole tile by `nthreads` threads (nthreads divides 1024): chunks q = t, t + nthreads, ...
-__device__ __forceinline__ void convert_tile(const uint8_t *src, uint8_t *dst, int t, int nthreads) {
-#pragma unroll 4
-    for (int q = t; q < 1024; q += nthreads) {
+// The same for a whole tile by NT threads (NT divides 1024): chunks q = t, t + NT, ... All of a thread's packed
+// chunks are read before any operand byte is written, so the loads overlap (source and destination may not be
+// proven disjoint by the compiler otherwise).
+template <int NT>
+__device__ __forceinline__ void convert_tile(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int t) {
+    constexpr int kPer = 1024 / NT;
+    uint2 v[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) v[j] = *reinterpret_cast<const uint2 *>(src + (t + j * NT) * 8);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int q = t + j * NT;
         const int row = q >> 3, ch = q & 7;
-        const uint4 o = expand_nibbles16(*reinterpret_cast<const uint2 *>(src + q * 8));
-        *reinterpret_cast<uint4 *>(dst + (row >> 3) * 1024 + (row & 7) * 128 + ((ch ^ (row & 7)) << 4)) = o;
+        *reinterpret_cast<uint4 *>(dst + (row >> 3) * 1024 + (row & 7) * 128 + ((ch ^ (row & 7)) << 4)) =
+            expand_nibbles16(v[j]);
     }
 }
 
