@@ -1,7 +1,9 @@
 """Benchmark of the A16W4 per-group MSD matmul on GB300.
 
-One step = one wqbmm_run over one batch of the workload (all steps of the method: A_max, unfold, the three
-integer matmuls on the tensor core, the per-group combine, the accumulation and the fp16 store, one kernel).
+One step = one wqbmm_run over one batch of the workload: all steps of the method (A_max, unfold, the three integer
+matmuls, the per-group combine, the accumulation and the fp16 store). Depending on M that is one fused kernel
+(3 <= M < 64) or an unfold kernel followed by the main kernel (M <= 2: dp4a matrix-vector kernel; M >= 64:
+tensor-core tile kernel).
 
 Default workload: decode GEMV M=1, K=4096, N=4096, G=128 (x ~ N(0,1) fp16, int4 weights uniform on [-8, 7],
 antiquant_scale uniform on [0.005, 0.02], seed 1). Metric: effective weight GB/s (K*N/2 bytes per step / step time).
@@ -75,6 +77,46 @@ def measured_peaks():
             return json.load(f), "measured"
     except (OSError, ValueError):
         return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS}, "fallback"
+
+
+def slowest_rank_ms(ms_total, world, device=None):
+    """The timed region's length on the slowest rank (every rank calls this; NCCL reduces on the GPU, gloo on the
+    host)."""
+    if world <= 1:
+        return ms_total
+    import torch
+    import torch.distributed as dist
+    on = device if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([ms_total], dtype=torch.float64, device=on)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def kernel_sources_hash():
+    """Hash of the CUDA sources the library is built from (names and contents, in name order)."""
+    import hashlib
+    h = hashlib.sha256()
+    src = os.path.join(ROOT, "weight_quantized_matmul_gb300", "csrc")
+    for name in sorted(os.listdir(src)):
+        if name.endswith((".cu", ".cuh")):
+            h.update(name.encode())
+            with open(os.path.join(src, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def dram_traffic(workload):
+    """DRAM bytes per launch of the workload's dominant kernel from the committed ncu capture, or None when there
+    is none or the kernel sources changed since it was taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            table = json.load(f)
+    except (OSError, ValueError):
+        return None
+    rec = table.get("workloads", {}).get(workload)
+    if not rec or table.get("kernel_sources_sha256") != kernel_sources_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
 
 
 def dist_env():
@@ -304,11 +346,7 @@ def main():
         torch.distributed.barrier()
     time.sleep(0.25)
     sampler.stop()
-    ms_total = start_ev.elapsed_time(stop_ev)
-    if world > 1:
-        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = slowest_rank_ms(start_ev.elapsed_time(stop_ev), world, dev)
     ms_step = ms_total / args.steps
     status = wq.wqbmm_read_device_status(stream=stream)
     if status != 0:
@@ -346,14 +384,14 @@ def main():
         hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
         achieved = alg_bytes / (ms_step * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                    "frac": achieved / hbm_peak, "traffic": None, "peak_source": f"{peak_kind} hbm_gbs",
+                    "frac": achieved / hbm_peak, "traffic": dram_traffic(wl.name), "peak_source": f"{peak_kind} hbm_gbs",
                     "algorithmic_bytes_per_launch": alg_bytes}
     else:
         # E4M3 dense tensor peak = the measured bf16 peak x 2 (the nominal fp8 : bf16 ratio 4.5 : 2.25)
         bf16 = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
         achieved = wl.int8_equiv_ops() / (ms_step * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": 2 * bf16, "unit": "TFLOP/s",
-                    "frac": achieved / (2 * bf16), "traffic": None,
+                    "frac": achieved / (2 * bf16), "traffic": dram_traffic(wl.name),
                     "peak_source": f"{peak_kind} bf16_tflops x 2 (e4m3)",
                     "algorithmic_flops_per_launch": wl.int8_equiv_ops()}
     line = {

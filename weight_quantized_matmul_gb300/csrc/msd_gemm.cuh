@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.off_misc + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nt = blockIdx.x, mt = blockIdx.y;
+    const int mt = blockIdx.x, nt = blockIdx.y;       // row tiles vary fastest: CTAs in flight share weight tiles
     const int K = p.K, N = p.N, G = p.G, M = p.M;
     const int gpk = L.gpk;
     const int Gn = K / G;

@@ -233,7 +233,7 @@ wqbmm_status launch_small(const RunParams &rp, const Plan &plan, DeviceInfo *inf
 // under programmatic launch (it fetches weights and scales while the pre-pass finishes).
 wqbmm_status launch_large(const Shape &s, const Plan &plan, const void *x, const void *w, const void *scale, void *y,
                           void *workspace, int dbg_group, int32_t *dbg_y123, DeviceInfo *info, cudaStream_t stream) {
-    if (plan.m_tiles > 65535) return WQBMM_ERR_INVALID;
+    if (plan.n_tiles > 65535) return WQBMM_ERR_INVALID;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         if (!info->gemm_smem_set) {
@@ -272,7 +272,7 @@ wqbmm_status launch_large(const Shape &s, const Plan &plan, const void *x, const
     gp.dbg_group = dbg_group;
     const GemmLayout L(gp.G);
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(plan.n_tiles, plan.m_tiles, 1);
+    cfg.gridDim = dim3(plan.m_tiles, plan.n_tiles, 1);     // row tiles fastest: concurrent CTAs share weight tiles
     cfg.blockDim = dim3(kGemmThreads, 1, 1);
     cfg.dynamicSmemBytes = L.smem_bytes;
     cfg.stream = stream;
