@@ -46,6 +46,8 @@ def _bind(path: str):
     lib.oracle_group_partials.argtypes = [p, p, i64, i64, i64, i64, i64, ctypes.c_int, p, i64, p]
     lib.oracle_msd_rows.argtypes = [p, p, p, i64, i64, i64, i64, ctypes.c_int, p, i64, p]
     lib.oracle_direct_rows.argtypes = [p, p, p, i64, i64, i64, i64, p, i64, p]
+    lib.oracle_msd_rows_ex.argtypes = [p, p, p, p, p, i64, i64, i64, i64, ctypes.c_int, p, i64, p]
+    lib.oracle_direct_rows_ex.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, i64, p]
     for f in ("oracle_decode_int4", "oracle_unfold", "oracle_group_partials", "oracle_msd_rows",
               "oracle_direct_rows"):
         getattr(lib, f).restype = ctypes.c_int
@@ -142,6 +144,41 @@ class Oracle:
                                            _ptr(out)), "msd_matmul")
         return out
 
+    def msd_matmul_ex(self, x: np.ndarray, w_packed: np.ndarray, scale: np.ndarray, G: int, zero_point=None,
+                      bias=None, mode: int = MODE_D, rows=None):
+        """Steps 1-11 with optional zero points fp16 [K/G, N] (weights stand for (w - zp) * scale) and bias fp16 [N]:
+        float64 [len(rows), N]."""
+        xb = _as_half_bits(x)
+        sb = _as_half_bits(scale)
+        zb = None if zero_point is None else _as_half_bits(zero_point)
+        bb = None if bias is None else _as_half_bits(np.asarray(bias).reshape(-1))
+        M, K = xb.shape
+        N = sb.shape[1]
+        w_packed = np.ascontiguousarray(w_packed, dtype=np.uint8)
+        r = _rows(M, rows)
+        out = np.empty((len(r), N), dtype=np.float64)
+        _check(self._lib().oracle_msd_rows_ex(_ptr(xb), _ptr(w_packed), _ptr(sb),
+                                              None if zb is None else _ptr(zb), None if bb is None else _ptr(bb),
+                                              M, K, N, G, mode, _ptr(r), len(r), _ptr(out)), "msd_matmul_ex")
+        return out
+
+    def direct_matmul_ex(self, x: np.ndarray, w_packed: np.ndarray, scale: np.ndarray, G: int, zero_point=None,
+                         bias=None, rows=None):
+        """x . ((w - zp) * scale) + bias in binary64: float64 [len(rows), N]."""
+        xb = _as_half_bits(x)
+        sb = _as_half_bits(scale)
+        zb = None if zero_point is None else _as_half_bits(zero_point)
+        bb = None if bias is None else _as_half_bits(np.asarray(bias).reshape(-1))
+        M, K = xb.shape
+        N = sb.shape[1]
+        w_packed = np.ascontiguousarray(w_packed, dtype=np.uint8)
+        r = _rows(M, rows)
+        out = np.empty((len(r), N), dtype=np.float64)
+        _check(self._lib().oracle_direct_rows_ex(_ptr(xb), _ptr(w_packed), _ptr(sb),
+                                                 None if zb is None else _ptr(zb), None if bb is None else _ptr(bb),
+                                                 M, K, N, G, _ptr(r), len(r), _ptr(out)), "direct_matmul_ex")
+        return out
+
     def direct_matmul(self, x: np.ndarray, w_packed: np.ndarray, scale: np.ndarray, G: int, rows=None):
         """x . (w * scale) in binary64: float64 [len(rows), N]."""
         xb = _as_half_bits(x)
@@ -173,3 +210,5 @@ unfold = _default.unfold
 group_partials = _default.group_partials
 msd_matmul = _default.msd_matmul
 direct_matmul = _default.direct_matmul
+msd_matmul_ex = _default.msd_matmul_ex
+direct_matmul_ex = _default.direct_matmul_ex

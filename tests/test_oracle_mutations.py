@@ -7,6 +7,7 @@ import pytest
 
 import oracle
 import test_oracle_pins as P
+import test_oracle_zp_bias as Z
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "wqbmm_oracle.c")
 
@@ -32,6 +33,9 @@ MUTATIONS = [
     ("int4 read as unsigned", "(int8_t)(hi >= 8 ? hi - 16 : hi)", "(int8_t)(hi)"),
     ("weight rows of a group reversed", "const int8_t *row = wg + k * N;", "const int8_t *row = wg + (G - 1 - k) * N;"),
     ("fp16 exponent bias off by one", "v = ldexp(1024.0 + f, e - 25);", "v = ldexp(1024.0 + f, e - 24);"),
+    ("zero point added instead of subtracted", "double y1 = yi[n] - z * s1", "double y1 = yi[n] + z * s1"),
+    ("zero point times the wrong plane sum", "s2 += a[G + k];", "s2 += a[k];"),
+    ("bias dropped", "yr[n] = yr[n] + oracle_half_to_double(bias[n]);", "yr[n] = yr[n];"),
 ]
 
 PINS = [
@@ -46,6 +50,8 @@ PINS = [
     lambda o: P.test_identity_weights_return_x(o),
     lambda o: P.test_constant_groups_scale_column_sums(o),
     lambda o: P.test_group_and_column_permutation_invariance(o),
+    lambda o: Z.test_integer_zero_point_equals_shifted_weights(o, oracle.MODE_D, 1),
+    lambda o: Z.test_bias_adds_itself(o),
 ]
 
 
