@@ -85,6 +85,15 @@ WQBMM_API wqbmm_status wqbmm_prepack_weight(const uint8_t *w_packed, void *w_pre
                                             int64_t G, wqbmm_stream_t stream);
 
 /*
+ * The same for a weight stored transposed, [N, K] (the operator's transpose option for the weight, page 2 section
+ * 5.4): w_packed_nk is uint8 [N, K/2], byte (n, kk) = w[2kk, n] in the low nibble and w[2kk+1, n] in the high
+ * nibble (two's complement). The output is the same prepacked buffer wqbmm_prepack_weight makes from the [K/2, N]
+ * form of the same weight. Errors as for wqbmm_prepack_weight.
+ */
+WQBMM_API wqbmm_status wqbmm_prepack_weight_nk(const uint8_t *w_packed_nk, void *w_prepacked, int64_t K, int64_t N,
+                                               int64_t G, wqbmm_stream_t stream);
+
+/*
  * Workspace bytes wqbmm_run needs for this shape on any GB300 (0 when the shape needs none). Host only.
  * For M <= 2 the workspace holds the unfolded planes of x as int8 (3 bytes per element, K padded to a multiple of
  * 128) and, per row and group, four floats of combine constants; for 3 <= M < 64 it holds split-K partial sums and

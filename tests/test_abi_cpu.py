@@ -95,6 +95,9 @@ CASES = [
     ("prepack_null_dst", lambda L: L.wqbmm_prepack_weight(A, None, 128, 128, 128, None), NULLPTR),
     ("prepack_misaligned_dst", lambda L: L.wqbmm_prepack_weight(A, MIS, 128, 128, 128, None), INVALID),
     ("prepack_bad_group", lambda L: L.wqbmm_prepack_weight(A, A, 128, 128, 16, None), INVALID),
+    ("prepack_nk_null_src", lambda L: L.wqbmm_prepack_weight_nk(None, A, 128, 128, 128, None), NULLPTR),
+    ("prepack_nk_misaligned_dst", lambda L: L.wqbmm_prepack_weight_nk(A, MIS, 128, 128, 128, None), INVALID),
+    ("prepack_nk_bad_shape", lambda L: L.wqbmm_prepack_weight_nk(A, A, 96, 128, 64, None), INVALID),
     ("run_null_x", lambda L: L.wqbmm_run(None, A, A, A, 1, 128, 128, 128, A, 1 << 20, None), NULLPTR),
     ("run_null_w", lambda L: L.wqbmm_run(A, None, A, A, 1, 128, 128, 128, A, 1 << 20, None), NULLPTR),
     ("run_null_scale", lambda L: L.wqbmm_run(A, A, None, A, 1, 128, 128, 128, A, 1 << 20, None), NULLPTR),

@@ -86,6 +86,23 @@ def test_prepack_matches_documented_layout(dev, K, N, G):
     np.testing.assert_array_equal(got, prepack_layout(wp, K, N))
 
 
+def pack_int4_nk(w_packed_kn, K, N):
+    """The [N, K/2] packing of the same weights (two k per byte, low nibble first), from their [K/2, N] packing."""
+    w = oracle.decode_int4(w_packed_kn, K, N)                       # [K, N] int8
+    u = (w.T.astype(np.int16) & 0xF).astype(np.uint8)               # [N, K] nibbles
+    return np.ascontiguousarray(u[:, 0::2] | (u[:, 1::2] << 4))
+
+
+@pytest.mark.parametrize("K,N,G", [(128, 128, 128), (640, 264, 64), (96, 1000, 32), (4096, 4096, 128)])
+def test_prepack_of_transposed_weights_matches(dev, K, N, G):
+    wp = I.make_w_packed(I.small_case(1, K, N, G, seed=K + 3 * N))
+    nk = pack_int4_nk(wp, K, N)
+    assert nk.shape == (N, K // 2)
+    a = wq.prepack_weight(to_dev(wp, dev), K, N, G).cpu().numpy()
+    b = wq.prepack_weight_nk(to_dev(nk, dev), K, N, G).cpu().numpy()
+    np.testing.assert_array_equal(a, b)
+
+
 # ------------------------------------------------------------------------------------------- steps 1-8
 
 def special_x():

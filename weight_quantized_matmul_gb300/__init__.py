@@ -15,7 +15,8 @@ __all__ = [
     "WqbmmError", "library_path", "load_library", "wqbmm_prepacked_weight_bytes", "wqbmm_prepack_weight",
     "wqbmm_workspace_bytes", "wqbmm_run", "wqbmm_debug_unfold", "wqbmm_debug_group_partials",
     "wqbmm_read_device_status", "wqbmm_debug_wait_timeout", "wqbmm_status_string", "prepack_weight",
-    "allocate_workspace", "msd_matmul", "SYMBOLS", "wqbmm_run_static_scratch",
+    "allocate_workspace", "msd_matmul", "SYMBOLS", "wqbmm_run_static_scratch", "wqbmm_prepack_weight_nk",
+    "prepack_weight_nk",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -29,7 +30,7 @@ OK, ERR_NULLPTR, ERR_INVALID, ERR_UNSUPPORTED_ARCH, ERR_CUDA, ERR_DEVICE_TIMEOUT
 SYMBOLS = (
     "wqbmm_prepacked_weight_bytes", "wqbmm_prepack_weight", "wqbmm_workspace_bytes", "wqbmm_run",
     "wqbmm_debug_unfold", "wqbmm_debug_group_partials", "wqbmm_read_device_status", "wqbmm_debug_wait_timeout",
-    "wqbmm_status_string", "wqbmm_run_static_scratch",
+    "wqbmm_status_string", "wqbmm_run_static_scratch", "wqbmm_prepack_weight_nk",
 )
 
 
@@ -64,6 +65,7 @@ def load_library():
                 "wqbmm_read_device_status": [ctypes.POINTER(ctypes.c_int32), ctypes.c_int, p],
                 "wqbmm_debug_wait_timeout": [i64, p],
                 "wqbmm_run_static_scratch": [p, p, p, p, i64, i64, i64, i64, p],
+                "wqbmm_prepack_weight_nk": [p, p, i64, i64, i64, p],
             }
             for name, args in sig.items():
                 f = getattr(lib, name)
@@ -110,6 +112,11 @@ def wqbmm_prepacked_weight_bytes(K: int, N: int, G: int) -> int:
 def wqbmm_prepack_weight(w_packed, w_prepacked, K: int, N: int, G: int, stream=None) -> None:
     _check(load_library().wqbmm_prepack_weight(_ptr(w_packed), _ptr(w_prepacked), K, N, G, _stream(stream)),
            "wqbmm_prepack_weight")
+
+
+def wqbmm_prepack_weight_nk(w_packed_nk, w_prepacked, K: int, N: int, G: int, stream=None) -> None:
+    _check(load_library().wqbmm_prepack_weight_nk(_ptr(w_packed_nk), _ptr(w_prepacked), K, N, G, _stream(stream)),
+           "wqbmm_prepack_weight_nk")
 
 
 def wqbmm_workspace_bytes(M: int, K: int, N: int, G: int) -> int:
@@ -167,6 +174,14 @@ def prepack_weight(w_packed, K: int, N: int, G: int, stream=None):
     import torch
     out = torch.empty(wqbmm_prepacked_weight_bytes(K, N, G), dtype=torch.uint8, device=w_packed.device)
     wqbmm_prepack_weight(w_packed, out, K, N, G, stream)
+    return out
+
+
+def prepack_weight_nk(w_packed_nk, K: int, N: int, G: int, stream=None):
+    """uint8 [N, K/2] packed int4 (a weight stored transposed) on the GPU -> a new prepacked uint8 tensor."""
+    import torch
+    out = torch.empty(wqbmm_prepacked_weight_bytes(K, N, G), dtype=torch.uint8, device=w_packed_nk.device)
+    wqbmm_prepack_weight_nk(w_packed_nk, out, K, N, G, stream)
     return out
 
 

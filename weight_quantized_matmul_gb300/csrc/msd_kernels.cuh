@@ -226,16 +226,20 @@ __device__ __forceinline__ void convert_tile(const uint8_t *__restrict__ src, ui
 
 // ------------------------------------------------------------------------------------------------ kernels
 
+// kNK: the packed weights come as [N, K/2] (each column's K contiguous, two k per byte), else as [K/2, N].
+template <bool kNK>
 __global__ void prepack_kernel(const uint8_t *__restrict__ in, uint8_t *__restrict__ out, int K, int N,
                                int kb_total) {
     __shared__ uint8_t tile[kKBlock / 2][kTileN + 4];
     const int nt = blockIdx.x, kb = blockIdx.y;
     const int half_k = K / 2;
     for (int idx = threadIdx.x; idx < (kKBlock / 2) * kTileN; idx += blockDim.x) {
-        const int kk = idx / kTileN, c = idx % kTileN;
+        // consecutive threads read consecutive bytes of the source
+        const int kk = kNK ? idx % (kKBlock / 2) : idx / kTileN, c = kNK ? idx / (kKBlock / 2) : idx % kTileN;
         const int gk = kb * (kKBlock / 2) + kk, gn = nt * kTileN + c;
         uint8_t v = 0;                                               // two zero weights
-        if (gk < half_k && gn < N) v = in[static_cast<size_t>(gk) * N + gn];
+        if (gk < half_k && gn < N)
+            v = kNK ? in[static_cast<size_t>(gn) * half_k + gk] : in[static_cast<size_t>(gk) * N + gn];
         tile[kk][c] = static_cast<uint8_t>(v ^ 0x88u);               // w -> w + 8 in both nibbles
     }
     __syncthreads();

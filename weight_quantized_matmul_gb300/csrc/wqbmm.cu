@@ -405,6 +405,26 @@ wqbmm_status static_scratch_address(int dev, void **addr) {
     return WQBMM_OK;
 }
 
+wqbmm_status prepack(const uint8_t *w_packed, void *w_prepacked, int64_t K, int64_t N, int64_t G, bool nk,
+                     wqbmm_stream_t stream) {
+    if (!w_packed || !w_prepacked) return WQBMM_ERR_NULLPTR;
+    wqbmm_status st = check_kng(K, N, G);
+    if (st != WQBMM_OK) return st;
+    if (!aligned16(w_prepacked)) return WQBMM_ERR_INVALID;
+    int dev;
+    DeviceInfo *info;
+    if ((st = current_device(&dev, &info)) != WQBMM_OK) return st;
+    const dim3 grid(static_cast<unsigned>(ceil_div(N, kTileN)), static_cast<unsigned>(ceil_div(K, kKBlock)));
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *out = static_cast<uint8_t *>(w_prepacked);
+    const int kb_total = static_cast<int>(ceil_div(K, kKBlock));
+    if (nk)
+        prepack_kernel<true><<<grid, 256, 0, s>>>(w_packed, out, static_cast<int>(K), static_cast<int>(N), kb_total);
+    else
+        prepack_kernel<false><<<grid, 256, 0, s>>>(w_packed, out, static_cast<int>(K), static_cast<int>(N), kb_total);
+    return cudaPeekAtLastError() == cudaSuccess ? WQBMM_OK : WQBMM_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace wqbmm
 
@@ -436,18 +456,12 @@ wqbmm_status wqbmm_prepacked_weight_bytes(int64_t K, int64_t N, int64_t G, size_
 
 wqbmm_status wqbmm_prepack_weight(const uint8_t *w_packed, void *w_prepacked, int64_t K, int64_t N, int64_t G,
                                   wqbmm_stream_t stream) {
-    if (!w_packed || !w_prepacked) return WQBMM_ERR_NULLPTR;
-    wqbmm_status st = check_kng(K, N, G);
-    if (st != WQBMM_OK) return st;
-    if (!aligned16(w_prepacked)) return WQBMM_ERR_INVALID;
-    int dev;
-    DeviceInfo *info;
-    if ((st = current_device(&dev, &info)) != WQBMM_OK) return st;
-    const dim3 grid(static_cast<unsigned>(ceil_div(N, kTileN)), static_cast<unsigned>(ceil_div(K, kKBlock)));
-    prepack_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        w_packed, static_cast<uint8_t *>(w_prepacked), static_cast<int>(K), static_cast<int>(N),
-        static_cast<int>(ceil_div(K, kKBlock)));
-    return cudaPeekAtLastError() == cudaSuccess ? WQBMM_OK : WQBMM_ERR_CUDA;
+    return prepack(w_packed, w_prepacked, K, N, G, false, stream);
+}
+
+wqbmm_status wqbmm_prepack_weight_nk(const uint8_t *w_packed_nk, void *w_prepacked, int64_t K, int64_t N, int64_t G,
+                                     wqbmm_stream_t stream) {
+    return prepack(w_packed_nk, w_prepacked, K, N, G, true, stream);
 }
 
 wqbmm_status wqbmm_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t G, size_t *bytes) {
