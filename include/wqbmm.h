@@ -128,6 +128,22 @@ WQBMM_API wqbmm_status wqbmm_run(const void *x, const void *w_prepacked, const v
                                  size_t workspace_bytes, wqbmm_stream_t stream);
 
 /*
+ * wqbmm_run with the operator's two optional inputs (its V2 interface): asymmetric weights and a bias. The weight
+ * of group g, column n stands for (w - zero_point[g, n]) * antiquant_scale[g, n], the dequantization convention of
+ * the GatherDequantInt8 page ("数学语义") and of the RKNN matmul page (section 4.1.1.3.1), with zero points per
+ * group and column like the scales. The planes of x do not change; step 9 becomes Y_i = A_i . W_g - zp S_i, S_i the
+ * sum of plane i over the group, and bias[n] is added to the accumulated sum of step 11 before the fp16 rounding.
+ *   zero_point  device, fp16 [K/G, N] row-major, or null (symmetric weights, as wqbmm_run)
+ *   bias        device, fp16 [N], or null
+ * Both start on 16-byte boundaries when given. Every other argument, the workspace size, the launch and the errors
+ * are as for wqbmm_run (wqbmm_workspace_bytes does not depend on the optional inputs).
+ */
+WQBMM_API wqbmm_status wqbmm_run_ex(const void *x, const void *w_prepacked, const void *antiquant_scale,
+                                    const void *zero_point, const void *bias, void *y, int64_t M, int64_t K,
+                                    int64_t N, int64_t G, void *workspace, size_t workspace_bytes,
+                                    wqbmm_stream_t stream);
+
+/*
  * Exposes steps 1-8 exactly as the run kernel computes them (for bit-exact checks).
  *   x       device, fp16 [M, K]
  *   planes  device, int8 [3, M, K]: plane i of row m at planes[(i * M + m) * K + k], values in [-7, 7]

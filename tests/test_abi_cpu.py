@@ -116,6 +116,17 @@ CASES = [
     ("run_misaligned_weights", lambda L: L.wqbmm_run(A, MIS, A, A, 1, 128, 128, 128, A, 1 << 20, None), INVALID),
     ("run_misaligned_workspace", lambda L: L.wqbmm_run(A, A, A, A, 1, 65536, 256, 128, MIS, 1 << 20, None),
      INVALID),
+    ("run_ex_null_x", lambda L: L.wqbmm_run_ex(None, A, A, A, A, A, 1, 128, 128, 128, A, 1 << 20, None), NULLPTR),
+    ("run_ex_null_scale", lambda L: L.wqbmm_run_ex(A, A, None, A, A, A, 1, 128, 128, 128, A, 1 << 20, None),
+     NULLPTR),
+    ("run_ex_null_y", lambda L: L.wqbmm_run_ex(A, A, A, A, A, None, 1, 128, 128, 128, A, 1 << 20, None), NULLPTR),
+    ("run_ex_misaligned_zero_point",
+     lambda L: L.wqbmm_run_ex(A, A, A, MIS, None, A, 1, 128, 128, 128, A, 1 << 20, None), INVALID),
+    ("run_ex_misaligned_bias",
+     lambda L: L.wqbmm_run_ex(A, A, A, None, MIS, A, 200, 128, 128, 128, A, 1 << 20, None), INVALID),
+    ("run_ex_bad_group", lambda L: L.wqbmm_run_ex(A, A, A, A, A, A, 8, 128, 128, 16, A, 1 << 20, None), INVALID),
+    ("run_ex_null_workspace_needed",
+     lambda L: L.wqbmm_run_ex(A, A, A, A, A, A, 1, 65536, 256, 128, None, 0, None), NULLPTR),
     ("unfold_null_planes", lambda L: L.wqbmm_debug_unfold(A, 1, 128, 128, None, A, None), NULLPTR),
     ("unfold_bad_group", lambda L: L.wqbmm_debug_unfold(A, 1, 128, 100, A, A, None), INVALID),
     ("partials_group_out_of_range",
@@ -154,3 +165,5 @@ def test_no_device_is_a_cuda_error(lib):
     # valid arguments, but no GPU: the device check fails with a CUDA error and nothing is launched
     assert lib.wqbmm_run(A, A, A, A, 16, 8192, 28672, 64, None, 0, None) == wq.ERR_CUDA
     assert lib.wqbmm_run(A, A, A, A, 2048, 8192, 28672, 64, A, 1 << 30, None) == wq.ERR_CUDA
+    assert lib.wqbmm_run_ex(A, A, A, A, A, A, 8, 4096, 11008, 128, A, 1 << 30, None) == wq.ERR_CUDA
+    assert lib.wqbmm_run_ex(A, A, A, None, None, A, 1, 4096, 4096, 128, A, 1 << 30, None) == wq.ERR_CUDA

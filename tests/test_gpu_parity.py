@@ -352,3 +352,104 @@ def test_workload_sampled_rows(dev, name, nrows):
     wq.wqbmm_debug_group_partials(to_dev(x, dev), w_pre, wl.M, wl.K, wl.N, wl.G, g, y123, ws)
     got = y123.cpu().numpy()[:, rows]
     np.testing.assert_array_equal(got, oracle.group_partials(x, wp, wl.N, wl.G, g, oracle.MODE_F, rows=rows))
+
+
+# ------------------------------------------------------------------------------------------- zero points, bias
+
+EX_CASES = [
+    # M, K, N, G, zero-point kind (None: no zero point), bias; covering every kernel path
+    (1, 4096, 520, 128, "int", True),          # decode kernel, one row
+    (2, 1024, 1000, 32, "frac", True),         # decode kernel, two rows, ragged last CTA
+    (1, 65536, 256, 128, "frac", False),       # decode kernel, many passes
+    (3, 512, 264, 64, "int", True),            # small-M tensor-core kernel
+    (5, 384, 136, 32, "frac", True),
+    (12, 2048, 640, 128, "int", False),
+    (4, 4096, 1024, 128, "frac", True),        # cluster-reduced split-K
+    (3, 65536, 256, 128, "frac", True),        # split-K through the workspace
+    (17, 640, 392, 64, None, True),            # bias alone
+    (40, 1280, 520, 128, "frac", False),
+    (64, 256, 128, 128, "int", True),          # large-M: unfold pre-pass + 128 x 128 tiles
+    (200, 96, 1000, 32, "frac", True),
+    (256, 320, 392, 64, None, True),
+    (300, 1280, 520, 128, "frac", False),
+]
+
+
+def gpu_run_ex(x, wp, sc, zp, bias, G, dev):
+    M, K = x.shape
+    N = sc.shape[1]
+    w_pre = wq.prepack_weight(to_dev(wp, dev), K, N, G)
+    y = wq.msd_matmul(to_dev(x, dev), w_pre, to_dev(sc, dev), G,
+                      zero_point=None if zp is None else to_dev(zp, dev),
+                      bias=None if bias is None else to_dev(bias, dev))
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("M,K,N,G,zkind,with_bias", EX_CASES)
+def test_run_ex_matches_oracle(dev, M, K, N, G, zkind, with_bias):
+    wl = I.small_case(M, K, N, G, seed=3 * M + K + N, x_dist="t3_clip60" if M % 2 else "normal")
+    x, wp, sc = I.make_inputs(wl)
+    zp = None if zkind is None else I.make_zero_point(wl, zkind)
+    bias = I.make_bias(wl) if with_bias else None
+    y = gpu_run_ex(x, wp, sc, zp, bias, G, dev)
+    for mode, what in ((oracle.MODE_D, "binary64 oracle"), (oracle.MODE_F, "binary32-unfold oracle")):
+        ref = oracle.msd_matmul_ex(x, wp, sc, G, zero_point=zp, bias=bias, mode=mode)
+        assert_within_tolerance(y, ref, what)
+
+
+@pytest.mark.parametrize("M,K,N,G", [(1, 1024, 264, 64), (9, 1024, 264, 64), (130, 512, 256, 64)])
+def test_run_ex_without_optionals_is_run(dev, M, K, N, G):
+    """Null zero point and bias take the plain kernels: the output is the one of wqbmm_run, bit for bit."""
+    x, wp, sc = I.make_inputs(I.small_case(M, K, N, G, seed=M + 40))
+    xd, sd = to_dev(x, dev), to_dev(sc, dev)
+    w_pre = wq.prepack_weight(to_dev(wp, dev), K, N, G)
+    ws = wq.allocate_workspace(M, K, N, G, dev)
+    a = torch.empty((M, N), dtype=torch.float16, device=dev)
+    b = torch.empty((M, N), dtype=torch.float16, device=dev)
+    wq.wqbmm_run(xd, w_pre, sd, a, M, K, N, G, ws)
+    wq.wqbmm_run_ex(xd, w_pre, sd, None, None, b, M, K, N, G, ws)
+    np.testing.assert_array_equal(a.cpu().numpy().view(np.uint16), b.cpu().numpy().view(np.uint16))
+
+
+def test_run_ex_zero_zero_point_and_bias_change_nothing(dev):
+    """zp = 0 and bias = 0 give the plain product (1 + 0/8 = 1 exactly; adding +0 keeps every nonzero value)."""
+    M, K, N, G = 6, 1024, 392, 128
+    x, wp, sc = I.make_inputs(I.small_case(M, K, N, G, seed=77))
+    xd, sd = to_dev(x, dev), to_dev(sc, dev)
+    w_pre = wq.prepack_weight(to_dev(wp, dev), K, N, G)
+    ws = wq.allocate_workspace(M, K, N, G, dev)
+    a = torch.empty((M, N), dtype=torch.float16, device=dev)
+    b = torch.empty((M, N), dtype=torch.float16, device=dev)
+    zeros_zp = torch.zeros((K // G, N), dtype=torch.float16, device=dev)
+    zeros_b = torch.zeros(N, dtype=torch.float16, device=dev)
+    wq.wqbmm_run(xd, w_pre, sd, a, M, K, N, G, ws)
+    wq.wqbmm_run_ex(xd, w_pre, sd, zeros_zp, zeros_b, b, M, K, N, G, ws)
+    np.testing.assert_array_equal(a.cpu().numpy().astype(np.float64), b.cpu().numpy().astype(np.float64))
+
+
+def test_run_ex_rejects_unaligned_optionals(dev):
+    M, K, N, G = 2, 256, 128, 128
+    x, wp, sc = I.make_inputs(I.small_case(M, K, N, G, seed=4))
+    xd, sd = to_dev(x, dev), to_dev(sc, dev)
+    w_pre = wq.prepack_weight(to_dev(wp, dev), K, N, G)
+    ws = wq.allocate_workspace(M, K, N, G, dev)
+    y = torch.full((M, N), 7.0, dtype=torch.float16, device=dev)
+    buf = torch.zeros(2 * N + 8, dtype=torch.float16, device=dev)
+    for zp, bias in ((buf.data_ptr() + 2, None), (None, buf.data_ptr() + 2)):
+        with pytest.raises(wq.WqbmmError) as e:
+            wq.wqbmm_run_ex(xd, w_pre, sd, zp, bias, y, M, K, N, G, ws)
+        assert e.value.status == wq.ERR_INVALID
+    torch.cuda.synchronize()
+    assert (y == 7.0).all()
+
+
+def test_run_ex_mid_workload_sampled_rows(dev):
+    """The mid-batch workload (M=128, K=5120, N=13824, G=128) with fractional zero points and a bias, through the
+    large-M kernels, on sampled rows."""
+    wl = I.WORKLOADS["mid_m128_k5120_n13824"]
+    x, wp, sc = I.make_inputs(wl)
+    zp, bias = I.make_zero_point(wl, "frac"), I.make_bias(wl)
+    y = gpu_run_ex(x, wp, sc, zp, bias, wl.G, dev)
+    rows = I.sample_rows(wl, 8)
+    ref = oracle.msd_matmul_ex(x, wp, sc, wl.G, zero_point=zp, bias=bias, mode=oracle.MODE_D, rows=rows)
+    assert_within_tolerance(y[rows], ref, wl.name)

@@ -16,7 +16,7 @@ __all__ = [
     "wqbmm_workspace_bytes", "wqbmm_run", "wqbmm_debug_unfold", "wqbmm_debug_group_partials",
     "wqbmm_read_device_status", "wqbmm_debug_wait_timeout", "wqbmm_status_string", "prepack_weight",
     "allocate_workspace", "msd_matmul", "SYMBOLS", "wqbmm_run_static_scratch", "wqbmm_prepack_weight_nk",
-    "prepack_weight_nk",
+    "prepack_weight_nk", "wqbmm_run_ex",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -30,7 +30,7 @@ OK, ERR_NULLPTR, ERR_INVALID, ERR_UNSUPPORTED_ARCH, ERR_CUDA, ERR_DEVICE_TIMEOUT
 SYMBOLS = (
     "wqbmm_prepacked_weight_bytes", "wqbmm_prepack_weight", "wqbmm_workspace_bytes", "wqbmm_run",
     "wqbmm_debug_unfold", "wqbmm_debug_group_partials", "wqbmm_read_device_status", "wqbmm_debug_wait_timeout",
-    "wqbmm_status_string", "wqbmm_run_static_scratch", "wqbmm_prepack_weight_nk",
+    "wqbmm_status_string", "wqbmm_run_static_scratch", "wqbmm_prepack_weight_nk", "wqbmm_run_ex",
 )
 
 
@@ -60,6 +60,7 @@ def load_library():
                 "wqbmm_prepack_weight": [p, p, i64, i64, i64, p],
                 "wqbmm_workspace_bytes": [i64, i64, i64, i64, ctypes.POINTER(sz)],
                 "wqbmm_run": [p, p, p, p, i64, i64, i64, i64, p, sz, p],
+                "wqbmm_run_ex": [p, p, p, p, p, p, i64, i64, i64, i64, p, sz, p],
                 "wqbmm_debug_unfold": [p, i64, i64, i64, p, p, p],
                 "wqbmm_debug_group_partials": [p, p, i64, i64, i64, i64, i64, p, p, sz, p],
                 "wqbmm_read_device_status": [ctypes.POINTER(ctypes.c_int32), ctypes.c_int, p],
@@ -133,6 +134,15 @@ def wqbmm_run(x, w_prepacked, antiquant_scale, y, M: int, K: int, N: int, G: int
                                      _ptr(workspace), workspace_bytes, _stream(stream)), "wqbmm_run")
 
 
+def wqbmm_run_ex(x, w_prepacked, antiquant_scale, zero_point, bias, y, M: int, K: int, N: int, G: int,
+                 workspace=None, workspace_bytes: int | None = None, stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().wqbmm_run_ex(_ptr(x), _ptr(w_prepacked), _ptr(antiquant_scale), _ptr(zero_point),
+                                        _ptr(bias), _ptr(y), M, K, N, G, _ptr(workspace), workspace_bytes,
+                                        _stream(stream)), "wqbmm_run_ex")
+
+
 def wqbmm_run_static_scratch(x, w_prepacked, antiquant_scale, y, M: int, K: int, N: int, G: int,
                              stream=None) -> None:
     """wqbmm_run without a caller workspace: the library's fixed 2 MiB device scratch is used instead (for callers
@@ -194,8 +204,10 @@ def allocate_workspace(M: int, K: int, N: int, G: int, device):
     return torch.zeros(nbytes, dtype=torch.uint8, device=device)
 
 
-def msd_matmul(x, w_prepacked, antiquant_scale, G: int, y=None, workspace=None, stream=None):
-    """y [M, N] fp16 = MSD matmul of x [M, K] fp16 with prepacked int4 weights and antiquant_scale [K/G, N] fp16."""
+def msd_matmul(x, w_prepacked, antiquant_scale, G: int, y=None, workspace=None, stream=None, zero_point=None,
+               bias=None):
+    """y [M, N] fp16 = MSD matmul of x [M, K] fp16 with prepacked int4 weights and antiquant_scale [K/G, N] fp16;
+    optionally with zero points [K/G, N] fp16 (weights (w - zp) * scale) and a bias [N] fp16."""
     import torch
     M, K = x.shape
     N = antiquant_scale.shape[1]
@@ -203,5 +215,8 @@ def msd_matmul(x, w_prepacked, antiquant_scale, G: int, y=None, workspace=None, 
         y = torch.empty((M, N), dtype=torch.float16, device=x.device)
     if workspace is None:
         workspace = allocate_workspace(M, K, N, G, x.device)
-    wqbmm_run(x, w_prepacked, antiquant_scale, y, M, K, N, G, workspace, None, stream)
+    if zero_point is None and bias is None:
+        wqbmm_run(x, w_prepacked, antiquant_scale, y, M, K, N, G, workspace, None, stream)
+    else:
+        wqbmm_run_ex(x, w_prepacked, antiquant_scale, zero_point, bias, y, M, K, N, G, workspace, None, stream)
     return y

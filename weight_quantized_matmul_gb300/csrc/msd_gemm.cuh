@@ -31,20 +31,24 @@ constexpr int kPlaneImageBytes = kGemmTileM * kKBlock;         // 16384: one pla
 constexpr int kGemmConstRowBytes = 16;                         // float4 per (row, group)
 constexpr int kGemmSmemLimit = 232448;                         // opt-in shared memory per CTA on sm_103
 
-// Shared-memory layout of msd_gemm_kernel (depends on the group size through the groups per k-block).
+// Shared-memory layout of msd_gemm_kernel (depends on the group size through the groups per k-block, and on whether
+// zero points are staged).
 struct GemmLayout {
     int gpk, const_bytes, scale_bytes, stage_bytes, p_stages;
-    int off_const, off_scale, off_scale32, off_p, off_b, off_bar, off_misc, smem_bytes;
+    int off_const, off_scale, off_scale32, off_zp, off_zp32, off_p, off_b, off_bar, off_misc, smem_bytes;
     __host__ __device__ static int align(int v, int a) { return (v + a - 1) / a * a; }
-    __host__ __device__ explicit GemmLayout(int G) {
+    __host__ __device__ GemmLayout(int G, bool zp) {
         gpk = kKBlock / G;
         const_bytes = gpk * kGemmTileM * kGemmConstRowBytes;
         scale_bytes = gpk * kGemmTileN * 2;
         // stage: three plane images | packed weight tile | constants | scale tile (fp16, as loaded) | scale (fp32)
+        //        [| zero-point tile (fp16, as loaded) | 1 + zp / 8 (fp32)]
         off_const = 3 * kPlaneImageBytes + kPackedTileBytes;
         off_scale = off_const + const_bytes;
         off_scale32 = off_scale + scale_bytes;
-        stage_bytes = align(off_scale32 + 2 * scale_bytes, 1024);
+        off_zp = off_scale32 + 2 * scale_bytes;
+        off_zp32 = off_zp + scale_bytes;
+        stage_bytes = align(zp ? off_zp32 + 2 * scale_bytes : off_zp, 1024);
         off_b = 0;                                             // converted weights ring first (1024-aligned)
         off_p = kGemmBStages * (kGemmTileN * kKBlock);
         const int fixed = off_p + 1024 /*align slack*/ + 512 /*barriers and flags*/;
@@ -60,6 +64,7 @@ struct GemmParams {
     const uint8_t *w;           // prepacked tiles
     const uint8_t *planes;      // [m_tiles][kb_total][3][16 KB] from unfold_planes_kernel
     const float4 *consts;       // [m_tiles][K/G][128 rows]
+    const __half *bias;         // [N] or null
     __half *y;
     int32_t *dbg_y123;          // debug: integer partials of group dbg_group, else null
     int M, K, N, G;
@@ -120,10 +125,13 @@ __device__ __forceinline__ uint32_t pack_half2(float2 v) {
 
 // kDebug: only the k-block of group p.dbg_group runs, the constant records hold the plane sums, and the epilogue
 // writes that group's integer partials instead of y.
-template <bool kDebug>
+// kZp: zero-point tiles ride with the scale tiles; the converters turn them into 1 + zp / 8, the factor of the
+// offset correction when the quantized weight is w - zp (the dots then need (8 + zp) S_i taken off).
+template <bool kDebug, bool kZp>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    msd_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmap_s) {
-    const GemmLayout L(p.G);
+    msd_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmap_s,
+                    const __grid_constant__ CUtensorMap tmap_z) {
+    const GemmLayout L(p.G, kZp);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *b_ring = smem + L.off_b;
@@ -156,7 +164,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     auto groups_in = [&](int kb) { return (min(K, (kb + 1) * kKBlock) - kb * kKBlock) / G; };
     auto stage_tx = [&](int kb) {
         return static_cast<uint32_t>(3 * kPlaneImageBytes + kPackedTileBytes + groups_in(kb) * kGemmTileM * 16 +
-                                     (kDebug ? 0 : gpk * kGemmTileN * 2));
+                                     (kDebug ? 0 : (kZp ? 2 : 1) * gpk * kGemmTileN * 2));
     };
     // read-only inputs of the call (weights, scales) may be fetched before the preceding kernel (the unfold) ends
     auto issue_static = [&](int i, uint64_t pol_stream, uint64_t pol_keep) {
@@ -166,6 +174,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         bulk_g2s(dst + 3 * kPlaneImageBytes, p.w + (static_cast<size_t>(nt) * p.kb_total + kb) * kPackedTileBytes,
                  kPackedTileBytes, full_p(s), pol_stream);
         if (!kDebug) tma_load_2d(dst + L.off_scale, &tmap_s, nt * kGemmTileN, kb * gpk, full_p(s), pol_keep);
+        if (kZp && !kDebug) tma_load_2d(dst + L.off_zp, &tmap_z, nt * kGemmTileN, kb * gpk, full_p(s), pol_keep);
     };
     auto issue_dynamic = [&](int i, uint64_t pol_keep) {
         const int s = i % P, kb = kb0 + i;
@@ -197,6 +206,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         pol_stream = l2_policy_evict_first();
         pol_keep = l2_policy_evict_last();
         prefetch_tensormap(&tmap_s);
+        if (kZp) prefetch_tensormap(&tmap_z);
         pdl_launch_dependents();
         for (int i = 0; i < first; ++i) issue_static(i, pol_stream, pol_keep);
         pdl_wait();
@@ -277,6 +287,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const __half2 *s16 = reinterpret_cast<const __half2 *>(stage + L.off_scale);
                 float2 *s32 = reinterpret_cast<float2 *>(stage + L.off_scale32);
                 for (int j = ct; j < gpk * kGemmTileN / 2; j += kConvThreads) s32[j] = __half22float2(s16[j]);
+                if constexpr (kZp) {
+                    const __half2 *z16 = reinterpret_cast<const __half2 *>(stage + L.off_zp);
+                    float2 *z32 = reinterpret_cast<float2 *>(stage + L.off_zp32);
+                    for (int j = ct; j < gpk * kGemmTileN / 2; j += kConvThreads) {
+                        const float2 z = __half22float2(z16[j]);
+                        z32[j] = make_float2(fmaf(z.x, 0.125f, 1.0f), fmaf(z.y, 0.125f, 1.0f));
+                    }
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sready(s));
             }
@@ -351,6 +369,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const float2 c3 = make_float2(cr.z, cr.z), nc = make_float2(-cr.w, -cr.w);
                     const float4 *srow =
                         reinterpret_cast<const float4 *>(stage + L.off_scale32) + (gg * kGemmTileN + half * 64) / 4;
+                    const float4 *zrow =
+                        reinterpret_cast<const float4 *>(stage + L.off_zp32) + (gg * kGemmTileN + half * 64) / 4;
 #pragma unroll
                     for (int ch = 0; ch < 4; ++ch) {
                         uint32_t d1[16], d2[16], d3[16];
@@ -361,6 +381,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {
                             const float4 sc = srow[ch * 4 + q4];           // same address in every lane: broadcast
+                            float4 zf = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+                            if constexpr (kZp) zf = zrow[ch * 4 + q4];
 #pragma unroll
                             for (int h = 0; h < 2; ++h) {
                                 const int q = q4 * 2 + h;
@@ -368,7 +390,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                 const float2 v1 = make_float2(__uint_as_float(d1[2 * q]), __uint_as_float(d1[2 * q + 1]));
                                 const float2 v2 = make_float2(__uint_as_float(d2[2 * q]), __uint_as_float(d2[2 * q + 1]));
                                 const float2 v3 = make_float2(__uint_as_float(d3[2 * q]), __uint_as_float(d3[2 * q + 1]));
-                                float2 acc = __ffma2_rn(c1, v1, nc);
+                                float2 ncz = nc;
+                                if constexpr (kZp)
+                                    ncz = __fmul2_rn(nc, h == 0 ? make_float2(zf.x, zf.y) : make_float2(zf.z, zf.w));
+                                float2 acc = __ffma2_rn(c1, v1, ncz);
                                 acc = __ffma2_rn(c2, v2, acc);
                                 acc = __ffma2_rn(c3, v3, acc);
                                 yacc[ch * 8 + q] = __ffma2_rn(scv, acc, yacc[ch * 8 + q]);
@@ -393,6 +418,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int c8 = 0; c8 < 8; ++c8) {
                 const int n = nt * kGemmTileN + half * 64 + c8 * 8;
                 if (n < N) {
+                    if (p.bias != nullptr) {
+                        // the same 8 bias values for every row of the tile (L1 hits after the first warp)
+                        const uint4 braw = *reinterpret_cast<const uint4 *>(p.bias + n);
+                        const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            yacc[c8 * 4 + q] = __fadd2_rn(yacc[c8 * 4 + q],
+                                                          __half22float2(*reinterpret_cast<const __half2 *>(&bw[q])));
+                    }
                     const uint4 o = make_uint4(pack_half2(yacc[c8 * 4 + 0]), pack_half2(yacc[c8 * 4 + 1]),
                                                pack_half2(yacc[c8 * 4 + 2]), pack_half2(yacc[c8 * 4 + 3]));
                     *reinterpret_cast<uint4 *>(yrow + n) = o;

@@ -81,6 +81,8 @@ __global__ void __launch_bounds__(128) gemv_unfold_kernel(const __half *__restri
 struct GemvParams {
     const uint8_t *w;           // prepacked tiles
     const __half *scale;        // [K/G, N]
+    const __half *zp;           // [K/G, N] zero points (kernel instantiated with kZp), else null
+    const __half *bias;         // [N] or null
     const int8_t *planes;       // from gemv_unfold_kernel
     const float4 *consts;
     __half *y;
@@ -136,7 +138,9 @@ struct GemvSmem {
     int abort_flag;
 };
 
-template <int MR, bool kDebug>
+// kZp: the quantized weight is w - zp[g, n], so a group's dots need (8 + zp) S_i taken off instead of 8 S_i: the
+// lane that applies the group's correction scales it by 1 + zp / 8.
+template <int MR, bool kDebug, bool kZp>
 __global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvParams p) {
     extern __shared__ __align__(128) uint8_t gemv_smem_raw[];
     GemvSmem<MR> &sm = *reinterpret_cast<GemvSmem<MR> *>(gemv_smem_raw);
@@ -173,6 +177,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvPar
         // they are used, so no instruction waits for them here)
         uint4 wa[kGemvKbPerPass], wb[kGemvKbPerPass];
         __half sa[kGemvKbPerPass], sb[kGemvKbPerPass];
+        __half2 zab[kGemvKbPerPass];                   // zero points of rows a and b (first chunk lane of a group)
 #pragma unroll
         for (int j = 0; j < kGemvKbPerPass; ++j) {
             if (j < nkb) {
@@ -202,6 +207,11 @@ __global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvPar
                 const bool in = j < nkb && g < Gn;
                 sa[j] = in && n_a < N ? __ldg(p.scale + static_cast<size_t>(g) * N + n_a) : __half(0.0f);
                 sb[j] = in && n_b < N ? __ldg(p.scale + static_cast<size_t>(g) * N + n_b) : __half(0.0f);
+                if constexpr (kZp) {
+                    const bool first = in && (chunk & (lpg_chunks - 1)) == 0;
+                    zab[j] = __halves2half2(first && n_a < N ? __ldg(p.zp + static_cast<size_t>(g) * N + n_a) : __half(0.0f),
+                                            first && n_b < N ? __ldg(p.zp + static_cast<size_t>(g) * N + n_b) : __half(0.0f));
+                }
             }
         }
         if (pass == 0 && threadIdx.x != 0) pdl_wait();
@@ -252,10 +262,16 @@ __global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvPar
                     // this lane's share of the group: c_i times its own dots; the group's first chunk also takes
                     // the offset correction (the combine is linear, the lanes are added at the end)
                     const float corr = (chunk & (lpg_chunks - 1)) == 0 ? -cr.w : 0.0f;
-                    float ta = fmaf(cr.x, small_int_to_float(da[0]), corr);
+                    float corr_a = corr, corr_b = corr;
+                    if constexpr (kZp) {
+                        const float2 z = __half22float2(zab[j]);
+                        corr_a = corr * fmaf(z.x, 0.125f, 1.0f);
+                        corr_b = corr * fmaf(z.y, 0.125f, 1.0f);
+                    }
+                    float ta = fmaf(cr.x, small_int_to_float(da[0]), corr_a);
                     ta = fmaf(cr.y, small_int_to_float(da[1]), ta);
                     ta = fmaf(cr.z, small_int_to_float(da[2]), ta);
-                    float tb = fmaf(cr.x, small_int_to_float(db[0]), corr);
+                    float tb = fmaf(cr.x, small_int_to_float(db[0]), corr_b);
                     tb = fmaf(cr.y, small_int_to_float(db[1]), tb);
                     tb = fmaf(cr.z, small_int_to_float(db[2]), tb);
                     yacc[m][0] = fmaf(__half2float(sa[j]), ta, yacc[m][0]);
@@ -292,7 +308,10 @@ __global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvPar
 #pragma unroll
             for (int w = 0; w < kGemvWarps; ++w) acc += sm.red[w][m][c];
             const int n = col0 + c;
-            if (m < p.M && n < N) p.y[static_cast<size_t>(m) * N + n] = __float2half_rn(acc);
+            if (m < p.M && n < N) {
+                if (p.bias != nullptr) acc += __half2float(p.bias[n]);
+                p.y[static_cast<size_t>(m) * N + n] = __float2half_rn(acc);
+            }
         }
     }
     // no bulk copy may still be writing shared memory when the CTA exits

@@ -52,7 +52,7 @@ constexpr int kEpiBarrierId = 1;
 constexpr int kMaxGroupsPerKBlock = kKBlock / 32;
 constexpr int kConstFloatsPerGroup = 8 * 16;          // a1 a2 a3 corr S1 S2 S3 (pad) x 16 rows
 constexpr int kScaleFloatsOffset = kMaxGroupsPerKBlock * kConstFloatsPerGroup;   // then scale[group][128 columns]
-constexpr int kConstStageFloats = kScaleFloatsOffset + kMaxGroupsPerKBlock * kTileN;
+constexpr int kZpFloatsOffset = kScaleFloatsOffset + kMaxGroupsPerKBlock * kTileN;  // then 1 + zp / 8 (zero points)
 
 // Method constants (page section 4.1): unfold factors and the combine weights 1/7.49, 1/(7.49*14.98), ...
 constexpr float kF1 = 7.49f;
@@ -73,17 +73,21 @@ enum WaitSite : int {
     kSiteDebugWait = 9,
 };
 
-template <int NMMA>
+template <int NMMA, bool kZp>
 struct Cfg {
     static_assert(NMMA == 16 || NMMA == 32 || NMMA == 48, "MMA N must be 16, 32 or 48");
     static constexpr int kMaxM = NMMA / 3;                         // rows of x per CTA (plane stride in B rows)
     static constexpr int kBufStride = NMMA <= 16 ? 16 : (NMMA <= 32 ? 32 : 64);   // TMEM columns per buffer
     static constexpr int kTmemCols = 2 * kBufStride < 32 ? 32 : 2 * kBufStride;
     static constexpr int kBTileBytes = NMMA * kKBlock;
-    // one load stage: packed weights, the x tile (rows x 128 k, fp16) and the scale tile (groups x 128 n, fp16)
+    // one load stage: packed weights, the x tile (rows x 128 k, fp16), the scale tile (groups x 128 n, fp16) and,
+    // with zero points, the zero-point tile (same shape)
     static constexpr int kXOff = kPackedTileBytes;
     static constexpr int kSOff = kXOff + kMaxM * kKBlock * 2;
-    static constexpr int kStageBytes = kSOff + kMaxGroupsPerKBlock * kTileN * 2;
+    static constexpr int kZOff = kSOff + kMaxGroupsPerKBlock * kTileN * 2;
+    static constexpr int kStageBytes = kZOff + (kZp ? kMaxGroupsPerKBlock * kTileN * 2 : 0);
+    // per operand slot: the combine constants, the fp32 scales and (zero points) the factors 1 + zp / 8
+    static constexpr int kConstStageFloats = kZpFloatsOffset + (kZp ? kMaxGroupsPerKBlock * kTileN : 0);
     // shared memory carve-up (offsets from a 1024-byte aligned base)
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kCStages * kATileBytes;
@@ -104,6 +108,8 @@ struct RunParams {
     const __half *x;
     const uint8_t *w;           // prepacked tiles
     const __half *scale;
+    const __half *zp;           // [K/G, N] zero points (kernels instantiated with kZp), else null
+    const __half *bias;         // [N] or null
     __half *y;
     float *ws_part;             // [splits, M, N] split-K partial sums (splits > 1)
     uint32_t *ws_count;         // [m_tiles, n_tiles] arrival counters (splits > 1)
@@ -365,10 +371,14 @@ __device__ __forceinline__ void unfold_rows(const __half *xs, uint8_t *bt, float
     }
 }
 
-template <int NMMA>
+// kZp: the weights carry zero points, w - zp[g, n] being the quantized value the scale multiplies. The plane dots
+// then need (8 + zp) S_i taken off instead of 8 S_i, that is the correction term times 1 + zp / 8.
+template <int NMMA, bool kZp>
 __global__ void __launch_bounds__(kThreads, 2)
-    msd_kernel(const RunParams p, const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_s) {
-    using C = Cfg<NMMA>;
+    msd_kernel(const RunParams p, const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_s,
+               const __grid_constant__ CUtensorMap tmap_z) {
+    using C = Cfg<NMMA, kZp>;
+    constexpr int kConstStageFloats = C::kConstStageFloats;
     constexpr int kMaxM = C::kMaxM;
     constexpr int kPStages = C::kPStages;
     extern __shared__ uint8_t smem_raw[];
@@ -407,9 +417,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     const int nkb = kb1 - kb0;
 
-    // One load stage: the k-block's packed weight tile, x tile and scale tile, all counted on full_p(s).
+    // One load stage: the k-block's packed weight tile, x tile, scale tile and zero-point tile, all counted on
+    // full_p(s).
     const uint8_t *w_src = p.w + (static_cast<size_t>(nt) * p.kb_total + kb0) * kPackedTileBytes;
-    const uint32_t stage_tx = kPackedTileBytes + p.m_sub * kKBlock * 2 + (debug ? 0 : gpk * kTileN * 2);
+    const uint32_t stage_tx =
+        kPackedTileBytes + p.m_sub * kKBlock * 2 + (debug ? 0 : (kZp ? 2 : 1) * gpk * kTileN * 2);
     // Weights and scales are read-only inputs of the call: they are fetched before waiting for the preceding kernel
     // on the stream. x may be that kernel's output, so its tiles are fetched only after pdl_wait().
     auto issue_static = [&](int i, uint64_t stream_policy, uint64_t keep_policy) {
@@ -419,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_arrive_expect_tx(full_p(s), stage_tx);
         bulk_g2s(dst, w_src + static_cast<size_t>(i) * kPackedTileBytes, kPackedTileBytes, full_p(s), stream_policy);
         if (!debug) tma_load_2d(dst + C::kSOff, &tmap_s, nt * kTileN, kb * gpk, full_p(s), keep_policy);
+        if (kZp && !debug) tma_load_2d(dst + C::kZOff, &tmap_z, nt * kTileN, kb * gpk, full_p(s), keep_policy);
     };
     auto issue_x = [&](int i, uint64_t keep_policy) {
         const int s = i % kPStages;
@@ -550,6 +563,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const __half *ss = reinterpret_cast<const __half *>(stage + C::kSOff);
                 for (int gg = 0; gg < gpk; ++gg)
                     cst[kScaleFloatsOffset + gg * kTileN + ct] = __half2float(ss[gg * kTileN + ct]);
+                if constexpr (kZp) {
+                    const __half *zs = reinterpret_cast<const __half *>(stage + C::kZOff);
+                    for (int gg = 0; gg < gpk; ++gg)
+                        cst[kZpFloatsOffset + gg * kTileN + ct] = fmaf(__half2float(zs[gg * kTileN + ct]), 0.125f, 1.0f);
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -566,6 +584,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int n_local = quarter * 32 + lane;
         const int n = nt * kTileN + n_local;
         const int rows_valid = min(p.m_sub, M - m0);
+        const float bias_n = p.bias != nullptr && n < N ? __half2float(p.bias[n]) : 0.0f;
         float yacc[kMaxM];
 #pragma unroll
         for (int m = 0; m < kMaxM; ++m) yacc[m] = 0.0f;
@@ -602,6 +621,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     const int b = j & 1;
                     const int g = gfirst + gg;
                     const float s_n = cst[kScaleFloatsOffset + gg * kTileN + n_local];
+                    const float f_n = kZp ? cst[kZpFloatsOffset + gg * kTileN + n_local] : 1.0f;
                     ok = mbar_wait_warp(full_t(b), (j >> 1) & 1, abort_flag, kSiteEpiTmemFull);
                     if (!ok) break;
                     tc_fence_after_sync();
@@ -643,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                             const float d1 = __uint_as_float(d[m >> 4][m & 15]);
                             const float d2 = __uint_as_float(d[(kMaxM + m) >> 4][(kMaxM + m) & 15]);
                             const float d3 = __uint_as_float(d[(2 * kMaxM + m) >> 4][(2 * kMaxM + m) & 15]);
-                            float t = fmaf(cg[m], d1, -cg[48 + m]);
+                            float t = fmaf(cg[m], d1, kZp ? -cg[48 + m] * f_n : -cg[48 + m]);
                             t = fmaf(cg[16 + m], d2, t);
                             t = fmaf(cg[32 + m], d3, t);
                             yacc[m] = fmaf(s_n, t, yacc[m]);
@@ -661,7 +681,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (p.reduce == kReduceNone) {
 #pragma unroll
                 for (int m = 0; m < kMaxM; ++m)
-                    if (m < rows_valid && n < N) p.y[static_cast<size_t>(m0 + m) * N + n] = __float2half_rn(yacc[m]);
+                    if (m < rows_valid && n < N)
+                        p.y[static_cast<size_t>(m0 + m) * N + n] =
+                            __float2half_rn(p.bias != nullptr ? yacc[m] + bias_n : yacc[m]);
             } else if (p.reduce == kReduceCluster) {
                 // this slice's partial sums go to shared memory (the converted-weight ring is idle by now); the
                 // cluster reduces them after the cluster barrier below
@@ -694,6 +716,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                             for (int q = 0; q < 8; ++q) acc += v[q];
                         }
+                        if (p.bias != nullptr) acc += bias_n;
                         p.y[static_cast<size_t>(m0 + m) * N + n] = __float2half_rn(acc);
                     }
                     if (et == 0) p.ws_count[static_cast<size_t>(mt) * p.n_tiles + nt] = 0u;
@@ -721,6 +744,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 float acc = 0.0f;
 #pragma unroll
                 for (int q = 0; q < kMaxClusterSplits; ++q) acc += v[q];
+                if (p.bias != nullptr) acc += __half2float(p.bias[n]);
                 p.y[static_cast<size_t>(m0 + m) * N + n] = __float2half_rn(acc);
             }
         }

@@ -24,7 +24,7 @@ struct DeviceInfo {
     bool probed = false;
     bool supported = false;
     int sms = 0;
-    bool smem_set[3] = {false, false, false};
+    bool smem_set[6] = {false, false, false, false, false, false};   // small-M kernels: [zero points][NMMA / 16 - 1]
     bool gemm_smem_set = false;
     bool gemv_smem_set = false;
 };
@@ -34,6 +34,12 @@ DeviceInfo g_devices[kMaxDevices];
 
 struct Shape {
     int64_t M, K, N, G;
+};
+
+// Device pointers of one product; zp and bias may be null.
+struct Operands {
+    const void *x, *w, *scale, *zp, *bias;
+    void *y;
 };
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -182,23 +188,25 @@ wqbmm_status current_device(int *dev_out, DeviceInfo **info_out) {
     return WQBMM_OK;
 }
 
-template <int NMMA>
+template <int NMMA, bool kZp>
 wqbmm_status launch_msd(const RunParams &rp, const Plan &plan, DeviceInfo *info, cudaStream_t stream) {
-    constexpr int idx = NMMA / 16 - 1;
-    const int smem = Cfg<NMMA>::kSmemBytes;
+    constexpr int idx = (kZp ? 3 : 0) + NMMA / 16 - 1;
+    const int smem = Cfg<NMMA, kZp>::kSmemBytes;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         if (!info->smem_set[idx]) {
-            if (cudaFuncSetAttribute(msd_kernel<NMMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            if (cudaFuncSetAttribute(msd_kernel<NMMA, kZp>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
                 cudaSuccess)
                 return WQBMM_ERR_CUDA;
             info->smem_set[idx] = true;
         }
     }
-    // x tiles: m_sub rows x 128 k; scale tiles: (128 / G) groups x 128 columns
-    CUtensorMap tmap_x{}, tmap_s{};
+    // x tiles: m_sub rows x 128 k; scale and zero-point tiles: (128 / G) groups x 128 columns
+    CUtensorMap tmap_x{}, tmap_s{}, tmap_z{};
     if (!fp16_tensor_map(&tmap_x, rp.x, rp.M, rp.K, rp.m_sub, kKBlock)) return WQBMM_ERR_CUDA;
     if (rp.dbg_group < 0 && !fp16_tensor_map(&tmap_s, rp.scale, rp.K / rp.G, rp.N, kKBlock / rp.G, kTileN))
+        return WQBMM_ERR_CUDA;
+    if (kZp && rp.dbg_group < 0 && !fp16_tensor_map(&tmap_z, rp.zp, rp.K / rp.G, rp.N, kKBlock / rp.G, kTileN))
         return WQBMM_ERR_CUDA;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(plan.n_tiles, plan.m_tiles, rp.dbg_group >= 0 ? 1 : plan.splits);
@@ -216,51 +224,65 @@ wqbmm_status launch_msd(const RunParams &rp, const Plan &plan, DeviceInfo *info,
     attr[1].val.clusterDim.z = static_cast<unsigned>(plan.splits);
     cfg.attrs = attr;
     cfg.numAttrs = rp.reduce == kReduceCluster ? 2 : 1;
-    if (cudaLaunchKernelEx(&cfg, msd_kernel<NMMA>, rp, tmap_x, tmap_s) != cudaSuccess) return WQBMM_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, msd_kernel<NMMA, kZp>, rp, tmap_x, tmap_s, tmap_z) != cudaSuccess)
+        return WQBMM_ERR_CUDA;
     return WQBMM_OK;
+}
+
+template <bool kZp>
+wqbmm_status launch_small_zp(const RunParams &rp, const Plan &plan, DeviceInfo *info, cudaStream_t stream) {
+    switch (plan.nmma) {
+        case 16: return launch_msd<16, kZp>(rp, plan, info, stream);
+        case 32: return launch_msd<32, kZp>(rp, plan, info, stream);
+        default: return launch_msd<48, kZp>(rp, plan, info, stream);
+    }
 }
 
 wqbmm_status launch_small(const RunParams &rp, const Plan &plan, DeviceInfo *info, cudaStream_t stream) {
     if (plan.m_tiles > 65535 || plan.splits > 65535) return WQBMM_ERR_INVALID;
-    switch (plan.nmma) {
-        case 16: return launch_msd<16>(rp, plan, info, stream);
-        case 32: return launch_msd<32>(rp, plan, info, stream);
-        default: return launch_msd<48>(rp, plan, info, stream);
-    }
+    // debug runs read no zero points (they expose the integer partials of the plain weights)
+    return rp.zp != nullptr && rp.dbg_group < 0 ? launch_small_zp<true>(rp, plan, info, stream)
+                                                : launch_small_zp<false>(rp, plan, info, stream);
 }
 
 // Large-M path: the unfold pre-pass writes plane tiles and constants into the workspace, then the GEMM kernel runs
 // under programmatic launch (it fetches weights and scales while the pre-pass finishes).
-wqbmm_status launch_large(const Shape &s, const Plan &plan, const void *x, const void *w, const void *scale, void *y,
-                          void *workspace, int dbg_group, int32_t *dbg_y123, DeviceInfo *info, cudaStream_t stream) {
+wqbmm_status launch_large(const Shape &s, const Plan &plan, const Operands &op, void *workspace, int dbg_group,
+                          int32_t *dbg_y123, DeviceInfo *info, cudaStream_t stream) {
     if (plan.n_tiles > 65535) return WQBMM_ERR_INVALID;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         if (!info->gemm_smem_set) {
-            if (cudaFuncSetAttribute(msd_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(msd_gemm_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kGemmSmemLimit) != cudaSuccess ||
-                cudaFuncSetAttribute(msd_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                cudaFuncSetAttribute(msd_gemm_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kGemmSmemLimit) != cudaSuccess ||
+                cudaFuncSetAttribute(msd_gemm_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kGemmSmemLimit) != cudaSuccess)
                 return WQBMM_ERR_CUDA;
             info->gemm_smem_set = true;
         }
     }
+    const bool dbg = dbg_group >= 0;
+    const bool zp = op.zp != nullptr && !dbg;
     uint8_t *planes = static_cast<uint8_t *>(workspace);
     float4 *consts = reinterpret_cast<float4 *>(planes + align256(planes_bytes(plan)));
     const dim3 ugrid(static_cast<unsigned>(plan.m_tiles * kGemmTileM / 8), static_cast<unsigned>(plan.kb_total));
-    unfold_planes_kernel<<<ugrid, 256, 0, stream>>>(static_cast<const __half *>(x), static_cast<int>(s.M),
+    unfold_planes_kernel<<<ugrid, 256, 0, stream>>>(static_cast<const __half *>(op.x), static_cast<int>(s.M),
                                                     static_cast<int>(s.K), static_cast<int>(s.G), plan.kb_total,
                                                     planes, consts, dbg_group >= 0 ? 1 : 0);
     if (cudaPeekAtLastError() != cudaSuccess) return WQBMM_ERR_CUDA;
-    CUtensorMap tmap_s{};
-    if (dbg_group < 0 &&
-        !fp16_tensor_map(&tmap_s, scale, s.K / s.G, s.N, static_cast<int>(kKBlock / s.G), kGemmTileN))
+    CUtensorMap tmap_s{}, tmap_z{};
+    if (!dbg && !fp16_tensor_map(&tmap_s, op.scale, s.K / s.G, s.N, static_cast<int>(kKBlock / s.G), kGemmTileN))
+        return WQBMM_ERR_CUDA;
+    if (zp && !fp16_tensor_map(&tmap_z, op.zp, s.K / s.G, s.N, static_cast<int>(kKBlock / s.G), kGemmTileN))
         return WQBMM_ERR_CUDA;
     GemmParams gp{};
-    gp.w = static_cast<const uint8_t *>(w);
+    gp.w = static_cast<const uint8_t *>(op.w);
     gp.planes = planes;
     gp.consts = consts;
-    gp.y = static_cast<__half *>(y);
+    gp.bias = static_cast<const __half *>(op.bias);
+    gp.y = static_cast<__half *>(op.y);
     gp.dbg_y123 = dbg_y123;
     gp.M = static_cast<int>(s.M);
     gp.K = static_cast<int>(s.K);
@@ -270,7 +292,7 @@ wqbmm_status launch_large(const Shape &s, const Plan &plan, const void *x, const
     gp.n_tiles = plan.n_tiles;
     gp.kb_total = plan.kb_total;
     gp.dbg_group = dbg_group;
-    const GemmLayout L(gp.G);
+    const GemmLayout L(gp.G, zp);
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(plan.m_tiles, plan.n_tiles, 1);     // row tiles fastest: concurrent CTAs share weight tiles
     cfg.blockDim = dim3(kGemmThreads, 1, 1);
@@ -281,27 +303,28 @@ wqbmm_status launch_large(const Shape &s, const Plan &plan, const void *x, const
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = dbg_group >= 0 ? cudaLaunchKernelEx(&cfg, msd_gemm_kernel<true>, gp, tmap_s)
-                                         : cudaLaunchKernelEx(&cfg, msd_gemm_kernel<false>, gp, tmap_s);
+    const cudaError_t e = dbg  ? cudaLaunchKernelEx(&cfg, msd_gemm_kernel<true, false>, gp, tmap_s, tmap_z)
+                          : zp ? cudaLaunchKernelEx(&cfg, msd_gemm_kernel<false, true>, gp, tmap_s, tmap_z)
+                               : cudaLaunchKernelEx(&cfg, msd_gemm_kernel<false, false>, gp, tmap_s, tmap_z);
     return e == cudaSuccess ? WQBMM_OK : WQBMM_ERR_CUDA;
 }
 
 // Decode path: the unfold of the one or two rows, then the dp4a matrix-vector kernel, both under programmatic launch
 // (the GEMV kernel streams its weights while the unfold runs).
-wqbmm_status launch_gemv(const Shape &s, const Plan &plan, const void *x, const void *w, const void *scale, void *y,
-                         void *workspace, int dbg_group, int32_t *dbg_y123, DeviceInfo *info, cudaStream_t stream) {
+template <int MR, bool kDebug, bool kZp>
+bool gemv_smem_attr() {
+    return cudaFuncSetAttribute(msd_gemv_kernel<MR, kDebug, kZp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(sizeof(GemvSmem<MR>))) == cudaSuccess;
+}
+
+wqbmm_status launch_gemv(const Shape &s, const Plan &plan, const Operands &op, void *workspace, int dbg_group,
+                         int32_t *dbg_y123, DeviceInfo *info, cudaStream_t stream) {
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         if (!info->gemv_smem_set) {
-            const int s1 = static_cast<int>(sizeof(GemvSmem<1>)), s2 = static_cast<int>(sizeof(GemvSmem<2>));
-            if (cudaFuncSetAttribute(msd_gemv_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, s1) !=
-                    cudaSuccess ||
-                cudaFuncSetAttribute(msd_gemv_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s1) !=
-                    cudaSuccess ||
-                cudaFuncSetAttribute(msd_gemv_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, s2) !=
-                    cudaSuccess ||
-                cudaFuncSetAttribute(msd_gemv_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s2) !=
-                    cudaSuccess)
+            if (!gemv_smem_attr<1, false, false>() || !gemv_smem_attr<1, false, true>() ||
+                !gemv_smem_attr<1, true, false>() || !gemv_smem_attr<2, false, false>() ||
+                !gemv_smem_attr<2, false, true>() || !gemv_smem_attr<2, true, false>())
                 return WQBMM_ERR_CUDA;
             info->gemv_smem_set = true;
         }
@@ -318,16 +341,18 @@ wqbmm_status launch_gemv(const Shape &s, const Plan &plan, const void *x, const 
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, gemv_unfold_kernel, static_cast<const __half *>(x), static_cast<int>(s.M),
+    if (cudaLaunchKernelEx(&cfg, gemv_unfold_kernel, static_cast<const __half *>(op.x), static_cast<int>(s.M),
                            static_cast<int>(s.K), static_cast<int>(s.G), plan.kb_total, planes, consts,
                            dbg_group >= 0 ? 1 : 0) != cudaSuccess)
         return WQBMM_ERR_CUDA;
     GemvParams gp{};
-    gp.w = static_cast<const uint8_t *>(w);
-    gp.scale = static_cast<const __half *>(scale);
+    gp.w = static_cast<const uint8_t *>(op.w);
+    gp.scale = static_cast<const __half *>(op.scale);
+    gp.zp = static_cast<const __half *>(op.zp);
+    gp.bias = static_cast<const __half *>(op.bias);
     gp.planes = planes;
     gp.consts = consts;
-    gp.y = static_cast<__half *>(y);
+    gp.y = static_cast<__half *>(op.y);
     gp.dbg_y123 = dbg_y123;
     gp.M = static_cast<int>(s.M);
     gp.K = static_cast<int>(s.K);
@@ -338,30 +363,36 @@ wqbmm_status launch_gemv(const Shape &s, const Plan &plan, const void *x, const 
     cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(s.N, kGemvCols)), 1, 1);
     cfg.blockDim = dim3(kGemvThreads, 1, 1);
     const bool dbg = dbg_group >= 0;
+    const bool zp = op.zp != nullptr && !dbg;
     auto go = [&](auto kernel, size_t smem) {
         cfg.dynamicSmemBytes = smem;
         return cudaLaunchKernelEx(&cfg, kernel, gp);
     };
     cudaError_t e;
     if (s.M == 1)
-        e = dbg ? go(msd_gemv_kernel<1, true>, sizeof(GemvSmem<1>)) : go(msd_gemv_kernel<1, false>, sizeof(GemvSmem<1>));
+        e = dbg  ? go(msd_gemv_kernel<1, true, false>, sizeof(GemvSmem<1>))
+            : zp ? go(msd_gemv_kernel<1, false, true>, sizeof(GemvSmem<1>))
+                 : go(msd_gemv_kernel<1, false, false>, sizeof(GemvSmem<1>));
     else
-        e = dbg ? go(msd_gemv_kernel<2, true>, sizeof(GemvSmem<2>)) : go(msd_gemv_kernel<2, false>, sizeof(GemvSmem<2>));
+        e = dbg  ? go(msd_gemv_kernel<2, true, false>, sizeof(GemvSmem<2>))
+            : zp ? go(msd_gemv_kernel<2, false, true>, sizeof(GemvSmem<2>))
+                 : go(msd_gemv_kernel<2, false, false>, sizeof(GemvSmem<2>));
     return e == cudaSuccess ? WQBMM_OK : WQBMM_ERR_CUDA;
 }
 
 // Launches one product (or, with dbg_group >= 0, the integer partials of one group) planned by `plan` on the current
 // device. `workspace` holds workspace_for(shape, plan) bytes; `clear_counters` clears the split-K counters first.
-wqbmm_status dispatch(const void *x, const void *w, const void *scale, void *y, const Shape &s, const Plan &plan,
-                      void *workspace, bool clear_counters, int dbg_group, int32_t *dbg_y123, DeviceInfo *info,
-                      cudaStream_t stream) {
-    if (plan.gemv) return launch_gemv(s, plan, x, w, scale, y, workspace, dbg_group, dbg_y123, info, stream);
-    if (plan.large) return launch_large(s, plan, x, w, scale, y, workspace, dbg_group, dbg_y123, info, stream);
+wqbmm_status dispatch(const Operands &op, const Shape &s, const Plan &plan, void *workspace, bool clear_counters,
+                      int dbg_group, int32_t *dbg_y123, DeviceInfo *info, cudaStream_t stream) {
+    if (plan.gemv) return launch_gemv(s, plan, op, workspace, dbg_group, dbg_y123, info, stream);
+    if (plan.large) return launch_large(s, plan, op, workspace, dbg_group, dbg_y123, info, stream);
     RunParams rp{};
-    rp.x = static_cast<const __half *>(x);
-    rp.w = static_cast<const uint8_t *>(w);
-    rp.scale = static_cast<const __half *>(scale);
-    rp.y = static_cast<__half *>(y);
+    rp.x = static_cast<const __half *>(op.x);
+    rp.w = static_cast<const uint8_t *>(op.w);
+    rp.scale = static_cast<const __half *>(op.scale);
+    rp.zp = static_cast<const __half *>(op.zp);
+    rp.bias = static_cast<const __half *>(op.bias);
+    rp.y = static_cast<__half *>(op.y);
     rp.dbg_y123 = dbg_y123;
     if (plan.reduce == kReduceGlobal) {
         const size_t counters_at = align256(static_cast<size_t>(plan.splits) * s.M * s.N * sizeof(float));
@@ -476,11 +507,19 @@ wqbmm_status wqbmm_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t G, s
 wqbmm_status wqbmm_run(const void *x, const void *w_prepacked, const void *antiquant_scale, void *y, int64_t M,
                        int64_t K, int64_t N, int64_t G, void *workspace, size_t workspace_bytes,
                        wqbmm_stream_t stream) {
+    return wqbmm_run_ex(x, w_prepacked, antiquant_scale, nullptr, nullptr, y, M, K, N, G, workspace, workspace_bytes,
+                        stream);
+}
+
+wqbmm_status wqbmm_run_ex(const void *x, const void *w_prepacked, const void *antiquant_scale,
+                          const void *zero_point, const void *bias, void *y, int64_t M, int64_t K, int64_t N,
+                          int64_t G, void *workspace, size_t workspace_bytes, wqbmm_stream_t stream) {
     if (!x || !w_prepacked || !antiquant_scale || !y) return WQBMM_ERR_NULLPTR;
     const Shape s{M, K, N, G};
     wqbmm_status st = check_shape(s);
     if (st != WQBMM_OK) return st;
-    if (!aligned16(x) || !aligned16(w_prepacked) || !aligned16(antiquant_scale) || !aligned16(y))
+    if (!aligned16(x) || !aligned16(w_prepacked) || !aligned16(antiquant_scale) || !aligned16(y) ||
+        !aligned16(zero_point) || !aligned16(bias))
         return WQBMM_ERR_INVALID;
     // the plan for this device never needs more workspace than wqbmm_workspace_bytes reports
     if (workspace_for(s, make_plan(s, kPlanSms)) > 0 && !workspace) return WQBMM_ERR_NULLPTR;
@@ -490,8 +529,8 @@ wqbmm_status wqbmm_run(const void *x, const void *w_prepacked, const void *antiq
     if ((st = current_device(&dev, &info)) != WQBMM_OK) return st;
     const Plan plan = make_plan(s, info->sms < kPlanSms ? info->sms : kPlanSms);
     if (workspace_bytes < workspace_for(s, plan)) return WQBMM_ERR_INVALID;
-    return dispatch(x, w_prepacked, antiquant_scale, y, s, plan, workspace, false, -1, nullptr, info,
-                    reinterpret_cast<cudaStream_t>(stream));
+    const Operands op{x, w_prepacked, antiquant_scale, zero_point, bias, y};
+    return dispatch(op, s, plan, workspace, false, -1, nullptr, info, reinterpret_cast<cudaStream_t>(stream));
 }
 
 wqbmm_status wqbmm_run_static_scratch(const void *x, const void *w_prepacked, const void *antiquant_scale, void *y,
@@ -511,8 +550,8 @@ wqbmm_status wqbmm_run_static_scratch(const void *x, const void *w_prepacked, co
     void *base = nullptr;
     if (need > 0 && (st = static_scratch_address(dev, &base)) != WQBMM_OK) return st;
     // the array keeps whatever the previous call (of any shape) left there: split-K counters are cleared first
-    return dispatch(x, w_prepacked, antiquant_scale, y, s, plan, base, true, -1, nullptr, info,
-                    reinterpret_cast<cudaStream_t>(stream));
+    const Operands op{x, w_prepacked, antiquant_scale, nullptr, nullptr, y};
+    return dispatch(op, s, plan, base, true, -1, nullptr, info, reinterpret_cast<cudaStream_t>(stream));
 }
 
 wqbmm_status wqbmm_debug_unfold(const void *x, int64_t M, int64_t K, int64_t G, int8_t *planes, float *amax,
@@ -554,7 +593,8 @@ wqbmm_status wqbmm_debug_group_partials(const void *x, const void *w_prepacked, 
         plan.splits = 1;
         plan.reduce = kReduceNone;
     }
-    return dispatch(x, w_prepacked, nullptr, nullptr, s, plan, workspace, false, static_cast<int>(g), y123, info,
+    const Operands op{x, w_prepacked, nullptr, nullptr, nullptr, nullptr};
+    return dispatch(op, s, plan, workspace, false, static_cast<int>(g), y123, info,
                     reinterpret_cast<cudaStream_t>(stream));
 }
 

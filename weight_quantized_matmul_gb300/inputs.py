@@ -155,7 +155,7 @@ WORKLOADS = {
 }
 
 # stream ids
-_S_X, _S_W, _S_SCALE, _S_COLS, _S_WSEL, _S_WPM, _S_ROWS = 1, 2, 3, 4, 5, 6, 7
+_S_X, _S_W, _S_SCALE, _S_COLS, _S_WSEL, _S_WPM, _S_ROWS, _S_ZP, _S_BIAS = 1, 2, 3, 4, 5, 6, 7, 8, 9
 
 
 def make_x(wl: Workload, M: Optional[int] = None) -> np.ndarray:
@@ -222,6 +222,24 @@ def make_w_int(wl: Workload) -> np.ndarray:
 def make_scale(wl: Workload) -> np.ndarray:
     n = wl.groups * wl.N
     return fp16(uniform(wl.seed, _S_SCALE, n, wl.scale_lo, wl.scale_hi)).reshape(wl.groups, wl.N)
+
+
+def make_zero_point(wl: Workload, kind: str = "int") -> np.ndarray:
+    """Zero points fp16 [K/G, N] of asymmetric weights (the weight stands for (w - zp) * scale): "int" draws
+    integers in [-4, 4], "frac" uniform reals in [-4, 4] rounded to fp16."""
+    n = wl.groups * wl.N
+    if kind == "int":
+        z = int_uniform(wl.seed, _S_ZP, n, -4, 4).astype(np.float64)
+    elif kind == "frac":
+        z = uniform(wl.seed, _S_ZP, n, -4.0, 4.0)
+    else:
+        raise ValueError(kind)
+    return fp16(z).reshape(wl.groups, wl.N)
+
+
+def make_bias(wl: Workload, lo: float = -1.0, hi: float = 1.0) -> np.ndarray:
+    """Bias fp16 [N], uniform in [lo, hi]."""
+    return fp16(uniform(wl.seed, _S_BIAS, wl.N, lo, hi))
 
 
 def make_inputs(wl: Workload):
