@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
     ap.add_argument("--impl", default="wqbmm", choices=["wqbmm", "reference"])
+    ap.add_argument("--zero-point", default="none", choices=["none", "int", "frac"],
+                    help="asymmetric weights: seeded zero points [K/G, N] (wqbmm_run_ex)")
+    ap.add_argument("--bias", action="store_true", help="add a seeded bias [N] (wqbmm_run_ex)")
     ap.add_argument("--sustain-s", type=float, default=1.5)
     ap.add_argument("--cpu-baseline-s", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -289,11 +292,20 @@ def main():
     ss = [sd] + [sd.clone() for _ in range(copies - 1)]
     ys = [torch.empty((wl.M, wl.N), dtype=torch.float16, device=dev) for _ in range(copies)]
     ws = [wq.allocate_workspace(wl.M, wl.K, wl.N, wl.G, dev) for _ in range(copies)]
+    zs = [None] * copies
+    if args.zero_point != "none":
+        zd = torch.from_numpy(I.make_zero_point(wl, args.zero_point)).to(dev)
+        zs = [zd] + [zd.clone() for _ in range(copies - 1)]
+    bd = torch.from_numpy(I.make_bias(wl)).to(dev) if args.bias else None
+    optionals = args.zero_point != "none" or args.bias
     stream = torch.cuda.Stream(device=dev)
 
     def step(i, s):
         c = i % copies
-        wq.wqbmm_run(xs[c], w_pre[c], ss[c], ys[c], wl.M, wl.K, wl.N, wl.G, ws[c], None, s)
+        if optionals:
+            wq.wqbmm_run_ex(xs[c], w_pre[c], ss[c], zs[c], bd, ys[c], wl.M, wl.K, wl.N, wl.G, ws[c], None, s)
+        else:
+            wq.wqbmm_run(xs[c], w_pre[c], ss[c], ys[c], wl.M, wl.K, wl.N, wl.G, ws[c], None, s)
 
     # ---- warm-up (eager, also sets kernel attributes before any capture)
     with torch.cuda.stream(stream):
@@ -376,22 +388,25 @@ def main():
             torch.distributed.destroy_process_group()
         return
 
-    # M <= 2 and M >= 64 run an unfold pre-pass and then the main kernel; in between one fused kernel
-    launches_per_step = 1 if 2 < wl.M < 64 else 2
+    # every path runs an unfold pre-pass and then the main kernel
+    launches_per_step = 2
     peaks, peak_kind = measured_peaks()
-    alg_bytes = wl.algorithmic_bytes()
+    # the optional inputs add their own bytes: zero points 2 (K/G) N, bias 2 N
+    alg_bytes = (wl.algorithmic_bytes() + (2 * wl.groups * wl.N if args.zero_point != "none" else 0) +
+                 (2 * wl.N if args.bias else 0))
     if wl.M <= 16:
         hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
         achieved = alg_bytes / (ms_step * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                    "frac": achieved / hbm_peak, "traffic": dram_traffic(wl.name), "peak_source": f"{peak_kind} hbm_gbs",
+                    "frac": achieved / hbm_peak, "traffic": None if optionals else dram_traffic(wl.name),
+                    "peak_source": f"{peak_kind} hbm_gbs",
                     "algorithmic_bytes_per_launch": alg_bytes}
     else:
         # E4M3 dense tensor peak = the measured bf16 peak x 2 (the nominal fp8 : bf16 ratio 4.5 : 2.25)
         bf16 = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
         achieved = wl.int8_equiv_ops() / (ms_step * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": 2 * bf16, "unit": "TFLOP/s",
-                    "frac": achieved / (2 * bf16), "traffic": dram_traffic(wl.name),
+                    "frac": achieved / (2 * bf16), "traffic": None if optionals else dram_traffic(wl.name),
                     "peak_source": f"{peak_kind} bf16_tflops x 2 (e4m3)",
                     "algorithmic_flops_per_launch": wl.int8_equiv_ops()}
     line = {
@@ -408,6 +423,7 @@ def main():
         "dtype": "fp16 x / int4 w -> e4m3 tensor-core MMA, f32 accumulate and epilogue",
         "data": "synthetic",
         "config": {"workload": wl.name, "M": wl.M, "K": wl.K, "N": wl.N, "G": wl.G,
+                   "zero_point": args.zero_point, "bias": bool(args.bias),
                    "parallelism": f"replicas{world}" if world > 1 else "single GPU",
                    "l2": f"{copies} rotating input copies ({copies * per_copy / 2**20:.0f} MiB > 2x L2)",
                    "launch": f"CUDA graphs of {chunk} steps"},

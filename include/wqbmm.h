@@ -94,12 +94,13 @@ WQBMM_API wqbmm_status wqbmm_prepack_weight_nk(const uint8_t *w_packed_nk, void 
                                                int64_t G, wqbmm_stream_t stream);
 
 /*
- * Workspace bytes wqbmm_run needs for this shape on any GB300 (0 when the shape needs none). Host only.
- * For M <= 2 the workspace holds the unfolded planes of x as int8 (3 bytes per element, K padded to a multiple of
- * 128) and, per row and group, four floats of combine constants; for 3 <= M < 64 it holds split-K partial sums and
- * per-tile arrival counters (only shapes whose split over K is wider than one thread-block cluster need any); for
- * M >= 64 it holds the unfolded planes of x (3 bytes per element of x, rows padded to a multiple of 128) and the
- * constants.
+ * Workspace bytes wqbmm_run needs for this shape on any GB300. Host only.
+ * Every shape needs one: x is unfolded once per call into it. For M <= 2 it holds the planes of x as int8 (3 bytes
+ * per element, K padded to a multiple of 128) and, per row and group, four floats of combine constants; for
+ * 3 <= M < 64 the planes as the tensor cores' operand image (16, 32 or 48 rows of 128 bytes per row tile of up to 16
+ * rows and per 128 k) and 128 floats of constants per row tile and group, then split-K partial sums and per-tile
+ * arrival counters (only shapes whose split over K is wider than one thread-block cluster need those); for M >= 64
+ * the planes (3 bytes per element of x, rows padded to a multiple of 128) and the constants.
  * It must be zero-filled once before its first use; every successful run leaves the counters at zero again, so the
  * same workspace can be reused by later runs on the same stream without clearing. Runs that execute concurrently must
  * use different workspaces.
@@ -113,7 +114,7 @@ WQBMM_API wqbmm_status wqbmm_workspace_bytes(int64_t M, int64_t K, int64_t N, in
  *   w_prepacked      device, output of wqbmm_prepack_weight for the same K, N, G
  *   antiquant_scale  device, fp16 [K/G, N] row-major
  *   y                device, fp16 [M, N] row-major (written; must not overlap the inputs or the workspace)
- *   workspace        device, at least wqbmm_workspace_bytes(M, K, N, G) bytes (may be null when that is 0)
+ *   workspace        device, at least wqbmm_workspace_bytes(M, K, N, G) bytes
  * The result is deterministic: split-K partial sums are reduced in a fixed order.
  * The kernel is launched with programmatic stream serialization: it may start while the kernel enqueued just before
  * it on `stream` is still finishing, and it reads w_prepacked and antiquant_scale before that kernel has ended (x is
@@ -157,8 +158,8 @@ WQBMM_API wqbmm_status wqbmm_debug_unfold(const void *x, int64_t M, int64_t K, i
  * Exposes step 9 for one group g as the run kernel's tensor-core path computes it (for bit-exact checks): the
  * kernel wqbmm_run would pick for this M, restricted to the k-block that holds group g.
  *   y123       device, int32 [3, M, N]: Y_i[m, n] of group g at y123[(i * M + m) * N + n]
- *   workspace  device, wqbmm_workspace_bytes(M, K, N, G) bytes when M <= 2 or M >= 64 (else ignored, may be null)
- * 0 <= g < K/G. Errors: NULLPTR, INVALID (also a workspace too small for M >= 64), UNSUPPORTED_ARCH, CUDA.
+ *   workspace  device, wqbmm_workspace_bytes(M, K, N, G) bytes
+ * 0 <= g < K/G. Errors: NULLPTR, INVALID (also a workspace too small), UNSUPPORTED_ARCH, CUDA.
  */
 WQBMM_API wqbmm_status wqbmm_debug_group_partials(const void *x, const void *w_prepacked, int64_t M, int64_t K,
                                                   int64_t N, int64_t G, int64_t g, int32_t *y123, void *workspace,

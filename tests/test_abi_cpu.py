@@ -65,18 +65,20 @@ def test_workspace_bytes():
     assert wq.wqbmm_workspace_bytes(1, 4096, 4096, 128) == 3 * 4096 + 16 * 32
     assert wq.wqbmm_workspace_bytes(2, 65536, 256, 128) == 2 * 3 * 65536 + 2 * 16 * 512
     assert wq.wqbmm_workspace_bytes(1, 320, 136, 64) == 1280 + 256     # 3 x 384 and 5 x 16, each in 256-byte blocks
-    # 8 column tiles of 16 rows split over K into 8 slices that reduce inside a thread-block cluster: no workspace
-    assert wq.wqbmm_workspace_bytes(16, 1024, 1024, 128) == 0
+    # 3 <= M < 64: x unfolded once per 128 k into the MMA operand image (three planes of up to 16 rows: 16, 32 or
+    # 48 rows x 128 bytes per k-block) plus 8 x 16 floats of constants per group. 8 column tiles of 16 rows split
+    # over K into 8 slices that reduce inside a thread-block cluster need nothing more
+    assert wq.wqbmm_workspace_bytes(16, 1024, 1024, 128) == 8 * 48 * 128 + 8 * 512
     # two column tiles and a long K: 160 slices (sized for up to 160 SMs, two CTAs each) reduce through the
-    # workspace: 160 x 3 x 256 fp32 partial sums + one 256-byte block of counters
-    assert wq.wqbmm_workspace_bytes(3, 65536, 256, 128) == 160 * 3 * 256 * 4 + 256
+    # workspace: 160 x 3 x 256 fp32 partial sums + one 256-byte block of counters after the unfolded x
+    assert wq.wqbmm_workspace_bytes(3, 65536, 256, 128) == 512 * 16 * 128 + 512 * 512 + 160 * 3 * 256 * 4 + 256
     # M >= 64: x unfolded once into three planes of 128-row tiles (3 bytes per element of x, rows padded to 128)
     # plus 16 bytes of combine constants per padded row and group
     assert wq.wqbmm_workspace_bytes(2048, 8192, 28672, 64) == 3 * 2048 * 8192 + 16 * 2048 * 128
     assert wq.wqbmm_workspace_bytes(128, 5120, 13824, 128) == 3 * 128 * 5120 + 16 * 128 * 40
     assert wq.wqbmm_workspace_bytes(64, 320, 136, 64) == 3 * 128 * 384 + 16 * 128 * 5
-    # 63 rows is still the fused small-M path: enough column tiles, no split, no workspace
-    assert wq.wqbmm_workspace_bytes(63, 4096, 28672, 64) == 0
+    # 63 rows is still the small-M path: four row tiles of 16, enough column tiles, no split
+    assert wq.wqbmm_workspace_bytes(63, 4096, 28672, 64) == 4 * 32 * 48 * 128 + 4 * 64 * 512
 
 
 # (entry, args, expected status) — table-driven error paths
@@ -163,7 +165,7 @@ def test_no_device_is_a_cuda_error(lib):
     if torch.cuda.is_available():
         pytest.skip("a CUDA device is present")
     # valid arguments, but no GPU: the device check fails with a CUDA error and nothing is launched
-    assert lib.wqbmm_run(A, A, A, A, 16, 8192, 28672, 64, None, 0, None) == wq.ERR_CUDA
+    assert lib.wqbmm_run(A, A, A, A, 16, 8192, 28672, 64, A, 1 << 30, None) == wq.ERR_CUDA
     assert lib.wqbmm_run(A, A, A, A, 2048, 8192, 28672, 64, A, 1 << 30, None) == wq.ERR_CUDA
     assert lib.wqbmm_run_ex(A, A, A, A, A, A, 8, 4096, 11008, 128, A, 1 << 30, None) == wq.ERR_CUDA
     assert lib.wqbmm_run_ex(A, A, A, None, None, A, 1, 4096, 4096, 128, A, 1 << 30, None) == wq.ERR_CUDA

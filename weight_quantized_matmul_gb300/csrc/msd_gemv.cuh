@@ -124,8 +124,9 @@ __device__ __forceinline__ float small_int_to_float(int v) {
 }
 
 // One CTA: columns [16 c, 16 c + 16) (rows r0 .. r0 + 15 of weight tile nt), all of K, in passes of at most 64
-// k-blocks. In a pass, warp w takes an eighth of the pass's k-blocks; lane l reads weight rows r0 + l / 4 and
-// r0 + 8 + l / 4, 32 k at (l % 4) * 32. The pass's planes and constants are copied into shared memory in one bulk
+// k-blocks. In a pass, warp w takes an eighth of the pass's k-blocks; lane l reads the adjacent weight rows
+// r0 + 2 (l / 4) and r0 + 2 (l / 4) + 1, 32 k at (l % 4) * 32, so that its two columns' scales (and zero points)
+// come in one 4-byte load. The pass's planes and constants are copied into shared memory in one bulk
 // copy each (the planes of a k-block are read by every warp of every CTA).
 constexpr int kGemvPassKb = kGemvWarps * kGemvKbPerPass;      // 64
 
@@ -160,9 +161,9 @@ __global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvPar
     }
     __syncthreads();
     const uint64_t policy = l2_policy_evict_first();
-    const uint8_t *wbase = p.w + static_cast<size_t>(nt) * kb_total * kPackedTileBytes + (r0 + (lane >> 2)) * 64 +
+    const uint8_t *wbase = p.w + static_cast<size_t>(nt) * kb_total * kPackedTileBytes + (r0 + 2 * (lane >> 2)) * 64 +
                            chunk * 16;
-    const int n_a = col0 + (lane >> 2), n_b = n_a + 8;
+    const int n_a = col0 + 2 * (lane >> 2), n_b = n_a + 1;     // N is even: n_a < N implies n_b < N
     float yacc[MR][2];
 #pragma unroll
     for (int m = 0; m < MR; ++m) yacc[m][0] = yacc[m][1] = 0.0f;
@@ -176,14 +177,14 @@ __global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvPar
         // weights and scales of the warp's k-blocks, all requested before any use (the scales stay fp16 until
         // they are used, so no instruction waits for them here)
         uint4 wa[kGemvKbPerPass], wb[kGemvKbPerPass];
-        __half sa[kGemvKbPerPass], sb[kGemvKbPerPass];
-        __half2 zab[kGemvKbPerPass];                   // zero points of rows a and b (first chunk lane of a group)
+        __half2 sab[kGemvKbPerPass];                   // scales of columns a and b
+        __half2 zab[kGemvKbPerPass];                   // zero points of columns a and b (first chunk lane of a group)
 #pragma unroll
         for (int j = 0; j < kGemvKbPerPass; ++j) {
             if (j < nkb) {
                 const uint8_t *src = wbase + static_cast<size_t>(kw0 + j) * kPackedTileBytes;
                 wa[j] = ldg_stream16(src, policy);
-                wb[j] = ldg_stream16(src + 8 * 64, policy);
+                wb[j] = ldg_stream16(src + 64, policy);
             }
         }
         if (threadIdx.x == 0) {
@@ -205,12 +206,12 @@ __global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvPar
             for (int j = 0; j < kGemvKbPerPass; ++j) {
                 const int g = ((kw0 + j) * kKBlock + chunk * 32) / G;
                 const bool in = j < nkb && g < Gn;
-                sa[j] = in && n_a < N ? __ldg(p.scale + static_cast<size_t>(g) * N + n_a) : __half(0.0f);
-                sb[j] = in && n_b < N ? __ldg(p.scale + static_cast<size_t>(g) * N + n_b) : __half(0.0f);
+                sab[j] = in && n_a < N ? __ldg(reinterpret_cast<const __half2 *>(p.scale + static_cast<size_t>(g) * N + n_a))
+                                       : __half2(0.0f, 0.0f);
                 if constexpr (kZp) {
-                    const bool first = in && (chunk & (lpg_chunks - 1)) == 0;
-                    zab[j] = __halves2half2(first && n_a < N ? __ldg(p.zp + static_cast<size_t>(g) * N + n_a) : __half(0.0f),
-                                            first && n_b < N ? __ldg(p.zp + static_cast<size_t>(g) * N + n_b) : __half(0.0f));
+                    const bool first = in && n_a < N && (chunk & (lpg_chunks - 1)) == 0;
+                    zab[j] = first ? __ldg(reinterpret_cast<const __half2 *>(p.zp + static_cast<size_t>(g) * N + n_a))
+                                   : __half2(0.0f, 0.0f);
                 }
             }
         }
@@ -274,8 +275,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvPar
                     float tb = fmaf(cr.x, small_int_to_float(db[0]), corr_b);
                     tb = fmaf(cr.y, small_int_to_float(db[1]), tb);
                     tb = fmaf(cr.z, small_int_to_float(db[2]), tb);
-                    yacc[m][0] = fmaf(__half2float(sa[j]), ta, yacc[m][0]);
-                    yacc[m][1] = fmaf(__half2float(sb[j]), tb, yacc[m][1]);
+                    yacc[m][0] = fmaf(__low2float(sab[j]), ta, yacc[m][0]);
+                    yacc[m][1] = fmaf(__high2float(sab[j]), tb, yacc[m][1]);
                 }
             }
         }
@@ -297,8 +298,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvPar
         if (chunk == 0) {
 #pragma unroll
             for (int m = 0; m < MR; ++m) {
-                sm.red[warp][m][lane >> 2] = yacc[m][0];
-                sm.red[warp][m][8 + (lane >> 2)] = yacc[m][1];
+                sm.red[warp][m][2 * (lane >> 2)] = yacc[m][0];
+                sm.red[warp][m][2 * (lane >> 2) + 1] = yacc[m][1];
             }
         }
         __syncthreads();

@@ -3,19 +3,22 @@
 // Kernels:
 //   prepack_kernel      packed int4 [K/2, N] -> 128x128 tiles, output-column-major, offset-binary nibbles
 //   unfold_debug_kernel steps 1-8 to global memory (int8 planes, float A_max), same arithmetic as the run kernel
-//   msd_kernel<NMMA>    steps 1-11 fused: per CTA one 128-column tile of y, a tile of rows and a K-slice
+//   unfold_small_kernel steps 1-8 once per (row tile, 128 k): the three planes as E4M3 bytes in the MMA's B operand
+//                       image (NMMA rows x 128 k, 128-byte swizzle), and per (row, group) the combine constants
+//   msd_kernel<NMMA>    steps 9-11: per CTA one 128-column tile of y, a tile of rows and a K-slice
 //   wait_timeout_kernel a bounded wait that nothing completes (exercises the timeout path)
 //
 // The run kernel computes the swapped product D^T = W^T . A_int^T on the 5th-generation tensor core: the MMA's
 // M side is 128 weight columns (so TMEM lane = output column n), its N side is the three stacked residual planes
 // of the row tile (NMMA = 16, 32 or 48 stacked rows), one MMA chain per K-group restarted at every group so the
-// integer partial sums stay exact in FP32. Roles inside a CTA (320 threads):
-//   warp 0      TMA producer: per 128 k, one bulk copy of the packed weight tile (8 KB) plus 2-D tensor copies of
-//               the x tile and the scale tile, into a ring deep enough to hold a decode CTA's whole K-slice
-//   warp 1      TMEM owner and single-thread MMA issuer (tcgen05.mma kind::f8f6f4, E4M3 x E4M3 -> F32)
+// integer partial sums stay exact in FP32. x is unfolded once by the pre-pass, not once per column tile. Roles
+// inside a CTA (320 threads):
+//   warp 0      TMA producer: per 128 k, bulk copies of the packed weight tile (8 KB), of the planes image and of
+//               the constants, and 2-D tensor copies of the scale (and zero-point) tile, into a ring of load stages
+//   warp 1      TMEM owner and single-thread MMA issuer (tcgen05.mma kind::f8f6f4, E4M3 x E4M3 -> F32); the planes
+//               are read in place in the load stage, whose release waits for the MMAs
 //   warps 2-5   operand builders, per k-block: int4 (offset binary) -> E4M3 for half of the weight tile (128-byte-
-//               swizzled K-major layout), then the unfold of the x tile (A_max, three planes as E4M3, per-group
-//               constants, the scale column of each thread), rows rotating over the warps from one k-block to the next
+//               swizzled K-major layout), the combine constants, scales and zero points into an operand slot
 //   warps 6-9   the other half of each weight tile, then the epilogue of the previous k-block: TMEM -> registers,
 //               Y_i = D_i - 8 S_i folded into the combine, scale, accumulate; releasing an operand slot after its
 //               epilogue (which has seen all of that k-block's MMAs complete)
@@ -51,8 +54,6 @@ constexpr int kNumEpiWarps = 4;
 constexpr int kEpiBarrierId = 1;
 constexpr int kMaxGroupsPerKBlock = kKBlock / 32;
 constexpr int kConstFloatsPerGroup = 8 * 16;          // a1 a2 a3 corr S1 S2 S3 (pad) x 16 rows
-constexpr int kScaleFloatsOffset = kMaxGroupsPerKBlock * kConstFloatsPerGroup;   // then scale[group][128 columns]
-constexpr int kZpFloatsOffset = kScaleFloatsOffset + kMaxGroupsPerKBlock * kTileN;  // then 1 + zp / 8 (zero points)
 
 // Method constants (page section 4.1): unfold factors and the combine weights 1/7.49, 1/(7.49*14.98), ...
 constexpr float kF1 = 7.49f;
@@ -73,39 +74,51 @@ enum WaitSite : int {
     kSiteDebugWait = 9,
 };
 
-template <int NMMA, bool kZp>
+template <int NMMA>
 struct Cfg {
     static_assert(NMMA == 16 || NMMA == 32 || NMMA == 48, "MMA N must be 16, 32 or 48");
     static constexpr int kMaxM = NMMA / 3;                         // rows of x per CTA (plane stride in B rows)
     static constexpr int kBufStride = NMMA <= 16 ? 16 : (NMMA <= 32 ? 32 : 64);   // TMEM columns per buffer
     static constexpr int kTmemCols = 2 * kBufStride < 32 ? 32 : 2 * kBufStride;
-    static constexpr int kBTileBytes = NMMA * kKBlock;
-    // one load stage: packed weights, the x tile (rows x 128 k, fp16), the scale tile (groups x 128 n, fp16) and,
-    // with zero points, the zero-point tile (same shape)
-    static constexpr int kXOff = kPackedTileBytes;
-    static constexpr int kSOff = kXOff + kMaxM * kKBlock * 2;
-    static constexpr int kZOff = kSOff + kMaxGroupsPerKBlock * kTileN * 2;
-    static constexpr int kStageBytes = kZOff + (kZp ? kMaxGroupsPerKBlock * kTileN * 2 : 0);
-    // per operand slot: the combine constants, the fp32 scales and (zero points) the factors 1 + zp / 8
-    static constexpr int kConstStageFloats = kZpFloatsOffset + (kZp ? kMaxGroupsPerKBlock * kTileN : 0);
-    // shared memory carve-up (offsets from a 1024-byte aligned base)
+    static constexpr int kBTileBytes = NMMA * kKBlock;             // planes image of one k-block
+    // fixed part of the shared memory (offsets from a 1024-byte aligned base): the converted-weight ring
     static constexpr int kOffA = 0;
-    static constexpr int kOffB = kOffA + kCStages * kATileBytes;
-    static constexpr int kOffConst = kOffB + kCStages * kBTileBytes;
-    static constexpr int kOffP = kOffConst + kCStages * kConstStageFloats * 4;
-    static constexpr int kFixedBytes = kOffP + 1024 + 256;         // + alignment slack, barriers, flags
-    // as many load stages as fit in the budget that keeps two CTAs per SM (at least 3, at most 8)
-    static constexpr int kPStagesFit = (kSmemBudget - kFixedBytes - 16 * 8) / kStageBytes;
-    static constexpr int kPStages = kPStagesFit < 3 ? 3 : (kPStagesFit > 8 ? 8 : kPStagesFit);
-    static constexpr int kOffBar = kOffP + kPStages * kStageBytes;
-    static constexpr int kNumBars = 2 * kPStages + 2 * kCStages + 4;
-    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kSmemBytes = kOffMisc + 64 + 1024;       // + alignment slack
-    static_assert(kStageBytes % 128 == 0, "TMA destinations must stay 128-byte aligned");
+    static constexpr int kOffConst = kOffA + kCStages * kATileBytes;
+};
+
+// The rest of the small-M kernel's shared memory, sized by the groups per k-block (gpk = 128 / G) and by whether
+// zero points are staged:
+//   load stage      packed weights | planes image (NMMA x 128 B, the MMA's B operand, 1024-aligned) |
+//                   constants (gpk x 8 x 16 floats) | scale tile (gpk x 128 n, fp16) [| zero-point tile]
+//   operand slot    per group the combine constants (8 x 16 floats) | fp32 scales (gpk x 128) [| 1 + zp / 8]
+// then as many load stages as fit in the budget that keeps two CTAs per SM (at least 3, at most 8), the barriers
+// and a few flags.
+struct SmallLayout {
+    int gpk, b_off, c_off, s_off, z_off, stage_bytes, scale_floats, zp_floats, slot_floats;
+    int off_p, p_stages, off_bar, off_misc, smem_bytes;
+    __host__ __device__ SmallLayout(int b_tile_bytes, int off_const, int G, bool zp) {
+        gpk = kKBlock / G;
+        b_off = kPackedTileBytes;
+        c_off = b_off + b_tile_bytes;
+        s_off = c_off + gpk * kConstFloatsPerGroup * 4;
+        z_off = s_off + gpk * kTileN * 2;
+        stage_bytes = (z_off + (zp ? gpk * kTileN * 2 : 0) + 1023) / 1024 * 1024;   // swizzled operand 1024-aligned
+        scale_floats = gpk * kConstFloatsPerGroup;
+        zp_floats = scale_floats + gpk * kTileN;
+        slot_floats = zp_floats + (zp ? gpk * kTileN : 0);
+        off_p = (off_const + kCStages * slot_floats * 4 + 1023) / 1024 * 1024;
+        const int fixed = off_p + 1024 + 256;                      // + alignment slack, barriers, flags
+        const int fit = (kSmemBudget - fixed - 16 * 8) / stage_bytes;
+        p_stages = fit < 3 ? 3 : (fit > 8 ? 8 : fit);
+        off_bar = off_p + p_stages * stage_bytes;
+        off_misc = off_bar + (2 * p_stages + 2 * kCStages + 4) * 8;
+        smem_bytes = off_misc + 64 + 1024;                         // + alignment slack
+    }
 };
 
 struct RunParams {
-    const __half *x;
+    const uint8_t *planes;      // [m_tiles][kb_total][NMMA x 128 B] planes images from unfold_small_kernel
+    const float *consts;        // [m_tiles][K/G][8 x 16] combine constants from unfold_small_kernel
     const uint8_t *w;           // prepacked tiles
     const __half *scale;
     const __half *zp;           // [K/G, N] zero points (kernels instantiated with kZp), else null
@@ -303,71 +316,57 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns) {
     }
 }
 
-// Unfold of R (1 or 2) rows of one 128-k block by one warp, interleaved for instruction-level parallelism: planes as
-// E4M3 into the B tile (plane i of row m at row i * kMaxM + m), per-group constants c_i A_max, the offset-binary
-// correction 8 sum_i c_i A_max S_i and the plane sums S_i into the constant slot.
-template <int kMaxM, int R>
-__device__ __forceinline__ void unfold_rows(const __half *xs, uint8_t *bt, float *cst, const int (&rows)[R], int lpg,
-                                            int lane) {
-    const int kbyte = lane * 4;
-    float v[R][4];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const uint2 raw = *reinterpret_cast<const uint2 *>(xs + rows[r] * kKBlock + kbyte);
-        const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
-        const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
-        v[r][0] = f01.x;
-        v[r][1] = f01.y;
-        v[r][2] = f23.x;
-        v[r][3] = f23.y;
-    }
-    float am[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-        am[r] = group_absmax(fmaxf(fmaxf(fabsf(v[r][0]), fabsf(v[r][1])), fmaxf(fabsf(v[r][2]), fabsf(v[r][3]))),
-                             lpg);
-    float a1[R][4], a2[R][4], a3[R][4];
-#pragma unroll
-    for (int r = 0; r < R; ++r) msd_unfold4(v[r], am[r], a1[r], a2[r], a3[r]);
+// Steps 1-8 for the small-M path, once per (row tile, 128-k block): block (kb, mt), one warp per row slot r of the
+// tile (lane: 4 k). Plane i of row r goes to row i * max_m + r of the k-block's B operand image (E4M3, 128-byte
+// swizzle, K-major); row slots past the tile's rows or past M, and the padding rows 3 max_m .. nmma - 1, hold zeros.
+// Per (row, group) the constant record holds 512 c_i A_max (i = 1..3, the MMA unit folded in), the offset-binary
+// correction 8 sum_i c_i A_max S_i and the plane sums S_i (read by debug runs), as [field][row] in 8 x 16 floats.
+__global__ void __launch_bounds__(512) unfold_small_kernel(const __half *__restrict__ x, int M, int K, int G,
+                                                           int kb_total, int m_sub, int nmma,
+                                                           uint8_t *__restrict__ planes, float *__restrict__ consts) {
+    pdl_launch_dependents();
+    pdl_wait();                  // x may be the preceding kernel's output, which may also still read the planes
+    const int lane = threadIdx.x & 31, r = threadIdx.x >> 5;
+    const int kb = blockIdx.x, mt = blockIdx.y;
+    const int max_m = nmma / 3, lpg = G / 4, Gn = K / G;
+    const int m = mt * m_sub + r;
+    const bool live = r < m_sub && m < M;
+    float v[4];
+    load_x4(x, live ? M : 0, K, m, kb * kKBlock + lane * 4, v);     // a dead row slot reads zeros
+    const float am = group_absmax(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))), lpg);
+    float a1[4], a2[4], a3[4];
+    msd_unfold4(v, am, a1, a2, a3);
     // plane sums of a lane (each in [-28, 28]): planes 1 and 2 packed in one word so one reduction serves both
     // (11-bit fields hold lane sums + 28, at most 32 * 56 = 1792 < 2048 over a whole-warp group), plane 3 alone
-    int packed[R], sum3[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int p1 = __float2int_rn((a1[r][0] + a1[r][1]) + (a1[r][2] + a1[r][3])) + 28;
-        const int p2 = __float2int_rn((a2[r][0] + a2[r][1]) + (a2[r][2] + a2[r][3])) + 28;
-        packed[r] = p1 | (p2 << 11);
-        sum3[r] = __float2int_rn((a3[r][0] + a3[r][1]) + (a3[r][2] + a3[r][3]));
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        packed[r] = group_isum(packed[r], lpg);
-        sum3[r] = group_isum(sum3[r], lpg);
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int m = rows[r];
-        *reinterpret_cast<uint32_t *>(bt + sw128_offset(m, kbyte)) =
-            e4m3x2(a1[r][1], a1[r][0]) | (e4m3x2(a1[r][3], a1[r][2]) << 16);
-        *reinterpret_cast<uint32_t *>(bt + sw128_offset(kMaxM + m, kbyte)) =
-            e4m3x2(a2[r][1], a2[r][0]) | (e4m3x2(a2[r][3], a2[r][2]) << 16);
-        *reinterpret_cast<uint32_t *>(bt + sw128_offset(2 * kMaxM + m, kbyte)) =
-            e4m3x2(a3[r][1], a3[r][0]) | (e4m3x2(a3[r][3], a3[r][2]) << 16);
-        if ((lane & (lpg - 1)) == 0) {
-            const int bias = 28 * lpg;
-            const float s1 = static_cast<float>((packed[r] & 0x7FF) - bias);
-            const float s2 = static_cast<float>(((packed[r] >> 11) & 0x7FF) - bias);
-            const float s3 = static_cast<float>(sum3[r]);
-            float *cg = cst + (lane / lpg) * kConstFloatsPerGroup;
-            const float c1 = kC1 * am[r], c2 = kC2 * am[r], c3 = kC3 * am[r];
-            cg[0 * 16 + m] = kMmaUnit * c1;                  // exact: power-of-two scaling
-            cg[1 * 16 + m] = kMmaUnit * c2;
-            cg[2 * 16 + m] = kMmaUnit * c3;
-            cg[3 * 16 + m] = 8.0f * (c1 * s1 + c2 * s2 + c3 * s3);
-            cg[4 * 16 + m] = s1;
-            cg[5 * 16 + m] = s2;
-            cg[6 * 16 + m] = s3;
-        }
+    const int p1 = __float2int_rn((a1[0] + a1[1]) + (a1[2] + a1[3])) + 28;
+    const int p2 = __float2int_rn((a2[0] + a2[1]) + (a2[2] + a2[3])) + 28;
+    const int packed = group_isum(p1 | (p2 << 11), lpg);
+    const int sum3 = group_isum(__float2int_rn((a3[0] + a3[1]) + (a3[2] + a3[3])), lpg);
+    uint8_t *img = planes + (static_cast<size_t>(mt) * kb_total + kb) * nmma * kKBlock;
+    const int kbyte = lane * 4;
+    *reinterpret_cast<uint32_t *>(img + sw128_offset(r, kbyte)) = e4m3x2(a1[1], a1[0]) | (e4m3x2(a1[3], a1[2]) << 16);
+    *reinterpret_cast<uint32_t *>(img + sw128_offset(max_m + r, kbyte)) =
+        e4m3x2(a2[1], a2[0]) | (e4m3x2(a2[3], a2[2]) << 16);
+    *reinterpret_cast<uint32_t *>(img + sw128_offset(2 * max_m + r, kbyte)) =
+        e4m3x2(a3[1], a3[0]) | (e4m3x2(a3[3], a3[2]) << 16);
+    if (r == 0)
+        for (int pr = 3 * max_m; pr < nmma; ++pr) *reinterpret_cast<uint32_t *>(img + sw128_offset(pr, kbyte)) = 0u;
+    const int g = kb * (kKBlock / G) + lane / lpg;
+    if ((lane & (lpg - 1)) == 0 && g < Gn) {
+        const int bias = 28 * lpg;
+        const float s1 = static_cast<float>((packed & 0x7FF) - bias);
+        const float s2 = static_cast<float>(((packed >> 11) & 0x7FF) - bias);
+        const float s3 = static_cast<float>(sum3);
+        const float c1 = kC1 * am, c2 = kC2 * am, c3 = kC3 * am;
+        float *cg = consts + (static_cast<size_t>(mt) * Gn + g) * kConstFloatsPerGroup;
+        cg[0 * 16 + r] = kMmaUnit * c1;                  // exact: power-of-two scaling
+        cg[1 * 16 + r] = kMmaUnit * c2;
+        cg[2 * 16 + r] = kMmaUnit * c3;
+        cg[3 * 16 + r] = 8.0f * (c1 * s1 + c2 * s2 + c3 * s3);
+        cg[4 * 16 + r] = s1;
+        cg[5 * 16 + r] = s2;
+        cg[6 * 16 + r] = s3;
+        cg[7 * 16 + r] = 0.0f;
     }
 }
 
@@ -375,31 +374,30 @@ __device__ __forceinline__ void unfold_rows(const __half *xs, uint8_t *bt, float
 // then need (8 + zp) S_i taken off instead of 8 S_i, that is the correction term times 1 + zp / 8.
 template <int NMMA, bool kZp>
 __global__ void __launch_bounds__(kThreads, 2)
-    msd_kernel(const RunParams p, const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_s,
-               const __grid_constant__ CUtensorMap tmap_z) {
-    using C = Cfg<NMMA, kZp>;
-    constexpr int kConstStageFloats = C::kConstStageFloats;
+    msd_kernel(const RunParams p, const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_z) {
+    using C = Cfg<NMMA>;
     constexpr int kMaxM = C::kMaxM;
-    constexpr int kPStages = C::kPStages;
+    const SmallLayout L(C::kBTileBytes, C::kOffConst, p.G, kZp);
+    const int P = L.p_stages;
+    const int slot_floats = L.slot_floats;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *a_ring = smem + C::kOffA;
-    uint8_t *b_ring = smem + C::kOffB;
-    uint8_t *p_ring = smem + C::kOffP;
+    uint8_t *p_ring = smem + L.off_p;
     float *const_ring = reinterpret_cast<float *>(smem + C::kOffConst);
-    const uint32_t bar0 = smem_addr(smem + C::kOffBar);
-    // barriers: full_p / empty_p  load stage landed / released by the warps that read it
+    const uint32_t bar0 = smem_addr(smem + L.off_bar);
+    // barriers: full_p / empty_p  load stage landed / released by the warps that read it and the MMAs
     //           full_o / sfree    operand slot (A, B, constants) built / released after the k-block's epilogue
     //           full_t / empty_t  TMEM accumulator buffer written by the MMAs / read by the epilogue
     auto full_p = [&](int s) { return bar0 + 8u * s; };
-    auto empty_p = [&](int s) { return bar0 + 8u * (kPStages + s); };
-    auto full_o = [&](int c) { return bar0 + 8u * (2 * kPStages + c); };
-    auto sfree = [&](int c) { return bar0 + 8u * (2 * kPStages + kCStages + c); };
-    auto full_t = [&](int b) { return bar0 + 8u * (2 * kPStages + 2 * kCStages + b); };
-    auto empty_t = [&](int b) { return bar0 + 8u * (2 * kPStages + 2 * kCStages + 2 + b); };
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
-    int *last_flag = reinterpret_cast<int *>(smem + C::kOffMisc + 8);
+    auto empty_p = [&](int s) { return bar0 + 8u * (P + s); };
+    auto full_o = [&](int c) { return bar0 + 8u * (2 * P + c); };
+    auto sfree = [&](int c) { return bar0 + 8u * (2 * P + kCStages + c); };
+    auto full_t = [&](int b) { return bar0 + 8u * (2 * P + 2 * kCStages + b); };
+    auto empty_t = [&](int b) { return bar0 + 8u * (2 * P + 2 * kCStages + 2 + b); };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.off_misc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.off_misc + 4);
+    int *last_flag = reinterpret_cast<int *>(smem + L.off_misc + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nt = blockIdx.x, mt = blockIdx.y, sp = blockIdx.z;
@@ -417,37 +415,44 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     const int nkb = kb1 - kb0;
 
-    // One load stage: the k-block's packed weight tile, x tile, scale tile and zero-point tile, all counted on
-    // full_p(s).
+    // One load stage: the k-block's packed weight tile, planes image, constants, scale tile and zero-point tile, all
+    // counted on full_p(s).
     const uint8_t *w_src = p.w + (static_cast<size_t>(nt) * p.kb_total + kb0) * kPackedTileBytes;
-    const uint32_t stage_tx =
-        kPackedTileBytes + p.m_sub * kKBlock * 2 + (debug ? 0 : (kZp ? 2 : 1) * gpk * kTileN * 2);
-    // Weights and scales are read-only inputs of the call: they are fetched before waiting for the preceding kernel
-    // on the stream. x may be that kernel's output, so its tiles are fetched only after pdl_wait().
-    auto issue_static = [&](int i, uint64_t stream_policy, uint64_t keep_policy) {
-        const int s = i % kPStages;
-        const uint32_t dst = smem_addr(p_ring + s * C::kStageBytes);
-        const int kb = kb0 + i;
-        mbar_arrive_expect_tx(full_p(s), stage_tx);
-        bulk_g2s(dst, w_src + static_cast<size_t>(i) * kPackedTileBytes, kPackedTileBytes, full_p(s), stream_policy);
-        if (!debug) tma_load_2d(dst + C::kSOff, &tmap_s, nt * kTileN, kb * gpk, full_p(s), keep_policy);
-        if (kZp && !debug) tma_load_2d(dst + C::kZOff, &tmap_z, nt * kTileN, kb * gpk, full_p(s), keep_policy);
+    const int Gn = K / G;
+    auto groups_in = [&](int kb) { return (min(K, (kb + 1) * kKBlock) - kb * kKBlock) / G; };
+    auto stage_tx = [&](int kb) {
+        return static_cast<uint32_t>(kPackedTileBytes + C::kBTileBytes + groups_in(kb) * kConstFloatsPerGroup * 4 +
+                                     (debug ? 0 : (kZp ? 2 : 1) * gpk * kTileN * 2));
     };
-    auto issue_x = [&](int i, uint64_t keep_policy) {
-        const int s = i % kPStages;
-        tma_load_2d(smem_addr(p_ring + s * C::kStageBytes) + C::kXOff, &tmap_x, (kb0 + i) * kKBlock, m0, full_p(s),
-                    keep_policy);
+    // Weights and scales are read-only inputs of the call: they are fetched before waiting for the preceding kernel
+    // on the stream. The planes and constants are the unfold pre-pass's output, fetched only after pdl_wait().
+    auto issue_static = [&](int i, uint64_t stream_policy, uint64_t keep_policy) {
+        const int s = i % P;
+        const uint32_t dst = smem_addr(p_ring + s * L.stage_bytes);
+        const int kb = kb0 + i;
+        mbar_arrive_expect_tx(full_p(s), stage_tx(kb));
+        bulk_g2s(dst, w_src + static_cast<size_t>(i) * kPackedTileBytes, kPackedTileBytes, full_p(s), stream_policy);
+        if (!debug) tma_load_2d(dst + L.s_off, &tmap_s, nt * kTileN, kb * gpk, full_p(s), keep_policy);
+        if (kZp && !debug) tma_load_2d(dst + L.z_off, &tmap_z, nt * kTileN, kb * gpk, full_p(s), keep_policy);
+    };
+    auto issue_dynamic = [&](int i, uint64_t keep_policy) {
+        const int s = i % P, kb = kb0 + i;
+        const uint32_t dst = smem_addr(p_ring + s * L.stage_bytes);
+        bulk_g2s(dst + L.b_off, p.planes + (static_cast<size_t>(mt) * p.kb_total + kb) * C::kBTileBytes,
+                 C::kBTileBytes, full_p(s), keep_policy);
+        bulk_g2s(dst + L.c_off, p.consts + (static_cast<size_t>(mt) * Gn + kb * gpk) * kConstFloatsPerGroup,
+                 static_cast<uint32_t>(groups_in(kb) * kConstFloatsPerGroup * 4), full_p(s), keep_policy);
     };
 
     // ---- set-up. Thread 0 lets the next kernel on the stream start launching, initialises the barriers and at once
     // starts the weight loads of the first ring's worth of k-blocks (the slots are free), so the memory latency
     // overlaps the rest of the set-up and, under programmatic launch, the tail of the preceding kernel.
-    const int first_loads = nkb < kPStages ? nkb : kPStages;
+    const int first_loads = nkb < P ? nkb : P;
     uint64_t stream_policy = 0, keep_policy = 0;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kPStages; ++s) {
+        for (int s = 0; s < P; ++s) {
             mbar_init(full_p(s), 1);
-            mbar_init(empty_p(s), kNumConvWarps + kNumEpiWarps);
+            mbar_init(empty_p(s), kNumConvWarps + kNumEpiWarps + 1);     // + the MMAs' commit
         }
         for (int c = 0; c < kCStages; ++c) {
             mbar_init(full_o(c), kNumConvWarps + kNumEpiWarps);
@@ -461,20 +466,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         *last_flag = 0;
         mbar_fence_init();
         stream_policy = l2_policy_evict_first();    // weights: read once per call
-        keep_policy = l2_policy_evict_last();       // x and scale tiles: shared by many CTAs
+        keep_policy = l2_policy_evict_last();       // planes, constants and scale tiles: shared by many CTAs
         pdl_launch_dependents();
         for (int i = 0; i < first_loads; ++i) issue_static(i, stream_policy, keep_policy);
         pdl_wait();
-        for (int i = 0; i < first_loads; ++i) issue_x(i, keep_policy);
+        for (int i = 0; i < first_loads; ++i) issue_dynamic(i, keep_policy);
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
         tmem_relinquish();
         tc_fence_before_sync();
     }
-    for (int i = threadIdx.x; i < kCStages * C::kBTileBytes / 16; i += kThreads)
-        reinterpret_cast<uint4 *>(b_ring)[i] = make_uint4(0, 0, 0, 0);
-    fence_proxy_async_smem();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
@@ -484,14 +486,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0) {
             int issued = first_loads;
             for (; issued < nkb; ++issued) {
-                const int s = issued % kPStages;
-                if (!mbar_wait(empty_p(s), ((issued / kPStages) & 1) ^ 1, abort_flag, kSiteProducerEmpty)) break;
+                const int s = issued % P;
+                if (!mbar_wait(empty_p(s), ((issued / P) & 1) ^ 1, abort_flag, kSiteProducerEmpty)) break;
                 issue_static(issued, stream_policy, keep_policy);
-                issue_x(issued, keep_policy);
+                issue_dynamic(issued, keep_policy);
             }
             // no copy may still be writing shared memory when the CTA exits
-            for (int j = issued > kPStages ? issued - kPStages : 0; j < issued; ++j)
-                mbar_wait_drain(full_p(j % kPStages), (j / kPStages) & 1);
+            for (int j = issued > P ? issued - P : 0; j < issued; ++j)
+                mbar_wait_drain(full_p(j % P), (j / P) & 1);
         }
     } else if (warp == kMmaWarp) {
         // ================================================================ MMA issuer
@@ -499,15 +501,16 @@ __global__ void __launch_bounds__(kThreads, 2)
             constexpr uint32_t idesc = idesc_e4m3_f32(NMMA);
             int j = 0;                       // CTA-local group counter
             int last_j[2] = {-1, -1};
+            int last_i = -1;                 // last k-block whose MMAs release its load stage
             for (int i = 0; i < nkb; ++i) {
-                const int c = i % kCStages;
+                const int c = i % kCStages, s = i % P;
+                // the builders have seen the stage land before building the slot; the planes are read in place
                 if (!mbar_wait(full_o(c), (i / kCStages) & 1, abort_flag, kSiteMmaOperands)) break;
+                if (!mbar_wait(full_p(s), (i / P) & 1, abort_flag, kSiteMmaOperands)) break;
                 tc_fence_after_sync();
-                const int kb = kb0 + i;
-                const int kend = min(K, (kb + 1) * kKBlock);
-                const int ng = (kend - kb * kKBlock) / G;
+                const int ng = groups_in(kb0 + i);
                 const uint32_t a_base = smem_addr(a_ring + c * kATileBytes);
-                const uint32_t b_base = smem_addr(b_ring + c * C::kBTileBytes);
+                const uint32_t b_base = smem_addr(p_ring + s * L.stage_bytes + L.b_off);
                 bool stop = false;
                 for (int gg = 0; gg < ng; ++gg, ++j) {
                     const int b = j & 1;
@@ -526,47 +529,37 @@ __global__ void __launch_bounds__(kThreads, 2)
                     last_j[b] = j;
                 }
                 if (stop) break;
+                umma_commit(empty_p(s));         // the stage (planes image) is free once these MMAs are done
+                last_i = i;
             }
-            // no MMA may still be writing TMEM when it is freed
+            // no MMA may still be writing TMEM when it is freed, nor arrive on a barrier after the CTA exits
             for (int b = 0; b < 2; ++b)
                 if (last_j[b] >= 0) mbar_wait_drain(full_t(b), (last_j[b] >> 1) & 1);
+            if (last_i >= 0) mbar_wait_drain(empty_p(last_i % P), (last_i / P) & 1);
         }
         __syncwarp();
     } else if (warp < kConvWarp0 + kNumConvWarps) {
         // ================================================================ operand builders
-        const int cw = warp - kConvWarp0;               // 0..3
         const int ct = threadIdx.x - kConvWarp0 * 32;   // 0..127: also this thread's column for the scale copy
-        const int lpg = G / 4;                          // lanes per group in the unfold
         for (int i = 0; i < nkb; ++i) {
-            const int s = i % kPStages, c = i % kCStages;
-            if (!mbar_wait_warp(full_p(s), (i / kPStages) & 1, abort_flag, kSiteConvFull)) break;
+            const int s = i % P, c = i % kCStages;
+            if (!mbar_wait_warp(full_p(s), (i / P) & 1, abort_flag, kSiteConvFull)) break;
             if (!mbar_wait_warp(sfree(c), ((i / kCStages) & 1) ^ 1, abort_flag, kSiteConvEmpty)) break;
-            const uint8_t *stage = p_ring + s * C::kStageBytes;
+            const uint8_t *stage = p_ring + s * L.stage_bytes;
             convert_half_tile(stage, a_ring + c * kATileBytes, ct, 0);
-            // unfold of this k-block's x tile; rows m = base, base + 4, ... rotate over the warps
-            const __half *xs = reinterpret_cast<const __half *>(stage + C::kXOff);
-            uint8_t *bt = b_ring + c * C::kBTileBytes;
-            float *cst = const_ring + c * kConstStageFloats;
-            const int base = (cw - i) & 3;
-#pragma unroll
-            for (int pair = 0; pair < (kMaxM + 7) / 8; ++pair) {
-                const int ma = base + 8 * pair, mb = ma + 4;
-                if (mb < p.m_sub) {
-                    const int rows[2] = {ma, mb};
-                    unfold_rows<kMaxM, 2>(xs, bt, cst, rows, lpg, lane);
-                } else if (ma < p.m_sub) {
-                    const int rows[1] = {ma};
-                    unfold_rows<kMaxM, 1>(xs, bt, cst, rows, lpg, lane);
-                }
-            }
+            // the combine constants of the k-block's groups (128 floats each: one per thread) and its scales
+            float *cst = const_ring + c * slot_floats;
+            const float *cs = reinterpret_cast<const float *>(stage + L.c_off);
+            const int ng = groups_in(kb0 + i);
+            for (int gg = 0; gg < ng; ++gg) cst[gg * kConstFloatsPerGroup + ct] = cs[gg * kConstFloatsPerGroup + ct];
             if (!debug) {
-                const __half *ss = reinterpret_cast<const __half *>(stage + C::kSOff);
+                const __half *ss = reinterpret_cast<const __half *>(stage + L.s_off);
                 for (int gg = 0; gg < gpk; ++gg)
-                    cst[kScaleFloatsOffset + gg * kTileN + ct] = __half2float(ss[gg * kTileN + ct]);
+                    cst[L.scale_floats + gg * kTileN + ct] = __half2float(ss[gg * kTileN + ct]);
                 if constexpr (kZp) {
-                    const __half *zs = reinterpret_cast<const __half *>(stage + C::kZOff);
+                    const __half *zs = reinterpret_cast<const __half *>(stage + L.z_off);
                     for (int gg = 0; gg < gpk; ++gg)
-                        cst[kZpFloatsOffset + gg * kTileN + ct] = fmaf(__half2float(zs[gg * kTileN + ct]), 0.125f, 1.0f);
+                        cst[L.zp_floats + gg * kTileN + ct] = fmaf(__half2float(zs[gg * kTileN + ct]), 0.125f, 1.0f);
                 }
             }
             fence_proxy_async_smem();
@@ -594,11 +587,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         int j = 0;
         for (int i = 0; i <= nkb && ok; ++i) {
             if (i < nkb) {
-                const int s = i % kPStages, c = i % kCStages;
-                ok = mbar_wait_warp(full_p(s), (i / kPStages) & 1, abort_flag, kSiteConvFull) &&
+                const int s = i % P, c = i % kCStages;
+                ok = mbar_wait_warp(full_p(s), (i / P) & 1, abort_flag, kSiteConvFull) &&
                      mbar_wait_warp(sfree(c), ((i / kCStages) & 1) ^ 1, abort_flag, kSiteConvEmpty);
                 if (ok) {
-                    convert_half_tile(p_ring + s * C::kStageBytes, a_ring + c * kATileBytes, et, 1);
+                    convert_half_tile(p_ring + s * L.stage_bytes, a_ring + c * kATileBytes, et, 1);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
@@ -616,12 +609,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int kb = kb0 + ie;
                 const int gfirst = kb * gpk;
                 const int ng = (min(K, (kb + 1) * kKBlock) - kb * kKBlock) / G;
-                const float *cst = const_ring + c * kConstStageFloats;
+                const float *cst = const_ring + c * slot_floats;
                 for (int gg = 0; gg < ng && ok; ++gg, ++j) {
                     const int b = j & 1;
                     const int g = gfirst + gg;
-                    const float s_n = cst[kScaleFloatsOffset + gg * kTileN + n_local];
-                    const float f_n = kZp ? cst[kZpFloatsOffset + gg * kTileN + n_local] : 1.0f;
+                    const float s_n = cst[L.scale_floats + gg * kTileN + n_local];
+                    const float f_n = kZp ? cst[L.zp_floats + gg * kTileN + n_local] : 1.0f;
                     ok = mbar_wait_warp(full_t(b), (j >> 1) & 1, abort_flag, kSiteEpiTmemFull);
                     if (!ok) break;
                     tc_fence_after_sync();

@@ -122,11 +122,21 @@ size_t gemv_planes_bytes(const Shape &s, const Plan &p) {
     return static_cast<size_t>(s.M) * p.kb_total * kGemvPlaneBytes;
 }
 
+// Small-M workspace: the planes images [m_tiles][kb][NMMA x 128 B], the constants [m_tiles][K/G][128] (float), then,
+// for a split over K wider than a cluster, the partial sums [splits][M][N] (float) and the arrival counters.
+size_t small_planes_bytes(const Plan &p) {
+    return static_cast<size_t>(p.m_tiles) * p.kb_total * p.nmma * kKBlock;
+}
+size_t small_consts_bytes(const Shape &s, const Plan &p) {
+    return static_cast<size_t>(p.m_tiles) * (s.K / s.G) * kConstFloatsPerGroup * sizeof(float);
+}
+
 size_t workspace_for(const Shape &s, const Plan &p) {
     if (p.gemv) return align256(gemv_planes_bytes(s, p)) + align256(static_cast<size_t>(s.M) * (s.K / s.G) * 16);
     if (p.large) return align256(planes_bytes(p)) + align256(consts_bytes(s, p));
-    if (p.reduce != kReduceGlobal) return 0;
-    return align256(static_cast<size_t>(p.splits) * s.M * s.N * sizeof(float)) +
+    const size_t unfolded = align256(small_planes_bytes(p)) + align256(small_consts_bytes(s, p));
+    if (p.reduce != kReduceGlobal) return unfolded;
+    return unfolded + align256(static_cast<size_t>(p.splits) * s.M * s.N * sizeof(float)) +
            align256(static_cast<size_t>(p.m_tiles) * p.n_tiles * sizeof(uint32_t));
 }
 
@@ -191,19 +201,25 @@ wqbmm_status current_device(int *dev_out, DeviceInfo **info_out) {
 template <int NMMA, bool kZp>
 wqbmm_status launch_msd(const RunParams &rp, const Plan &plan, DeviceInfo *info, cudaStream_t stream) {
     constexpr int idx = (kZp ? 3 : 0) + NMMA / 16 - 1;
-    const int smem = Cfg<NMMA, kZp>::kSmemBytes;
+    using C = Cfg<NMMA>;
+    const int smem = SmallLayout(C::kBTileBytes, C::kOffConst, rp.G, kZp).smem_bytes;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         if (!info->smem_set[idx]) {
-            if (cudaFuncSetAttribute(msd_kernel<NMMA, kZp>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            // the limit covers every group size (G = 32 has the largest layout)
+            int most = 0;
+            for (int g : {32, 64, 128}) {
+                const int b = SmallLayout(C::kBTileBytes, C::kOffConst, g, kZp).smem_bytes;
+                most = b > most ? b : most;
+            }
+            if (cudaFuncSetAttribute(msd_kernel<NMMA, kZp>, cudaFuncAttributeMaxDynamicSharedMemorySize, most) !=
                 cudaSuccess)
                 return WQBMM_ERR_CUDA;
             info->smem_set[idx] = true;
         }
     }
-    // x tiles: m_sub rows x 128 k; scale and zero-point tiles: (128 / G) groups x 128 columns
-    CUtensorMap tmap_x{}, tmap_s{}, tmap_z{};
-    if (!fp16_tensor_map(&tmap_x, rp.x, rp.M, rp.K, rp.m_sub, kKBlock)) return WQBMM_ERR_CUDA;
+    // scale and zero-point tiles: (128 / G) groups x 128 columns
+    CUtensorMap tmap_s{}, tmap_z{};
     if (rp.dbg_group < 0 && !fp16_tensor_map(&tmap_s, rp.scale, rp.K / rp.G, rp.N, kKBlock / rp.G, kTileN))
         return WQBMM_ERR_CUDA;
     if (kZp && rp.dbg_group < 0 && !fp16_tensor_map(&tmap_z, rp.zp, rp.K / rp.G, rp.N, kKBlock / rp.G, kTileN))
@@ -213,8 +229,8 @@ wqbmm_status launch_msd(const RunParams &rp, const Plan &plan, DeviceInfo *info,
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    // programmatic launch: this kernel may start while the preceding kernel on the stream finishes; it fetches only
-    // weights and scales before griddepcontrol.wait (see msd_kernel)
+    // programmatic launch: this kernel may start while the unfold pre-pass finishes; it fetches only weights and
+    // scales before griddepcontrol.wait (see msd_kernel)
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -224,7 +240,7 @@ wqbmm_status launch_msd(const RunParams &rp, const Plan &plan, DeviceInfo *info,
     attr[1].val.clusterDim.z = static_cast<unsigned>(plan.splits);
     cfg.attrs = attr;
     cfg.numAttrs = rp.reduce == kReduceCluster ? 2 : 1;
-    if (cudaLaunchKernelEx(&cfg, msd_kernel<NMMA, kZp>, rp, tmap_x, tmap_s, tmap_z) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, msd_kernel<NMMA, kZp>, rp, tmap_s, tmap_z) != cudaSuccess)
         return WQBMM_ERR_CUDA;
     return WQBMM_OK;
 }
@@ -238,8 +254,24 @@ wqbmm_status launch_small_zp(const RunParams &rp, const Plan &plan, DeviceInfo *
     }
 }
 
-wqbmm_status launch_small(const RunParams &rp, const Plan &plan, DeviceInfo *info, cudaStream_t stream) {
+// Small-M path: the unfold pre-pass writes the planes images and constants into the workspace, then the tensor-core
+// kernel runs under programmatic launch.
+wqbmm_status launch_small(const void *x, const RunParams &rp, const Plan &plan, DeviceInfo *info,
+                          cudaStream_t stream) {
     if (plan.m_tiles > 65535 || plan.splits > 65535) return WQBMM_ERR_INVALID;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(plan.kb_total), static_cast<unsigned>(plan.m_tiles), 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(32 * (plan.nmma / 3)), 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, unfold_small_kernel, static_cast<const __half *>(x), rp.M, rp.K, rp.G, plan.kb_total,
+                           plan.m_sub, plan.nmma, const_cast<uint8_t *>(rp.planes),
+                           const_cast<float *>(rp.consts)) != cudaSuccess)
+        return WQBMM_ERR_CUDA;
     // debug runs read no zero points (they expose the integer partials of the plain weights)
     return rp.zp != nullptr && rp.dbg_group < 0 ? launch_small_zp<true>(rp, plan, info, stream)
                                                 : launch_small_zp<false>(rp, plan, info, stream);
@@ -387,7 +419,8 @@ wqbmm_status dispatch(const Operands &op, const Shape &s, const Plan &plan, void
     if (plan.gemv) return launch_gemv(s, plan, op, workspace, dbg_group, dbg_y123, info, stream);
     if (plan.large) return launch_large(s, plan, op, workspace, dbg_group, dbg_y123, info, stream);
     RunParams rp{};
-    rp.x = static_cast<const __half *>(op.x);
+    rp.planes = static_cast<const uint8_t *>(workspace);
+    rp.consts = reinterpret_cast<const float *>(static_cast<uint8_t *>(workspace) + align256(small_planes_bytes(plan)));
     rp.w = static_cast<const uint8_t *>(op.w);
     rp.scale = static_cast<const __half *>(op.scale);
     rp.zp = static_cast<const __half *>(op.zp);
@@ -395,9 +428,11 @@ wqbmm_status dispatch(const Operands &op, const Shape &s, const Plan &plan, void
     rp.y = static_cast<__half *>(op.y);
     rp.dbg_y123 = dbg_y123;
     if (plan.reduce == kReduceGlobal) {
+        uint8_t *part = static_cast<uint8_t *>(workspace) + align256(small_planes_bytes(plan)) +
+                        align256(small_consts_bytes(s, plan));
         const size_t counters_at = align256(static_cast<size_t>(plan.splits) * s.M * s.N * sizeof(float));
-        rp.ws_part = static_cast<float *>(workspace);
-        rp.ws_count = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) + counters_at);
+        rp.ws_part = reinterpret_cast<float *>(part);
+        rp.ws_count = reinterpret_cast<uint32_t *>(part + counters_at);
         if (clear_counters &&
             cudaMemsetAsync(rp.ws_count, 0, static_cast<size_t>(plan.m_tiles) * plan.n_tiles * sizeof(uint32_t),
                             stream) != cudaSuccess)
@@ -414,7 +449,7 @@ wqbmm_status dispatch(const Operands &op, const Shape &s, const Plan &plan, void
     rp.kb_total = plan.kb_total;
     rp.reduce = plan.reduce;
     rp.dbg_group = dbg_group;
-    return launch_small(rp, plan, info, stream);
+    return launch_small(op.x, rp, plan, info, stream);
 }
 
 // Scratch for wqbmm_run_static_scratch: a fixed device array instead of a caller workspace. Host code must not
@@ -581,10 +616,10 @@ wqbmm_status wqbmm_debug_group_partials(const void *x, const void *w_prepacked, 
     if (g < 0 || g >= K / G) return WQBMM_ERR_INVALID;
     if (!aligned16(x) || !aligned16(w_prepacked)) return WQBMM_ERR_INVALID;
     if (workspace && !aligned16(workspace)) return WQBMM_ERR_INVALID;
-    if (M >= kLargeM || M <= kGemvMaxM) {               // these plans do not depend on the SM count
-        if (!workspace) return WQBMM_ERR_NULLPTR;
-        if (workspace_bytes < workspace_for(s, make_plan(s, kPlanSms))) return WQBMM_ERR_INVALID;
-    }
+    if (!workspace) return WQBMM_ERR_NULLPTR;            // every path unfolds x into the workspace
+    if ((M >= kLargeM || M <= kGemvMaxM) &&              // these plans do not depend on the SM count
+        workspace_bytes < workspace_for(s, make_plan(s, kPlanSms)))
+        return WQBMM_ERR_INVALID;
     int dev;
     DeviceInfo *info;
     if ((st = current_device(&dev, &info)) != WQBMM_OK) return st;
@@ -593,6 +628,7 @@ wqbmm_status wqbmm_debug_group_partials(const void *x, const void *w_prepacked, 
         plan.splits = 1;
         plan.reduce = kReduceNone;
     }
+    if (workspace_bytes < workspace_for(s, plan)) return WQBMM_ERR_INVALID;
     const Operands op{x, w_prepacked, nullptr, nullptr, nullptr, nullptr};
     return dispatch(op, s, plan, workspace, false, static_cast<int>(g), y123, info,
                     reinterpret_cast<cudaStream_t>(stream));
