@@ -65,13 +65,14 @@ def test_workspace_bytes():
     assert wq.wqbmm_workspace_bytes(1, 4096, 4096, 128) == 3 * 4096 + 16 * 32
     assert wq.wqbmm_workspace_bytes(2, 65536, 256, 128) == 2 * 3 * 65536 + 2 * 16 * 512
     assert wq.wqbmm_workspace_bytes(1, 320, 136, 64) == 1280 + 256     # 3 x 384 and 5 x 16, each in 256-byte blocks
-    # 3 <= M < 64: x unfolded once per 128 k into the MMA operand image (three planes of up to 16 rows: 16, 32 or
-    # 48 rows x 128 bytes per k-block) plus 8 x 16 floats of constants per group. 8 column tiles of 16 rows split
-    # over K into 8 slices that reduce inside a thread-block cluster need nothing more
+    # 3 <= M < 64: x unfolded once per 128 k into the tensor-core operand image (three planes of up to 16 rows:
+    # 16, 32 or 48 rows x 128 bytes per row tile and k-block) plus 8 x 16 floats of constants per group. 8 column
+    # tiles of 16 rows split over K into 8 slices that reduce inside a thread-block cluster need nothing more
     assert wq.wqbmm_workspace_bytes(16, 1024, 1024, 128) == 8 * 48 * 128 + 8 * 512
     # two column tiles and a long K: 160 slices (sized for up to 160 SMs, two CTAs each) reduce through the
     # workspace: 160 x 3 x 256 fp32 partial sums + one 256-byte block of counters after the unfolded x
     assert wq.wqbmm_workspace_bytes(3, 65536, 256, 128) == 512 * 16 * 128 + 512 * 512 + 160 * 3 * 256 * 4 + 256
+    assert wq.wqbmm_workspace_bytes(40, 1024, 28672, 128) == 3 * 8 * 48 * 128 + 3 * 8 * 512
     # M >= 64: x unfolded once into three planes of 128-row tiles (3 bytes per element of x, rows padded to 128)
     # plus 16 bytes of combine constants per padded row and group
     assert wq.wqbmm_workspace_bytes(2048, 8192, 28672, 64) == 3 * 2048 * 8192 + 16 * 2048 * 128

@@ -90,14 +90,6 @@ struct GemvParams {
     int M, K, N, G, kb_total, dbg_group;
 };
 
-__device__ __forceinline__ uint4 ldg_stream16(const void *p, uint64_t policy) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p), "l"(policy));
-    return v;
-}
-
 __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
     int d;
     asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));

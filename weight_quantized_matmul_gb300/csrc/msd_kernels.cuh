@@ -42,18 +42,19 @@ constexpr int kTileN = 128;                          // output columns per CTA (
 constexpr int kKBlock = 128;                         // k per pipeline stage (one 128-byte E4M3 swizzle row)
 constexpr int kPackedTileBytes = kTileN * kKBlock / 2;  // 8192
 constexpr int kATileBytes = kTileN * kKBlock;        // 16384
-constexpr int kCStages = 3;                          // converted weights / planes / constants ring
+constexpr int kASlots = 2;                           // converted weight tiles in flight
+constexpr int kMaxTmemBufs = 8;                      // TMEM accumulators (one per K-group) in flight, at most
 constexpr int kSmemBudget = 110 * 1024;              // per CTA, so that two CTAs share an SM
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
-constexpr int kConvWarp0 = 2;
-constexpr int kNumConvWarps = 4;
-constexpr int kEpiWarp0 = 6;
-constexpr int kNumEpiWarps = 4;
-constexpr int kEpiBarrierId = 1;
-constexpr int kMaxGroupsPerKBlock = kKBlock / 32;
-constexpr int kConstFloatsPerGroup = 8 * 16;          // a1 a2 a3 corr S1 S2 S3 (pad) x 16 rows
+constexpr int kWorkWarp0 = 2;
+constexpr int kNumWorkWarps = 8;
+constexpr int kWorkThreads = kNumWorkWarps * 32;
+constexpr int kWorkBarrierId = 1;
+constexpr int kOperandBarrier0 = 2;                  // named barriers 2, 3: converted weight slot 0, 1 ready
+constexpr int kOperandThreads = kWorkThreads + 32;   // the workers and the MMA warp
+constexpr int kConstFloatsPerGroup = 16 * 8;          // 16 rows x {c1 c2 c3 corr, S1 S2 S3 0}
 
 // Method constants (page section 4.1): unfold factors and the combine weights 1/7.49, 1/(7.49*14.98), ...
 constexpr float kF1 = 7.49f;
@@ -78,40 +79,35 @@ template <int NMMA>
 struct Cfg {
     static_assert(NMMA == 16 || NMMA == 32 || NMMA == 48, "MMA N must be 16, 32 or 48");
     static constexpr int kMaxM = NMMA / 3;                         // rows of x per CTA (plane stride in B rows)
+    static constexpr int kRowsPerWarp = (kMaxM + 1) / 2;           // two worker warps share a TMEM lane quarter
     static constexpr int kBufStride = NMMA <= 16 ? 16 : (NMMA <= 32 ? 32 : 64);   // TMEM columns per buffer
-    static constexpr int kTmemCols = 2 * kBufStride < 32 ? 32 : 2 * kBufStride;
+    // eight buffers hold two k-blocks of the smallest groups; NMMA = 48 keeps four, so that two CTAs fit in TMEM
+    static constexpr int kTmemBufs = NMMA <= 32 ? 8 : 4;
+    static constexpr int kTmemCols = kTmemBufs * kBufStride;
     static constexpr int kBTileBytes = NMMA * kKBlock;             // planes image of one k-block
-    // fixed part of the shared memory (offsets from a 1024-byte aligned base): the converted-weight ring
+    // fixed part of the shared memory (offsets from a 1024-byte aligned base): the converted-weight slots
     static constexpr int kOffA = 0;
-    static constexpr int kOffConst = kOffA + kCStages * kATileBytes;
+    static constexpr int kOffStages = kOffA + kASlots * kATileBytes;
 };
 
-// The rest of the small-M kernel's shared memory, sized by the groups per k-block (gpk = 128 / G) and by whether
-// zero points are staged:
-//   load stage      packed weights | planes image (NMMA x 128 B, the MMA's B operand, 1024-aligned) |
-//                   constants (gpk x 8 x 16 floats) | scale tile (gpk x 128 n, fp16) [| zero-point tile]
-//   operand slot    per group the combine constants (8 x 16 floats) | fp32 scales (gpk x 128) [| 1 + zp / 8]
-// then as many load stages as fit in the budget that keeps two CTAs per SM (at least 3, at most 8), the barriers
-// and a few flags.
+// The load stages of the small-M kernel, sized by the groups per k-block (gpk = 128 / G) and by whether zero points
+// are staged: packed weights | planes image (NMMA x 128 B, the MMA's B operand, 1024-aligned) | constants (gpk x 16
+// rows x 8 floats) | scale tile (gpk x 128 n, fp16) [| zero-point tile]. As many stages as fit in the budget that
+// keeps two CTAs per SM (at least 3, at most 8), then the barriers and a few flags.
 struct SmallLayout {
-    int gpk, b_off, c_off, s_off, z_off, stage_bytes, scale_floats, zp_floats, slot_floats;
-    int off_p, p_stages, off_bar, off_misc, smem_bytes;
-    __host__ __device__ SmallLayout(int b_tile_bytes, int off_const, int G, bool zp) {
+    int gpk, b_off, c_off, s_off, z_off, stage_bytes, p_stages, off_bar, off_misc, smem_bytes;
+    __host__ __device__ SmallLayout(int b_tile_bytes, int off_stages, int G, bool zp) {
         gpk = kKBlock / G;
         b_off = kPackedTileBytes;
         c_off = b_off + b_tile_bytes;
         s_off = c_off + gpk * kConstFloatsPerGroup * 4;
         z_off = s_off + gpk * kTileN * 2;
         stage_bytes = (z_off + (zp ? gpk * kTileN * 2 : 0) + 1023) / 1024 * 1024;   // swizzled operand 1024-aligned
-        scale_floats = gpk * kConstFloatsPerGroup;
-        zp_floats = scale_floats + gpk * kTileN;
-        slot_floats = zp_floats + (zp ? gpk * kTileN : 0);
-        off_p = (off_const + kCStages * slot_floats * 4 + 1023) / 1024 * 1024;
-        const int fixed = off_p + 1024 + 256;                      // + alignment slack, barriers, flags
+        const int fixed = off_stages + 1024 + 256;                 // + alignment slack, barriers, flags
         const int fit = (kSmemBudget - fixed - 16 * 8) / stage_bytes;
         p_stages = fit < 3 ? 3 : (fit > 8 ? 8 : fit);
-        off_bar = off_p + p_stages * stage_bytes;
-        off_misc = off_bar + (2 * p_stages + 2 * kCStages + 4) * 8;
+        off_bar = off_stages + p_stages * stage_bytes;
+        off_misc = off_bar + (2 * p_stages + 2 * kMaxTmemBufs) * 8;
         smem_bytes = off_misc + 64 + 1024;                         // + alignment slack
     }
 };
@@ -213,15 +209,20 @@ __device__ __forceinline__ uint4 expand_nibbles16(uint2 v) {
     return make_uint4(v.x & 0x0F0F0F0Fu, (v.x >> 4) & 0x0F0F0F0Fu, v.y & 0x0F0F0F0Fu, (v.y >> 4) & 0x0F0F0F0Fu);
 }
 
-// Weight bytes for the chunks q = t, t + 128, ... (4 of them) of one half of a packed 128 x 128 weight tile: chunk
-// q is 16 k of weight row q / 8, written to its place in the 128-byte-swizzled K-major operand tile.
-__device__ __forceinline__ void convert_half_tile(const uint8_t *src, uint8_t *dst, int t, int half) {
+// Weight bytes of one packed 128 x 128 tile by 256 threads: thread t takes the 16-byte pieces t and t + 256 (32 k of
+// weight row piece / 4 each) and writes their 32 E4M3 bytes as two 16-byte chunks of the 128-byte-swizzled K-major
+// operand tile. Both pieces are read before anything is written.
+__device__ __forceinline__ void convert_tile256(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int t) {
+    uint4 v[2];
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const int q = t + (half * 4 + it) * 128;
-        const int row = q >> 3, ch = q & 7;
-        const uint4 o = expand_nibbles16(*reinterpret_cast<const uint2 *>(src + q * 8));
-        *reinterpret_cast<uint4 *>(dst + (row >> 3) * 1024 + (row & 7) * 128 + ((ch ^ (row & 7)) << 4)) = o;
+    for (int j = 0; j < 2; ++j) v[j] = *reinterpret_cast<const uint4 *>(src + (t + 256 * j) * 16);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int piece = t + 256 * j, row = piece >> 2, ch = (piece & 3) * 2;
+        uint8_t *base = dst + (row >> 3) * 1024 + (row & 7) * 128;
+        *reinterpret_cast<uint4 *>(base + ((ch ^ (row & 7)) << 4)) = expand_nibbles16(make_uint2(v[j].x, v[j].y));
+        *reinterpret_cast<uint4 *>(base + (((ch + 1) ^ (row & 7)) << 4)) =
+            expand_nibbles16(make_uint2(v[j].z, v[j].w));
     }
 }
 
@@ -320,7 +321,7 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns) {
 // tile (lane: 4 k). Plane i of row r goes to row i * max_m + r of the k-block's B operand image (E4M3, 128-byte
 // swizzle, K-major); row slots past the tile's rows or past M, and the padding rows 3 max_m .. nmma - 1, hold zeros.
 // Per (row, group) the constant record holds 512 c_i A_max (i = 1..3, the MMA unit folded in), the offset-binary
-// correction 8 sum_i c_i A_max S_i and the plane sums S_i (read by debug runs), as [field][row] in 8 x 16 floats.
+// correction 8 sum_i c_i A_max S_i, then the plane sums S_i (read by debug runs) and a zero: [row][8] per group.
 __global__ void __launch_bounds__(512) unfold_small_kernel(const __half *__restrict__ x, int M, int K, int G,
                                                            int kb_total, int m_sub, int nmma,
                                                            uint8_t *__restrict__ planes, float *__restrict__ consts) {
@@ -358,43 +359,91 @@ __global__ void __launch_bounds__(512) unfold_small_kernel(const __half *__restr
         const float s2 = static_cast<float>(((packed >> 11) & 0x7FF) - bias);
         const float s3 = static_cast<float>(sum3);
         const float c1 = kC1 * am, c2 = kC2 * am, c3 = kC3 * am;
-        float *cg = consts + (static_cast<size_t>(mt) * Gn + g) * kConstFloatsPerGroup;
-        cg[0 * 16 + r] = kMmaUnit * c1;                  // exact: power-of-two scaling
-        cg[1 * 16 + r] = kMmaUnit * c2;
-        cg[2 * 16 + r] = kMmaUnit * c3;
-        cg[3 * 16 + r] = 8.0f * (c1 * s1 + c2 * s2 + c3 * s3);
-        cg[4 * 16 + r] = s1;
-        cg[5 * 16 + r] = s2;
-        cg[6 * 16 + r] = s3;
-        cg[7 * 16 + r] = 0.0f;
+        float4 *cg = reinterpret_cast<float4 *>(consts + (static_cast<size_t>(mt) * Gn + g) * kConstFloatsPerGroup) +
+                     2 * r;
+        cg[0] = make_float4(kMmaUnit * c1, kMmaUnit * c2, kMmaUnit * c3,      // exact: power-of-two scaling
+                            8.0f * (c1 * s1 + c2 * s2 + c3 * s3));
+        cg[1] = make_float4(s1, s2, s3, 0.0f);
+    }
+}
+
+// Steps 10-11 for rows H * R .. H * R + R - 1 of the tile (compile-time, so the accumulator registers are indexed
+// statically) from one K-group's TMEM columns d (column i * kMaxM + m holds 2^-9 sum_k A_i[m, k] u[k, n]):
+// y[m] += s_n (sum_i (512 c_i A_max) d_i - corr f_n), with corr = 8 sum_i c_i A_max S_i and f_n = 1 + zp / 8.
+template <int kMaxM, int R, int H, bool kZp>
+__device__ __forceinline__ void combine_rows(const uint32_t (&d)[3][16], const float4 *cg, float s_n, float f_n,
+                                             int rows_valid, float (&yacc)[R]) {
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {
+        const int m = H * R + rr;
+        if (m < kMaxM && m < rows_valid) {
+            const float4 c = cg[2 * m];
+            const float d1 = __uint_as_float(d[m >> 4][m & 15]);
+            const float d2 = __uint_as_float(d[(kMaxM + m) >> 4][(kMaxM + m) & 15]);
+            const float d3 = __uint_as_float(d[(2 * kMaxM + m) >> 4][(2 * kMaxM + m) & 15]);
+            float t = fmaf(c.x, d1, kZp ? -c.w * f_n : -c.w);
+            t = fmaf(c.y, d2, t);
+            t = fmaf(c.z, d3, t);
+            yacc[rr] = fmaf(s_n, t, yacc[rr]);
+        }
+    }
+}
+
+// Debug: the integer partials Y_i = 512 d_i - 8 S_i of the same rows for group dbg_group.
+template <int kMaxM, int R, int H>
+__device__ __forceinline__ void debug_rows(const uint32_t (&d)[3][16], const float4 *cg, int rows_valid, int32_t *dbg,
+                                           int M, int N, int m0, int n) {
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {
+        const int m = H * R + rr;
+        if (m < kMaxM && m < rows_valid) {
+            const float4 sv = cg[2 * m + 1];
+            const float sp[3] = {sv.x, sv.y, sv.z};
+#pragma unroll
+            for (int pl = 0; pl < 3; ++pl) {
+                const int col = pl * kMaxM + m;
+                const float yi = kMmaUnit * __uint_as_float(d[col >> 4][col & 15]) - 8.0f * sp[pl];
+                dbg[(static_cast<size_t>(pl) * M + m0 + m) * N + n] = __float2int_rn(yi);
+            }
+        }
     }
 }
 
 // kZp: the weights carry zero points, w - zp[g, n] being the quantized value the scale multiplies. The plane dots
 // then need (8 + zp) S_i taken off instead of 8 S_i, that is the correction term times 1 + zp / 8.
+// Roles: warp 0 lane 0 issues the loads, warp 1 lane 0 the MMAs; warps 2-9 (the workers) convert each k-block's
+// weight tile together, then run the previous k-block's epilogue: two warps per TMEM lane quarter (32 output
+// columns), each taking half of the rows, reading the constants and scales in place in the load stage. The workers
+// hand a converted tile to the MMA warp through a hardware named barrier. The MMA-issuing thread makes no ordinary
+// shared-memory access between its MMAs (such an access waits for its MMAs in flight to finish reading their
+// operands): it never checks the abort flag, and with enough TMEM buffers it never waits for one to be free. So
+// after a failed wait the workers skip their work but keep every synchronisation (arrivals on the named barrier,
+// waits for the MMAs' commits), and the MMA warp keeps issuing, and nothing can wait forever.
 template <int NMMA, bool kZp>
 __global__ void __launch_bounds__(kThreads, 2)
     msd_kernel(const RunParams p, const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_z) {
     using C = Cfg<NMMA>;
     constexpr int kMaxM = C::kMaxM;
-    const SmallLayout L(C::kBTileBytes, C::kOffConst, p.G, kZp);
+    constexpr int R = C::kRowsPerWarp;
+    const SmallLayout L(C::kBTileBytes, C::kOffStages, p.G, kZp);
     const int P = L.p_stages;
-    const int slot_floats = L.slot_floats;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *a_ring = smem + C::kOffA;
-    uint8_t *p_ring = smem + L.off_p;
-    float *const_ring = reinterpret_cast<float *>(smem + C::kOffConst);
+    uint8_t *p_ring = smem + C::kOffStages;
     const uint32_t bar0 = smem_addr(smem + L.off_bar);
-    // barriers: full_p / empty_p  load stage landed / released by the warps that read it and the MMAs
-    //           full_o / sfree    operand slot (A, B, constants) built / released after the k-block's epilogue
-    //           full_t / empty_t  TMEM accumulator buffer written by the MMAs / read by the epilogue
+    // barriers: full_p / empty_p  load stage landed / released after the k-block's epilogue
+    //           full_t / empty_t  TMEM accumulator written by the MMAs / read by the workers
+    // and the named barriers kOperandBarrier0 + c: converted weight slot c ready for k-block i (i % 2 == c). When
+    // the workers arrive there for k-block i they have finished the epilogue of k-block i - 2, so the MMAs of the
+    // slot's previous k-block are done and so is every read of the TMEM buffers used two k-blocks back; and the MMA
+    // warp has passed that barrier for k-block i - 2 (the workers waited for its commits), so no arrival can count
+    // towards an earlier phase.
     auto full_p = [&](int s) { return bar0 + 8u * s; };
     auto empty_p = [&](int s) { return bar0 + 8u * (P + s); };
-    auto full_o = [&](int c) { return bar0 + 8u * (2 * P + c); };
-    auto sfree = [&](int c) { return bar0 + 8u * (2 * P + kCStages + c); };
-    auto full_t = [&](int b) { return bar0 + 8u * (2 * P + 2 * kCStages + b); };
-    auto empty_t = [&](int b) { return bar0 + 8u * (2 * P + 2 * kCStages + 2 + b); };
+    constexpr int kTmemBufs = C::kTmemBufs;
+    auto full_t = [&](int b) { return bar0 + 8u * (2 * P + b); };
+    auto empty_t = [&](int b) { return bar0 + 8u * (2 * P + kMaxTmemBufs + b); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.off_misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.off_misc + 4);
     int *last_flag = reinterpret_cast<int *>(smem + L.off_misc + 8);
@@ -404,6 +453,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int M = p.M, K = p.K, N = p.N, G = p.G;
     const int m0 = mt * p.m_sub;
     const int gpk = kKBlock / G;                         // groups per k-block
+    const int Gn = K / G;
     const bool debug = p.dbg_group >= 0;
     int kb0, kb1;
     if (debug) {
@@ -418,7 +468,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     // One load stage: the k-block's packed weight tile, planes image, constants, scale tile and zero-point tile, all
     // counted on full_p(s).
     const uint8_t *w_src = p.w + (static_cast<size_t>(nt) * p.kb_total + kb0) * kPackedTileBytes;
-    const int Gn = K / G;
     auto groups_in = [&](int kb) { return (min(K, (kb + 1) * kKBlock) - kb * kKBlock) / G; };
     auto stage_tx = [&](int kb) {
         return static_cast<uint32_t>(kPackedTileBytes + C::kBTileBytes + groups_in(kb) * kConstFloatsPerGroup * 4 +
@@ -446,21 +495,17 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // ---- set-up. Thread 0 lets the next kernel on the stream start launching, initialises the barriers and at once
     // starts the weight loads of the first ring's worth of k-blocks (the slots are free), so the memory latency
-    // overlaps the rest of the set-up and, under programmatic launch, the tail of the preceding kernel.
+    // overlaps the rest of the set-up and, under programmatic launch, the tail of the unfold pre-pass.
     const int first_loads = nkb < P ? nkb : P;
     uint64_t stream_policy = 0, keep_policy = 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < P; ++s) {
             mbar_init(full_p(s), 1);
-            mbar_init(empty_p(s), kNumConvWarps + kNumEpiWarps + 1);     // + the MMAs' commit
+            mbar_init(empty_p(s), kNumWorkWarps);
         }
-        for (int c = 0; c < kCStages; ++c) {
-            mbar_init(full_o(c), kNumConvWarps + kNumEpiWarps);
-            mbar_init(sfree(c), kNumEpiWarps);
-        }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kTmemBufs; ++b) {
             mbar_init(full_t(b), 1);
-            mbar_init(empty_t(b), kNumEpiWarps);
+            mbar_init(empty_t(b), kNumWorkWarps);
         }
         *abort_flag = 0;
         *last_flag = 0;
@@ -492,31 +537,35 @@ __global__ void __launch_bounds__(kThreads, 2)
                 issue_dynamic(issued, keep_policy);
             }
             // no copy may still be writing shared memory when the CTA exits
-            for (int j = issued > P ? issued - P : 0; j < issued; ++j)
-                mbar_wait_drain(full_p(j % P), (j / P) & 1);
+            for (int j = issued > P ? issued - P : 0; j < issued; ++j) mbar_wait_drain(full_p(j % P), (j / P) & 1);
         }
     } else if (warp == kMmaWarp) {
         // ================================================================ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_e4m3_f32(NMMA);
-            int j = 0;                       // CTA-local group counter
-            int last_j[2] = {-1, -1};
-            int last_i = -1;                 // last k-block whose MMAs release its load stage
-            for (int i = 0; i < nkb; ++i) {
-                const int c = i % kCStages, s = i % P;
-                // the builders have seen the stage land before building the slot; the planes are read in place
-                if (!mbar_wait(full_o(c), (i / kCStages) & 1, abort_flag, kSiteMmaOperands)) break;
-                if (!mbar_wait(full_p(s), (i / P) & 1, abort_flag, kSiteMmaOperands)) break;
+        constexpr uint32_t idesc = idesc_e4m3_f32(NMMA);
+        int j = 0;                           // CTA-local group counter
+        int last_j[kTmemBufs];
+        for (int b = 0; b < kTmemBufs; ++b) last_j[b] = -1;
+        int prev_first = 0;                  // first group of the previous k-block
+        for (int i = 0; i < nkb; ++i) {
+            const int c = i % kASlots, s = i % P;
+            // the whole warp: converted tile i is ready (barrier ids stay compile-time constants)
+            if (c == 0) named_bar_sync(kOperandBarrier0, kOperandThreads);
+            else named_bar_sync(kOperandBarrier0 + 1, kOperandThreads);
+            const int ng = groups_in(kb0 + i);
+            const int first = j;
+            if (lane == 0) {
                 tc_fence_after_sync();
-                const int ng = groups_in(kb0 + i);
                 const uint32_t a_base = smem_addr(a_ring + c * kATileBytes);
                 const uint32_t b_base = smem_addr(p_ring + s * L.stage_bytes + L.b_off);
-                bool stop = false;
-                for (int gg = 0; gg < ng; ++gg, ++j) {
-                    const int b = j & 1;
-                    if (!mbar_wait(empty_t(b), ((j >> 1) & 1) ^ 1, abort_flag, kSiteMmaTmemEmpty)) {
-                        stop = true;
-                        break;
+                for (int gg = 0; gg < ng; ++gg) {
+                    const int jj = first + gg, b = jj % kTmemBufs;
+                    // a buffer last used two or more k-blocks back was read before the workers arrived above;
+                    // one used by the previous k-block (four buffers and G = 32 only) may still be read by its
+                    // epilogue. That wait ignores the abort flag: the workers keep releasing buffers regardless.
+                    if (jj - kTmemBufs >= prev_first &&
+                        !mbar_wait_drain(empty_t(b), ((jj / kTmemBufs) & 1) ^ 1)) {
+                        *abort_flag = 1;
+                        record_timeout(kSiteMmaTmemEmpty);
                     }
                     tc_fence_after_sync();
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * C::kBufStride);
@@ -526,179 +575,146 @@ __global__ void __launch_bounds__(kThreads, 2)
                                     idesc, ks > 0 ? 1u : 0u);
                     }
                     umma_commit(full_t(b));
-                    last_j[b] = j;
-                }
-                if (stop) break;
-                umma_commit(empty_p(s));         // the stage (planes image) is free once these MMAs are done
-                last_i = i;
-            }
-            // no MMA may still be writing TMEM when it is freed, nor arrive on a barrier after the CTA exits
-            for (int b = 0; b < 2; ++b)
-                if (last_j[b] >= 0) mbar_wait_drain(full_t(b), (last_j[b] >> 1) & 1);
-            if (last_i >= 0) mbar_wait_drain(empty_p(last_i % P), (last_i / P) & 1);
-        }
-        __syncwarp();
-    } else if (warp < kConvWarp0 + kNumConvWarps) {
-        // ================================================================ operand builders
-        const int ct = threadIdx.x - kConvWarp0 * 32;   // 0..127: also this thread's column for the scale copy
-        for (int i = 0; i < nkb; ++i) {
-            const int s = i % P, c = i % kCStages;
-            if (!mbar_wait_warp(full_p(s), (i / P) & 1, abort_flag, kSiteConvFull)) break;
-            if (!mbar_wait_warp(sfree(c), ((i / kCStages) & 1) ^ 1, abort_flag, kSiteConvEmpty)) break;
-            const uint8_t *stage = p_ring + s * L.stage_bytes;
-            convert_half_tile(stage, a_ring + c * kATileBytes, ct, 0);
-            // the combine constants of the k-block's groups (128 floats each: one per thread) and its scales
-            float *cst = const_ring + c * slot_floats;
-            const float *cs = reinterpret_cast<const float *>(stage + L.c_off);
-            const int ng = groups_in(kb0 + i);
-            for (int gg = 0; gg < ng; ++gg) cst[gg * kConstFloatsPerGroup + ct] = cs[gg * kConstFloatsPerGroup + ct];
-            if (!debug) {
-                const __half *ss = reinterpret_cast<const __half *>(stage + L.s_off);
-                for (int gg = 0; gg < gpk; ++gg)
-                    cst[L.scale_floats + gg * kTileN + ct] = __half2float(ss[gg * kTileN + ct]);
-                if constexpr (kZp) {
-                    const __half *zs = reinterpret_cast<const __half *>(stage + L.z_off);
-                    for (int gg = 0; gg < gpk; ++gg)
-                        cst[L.zp_floats + gg * kTileN + ct] = fmaf(__half2float(zs[gg * kTileN + ct]), 0.125f, 1.0f);
+                    last_j[b] = jj;
                 }
             }
-            fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(empty_p(s));
-                mbar_arrive(full_o(c));
-            }
+            prev_first = first;
+            j = first + ng;
         }
+        // no MMA may still be writing TMEM when it is freed, nor arrive on a barrier after the CTA exits
+        if (lane == 0)
+            for (int b = 0; b < kTmemBufs; ++b)
+                if (last_j[b] >= 0) mbar_wait_drain(full_t(b), (last_j[b] / kTmemBufs) & 1);
+        __syncwarp();
     } else {
-        // ================================================================ epilogue
+        // ================================================================ workers
         pdl_wait();                                      // outputs are written after the preceding kernel ended
+        const int w = warp - kWorkWarp0;                 // 0..7
+        const int wt = threadIdx.x - kWorkWarp0 * 32;    // 0..255
         const int quarter = warp & 3;                    // TMEM lanes this warp may read
-        const int et = threadIdx.x - kEpiWarp0 * 32;
+        const int half = w >> 2;                         // rows [half * R, half * R + R)
         const int n_local = quarter * 32 + lane;
         const int n = nt * kTileN + n_local;
         const int rows_valid = min(p.m_sub, M - m0);
-        const float bias_n = p.bias != nullptr && n < N ? __half2float(p.bias[n]) : 0.0f;
-        float yacc[kMaxM];
+        float yacc[R];
 #pragma unroll
-        for (int m = 0; m < kMaxM; ++m) yacc[m] = 0.0f;
+        for (int r = 0; r < R; ++r) yacc[r] = 0.0f;
 
-        // Iteration i converts the second half of k-block i's weight tile, then runs the epilogue of k-block i - 1.
+        // Iteration i converts k-block i's weight tile, then runs the epilogue of k-block i - 1. After a failed wait
+        // the work is skipped, but every synchronisation with the MMA warp goes on.
         bool ok = true;
         int j = 0;
-        for (int i = 0; i <= nkb && ok; ++i) {
+        for (int i = 0; i <= nkb; ++i) {
             if (i < nkb) {
-                const int s = i % P, c = i % kCStages;
-                ok = mbar_wait_warp(full_p(s), (i / P) & 1, abort_flag, kSiteConvFull) &&
-                     mbar_wait_warp(sfree(c), ((i / kCStages) & 1) ^ 1, abort_flag, kSiteConvEmpty);
+                const int s = i % P, c = i % kASlots;
+                ok = ok && mbar_wait_warp(full_p(s), (i / P) & 1, abort_flag, kSiteConvFull);
                 if (ok) {
-                    convert_half_tile(p_ring + s * L.stage_bytes, a_ring + c * kATileBytes, et, 1);
+                    convert_tile256(p_ring + s * L.stage_bytes, a_ring + c * kATileBytes, wt);
                     fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(empty_p(s));
-                        mbar_arrive(full_o(c));
-                    }
                 }
+                __syncwarp();
+                if (c == 0) named_bar_arrive(kOperandBarrier0, kOperandThreads);
+                else named_bar_arrive(kOperandBarrier0 + 1, kOperandThreads);
             }
             const int ie = i - 1;                        // k-block whose epilogue runs now
-            if (ok && ie >= 0) {
-                const int c = ie % kCStages;
-                // the builders' constant writes for this k-block are ordered before this wait (the phase cannot
-                // move on: the next use of slot c waits for sfree(c), which is released below)
-                ok = mbar_wait_warp(full_o(c), (ie / kCStages) & 1, abort_flag, kSiteEpiOperandsEmpty);
-                const int kb = kb0 + ie;
-                const int gfirst = kb * gpk;
-                const int ng = (min(K, (kb + 1) * kKBlock) - kb * kKBlock) / G;
-                const float *cst = const_ring + c * slot_floats;
-                for (int gg = 0; gg < ng && ok; ++gg, ++j) {
-                    const int b = j & 1;
-                    const int g = gfirst + gg;
-                    const float s_n = cst[L.scale_floats + gg * kTileN + n_local];
-                    const float f_n = kZp ? cst[L.zp_floats + gg * kTileN + n_local] : 1.0f;
-                    ok = mbar_wait_warp(full_t(b), (j >> 1) & 1, abort_flag, kSiteEpiTmemFull);
-                    if (!ok) break;
-                    tc_fence_after_sync();
-                    uint32_t d[3][16];
-                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                           static_cast<uint32_t>(b * C::kBufStride);
-                    tmem_ld16(taddr, d[0]);
-                    if (NMMA > 16) tmem_ld16(taddr + 16, d[1]);
-                    if (NMMA > 32) tmem_ld16(taddr + 32, d[2]);
-                    tmem_wait_ld();
-                    reg_fence16(d[0]);
-                    if (NMMA > 16) reg_fence16(d[1]);
-                    if (NMMA > 32) reg_fence16(d[2]);
-                    tc_fence_before_sync();
+            if (ie < 0) continue;
+            const int se = ie % P;
+            const uint8_t *stage = p_ring + se * L.stage_bytes;
+            const float4 *cs = reinterpret_cast<const float4 *>(stage + L.c_off);
+            const __half *ss = reinterpret_cast<const __half *>(stage + L.s_off);
+            const __half *zs = reinterpret_cast<const __half *>(stage + L.z_off);
+            const int kb = kb0 + ie;
+            const int ng = groups_in(kb);
+            for (int gg = 0; gg < ng; ++gg, ++j) {
+                const int b = j % kTmemBufs;
+                const bool live = ok;
+                const float s_n = debug || !live ? 0.0f : __half2float(ss[gg * kTileN + n_local]);
+                const float f_n =
+                    kZp && !debug && live ? fmaf(__half2float(zs[gg * kTileN + n_local]), 0.125f, 1.0f) : 1.0f;
+                // the MMAs' commit is waited for even after a failure (bounded), so that this warp never gets two
+                // phases ahead of the MMA warp on an operand barrier
+                if (!mbar_wait_warp(full_t(b), (j / kTmemBufs) & 1, abort_flag, kSiteEpiTmemFull)) {
+                    ok = false;
+                    bool drained = true;
+                    if (lane == 0) drained = mbar_wait_drain(full_t(b), (j / kTmemBufs) & 1);
+                    (void)__shfl_sync(0xffffffffu, drained ? 1 : 0, 0);
+                }
+                if (!live || !ok) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(empty_t(b));
-                    const float *cg = cst + gg * kConstFloatsPerGroup;
-                    if (debug) {
-                        if (g == p.dbg_group && n < N) {
-#pragma unroll
-                            for (int m = 0; m < kMaxM; ++m) {
-                                if (m < rows_valid) {
-#pragma unroll
-                                    for (int pl = 0; pl < 3; ++pl) {
-                                        const int col = pl * kMaxM + m;
-                                        const float dv = __uint_as_float(d[col >> 4][col & 15]);
-                                        const float yi = kMmaUnit * dv - 8.0f * cg[(4 + pl) * 16 + m];
-                                        p.dbg_y123[(static_cast<size_t>(pl) * M + m0 + m) * N + n] =
-                                            __float2int_rn(yi);
-                                    }
-                                }
-                            }
-                        }
-                        continue;
-                    }
-#pragma unroll
-                    for (int m = 0; m < kMaxM; ++m) {
-                        if (m < rows_valid) {
-                            const float d1 = __uint_as_float(d[m >> 4][m & 15]);
-                            const float d2 = __uint_as_float(d[(kMaxM + m) >> 4][(kMaxM + m) & 15]);
-                            const float d3 = __uint_as_float(d[(2 * kMaxM + m) >> 4][(2 * kMaxM + m) & 15]);
-                            float t = fmaf(cg[m], d1, kZp ? -cg[48 + m] * f_n : -cg[48 + m]);
-                            t = fmaf(cg[16 + m], d2, t);
-                            t = fmaf(cg[32 + m], d3, t);
-                            yacc[m] = fmaf(s_n, t, yacc[m]);
-                        }
-                    }
+                    continue;
                 }
-                // this k-block's MMAs have all completed (the last full_t wait saw them): release the slot
+                tc_fence_after_sync();
+                uint32_t d[3][16];
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                       static_cast<uint32_t>(b * C::kBufStride);
+                tmem_ld16(taddr, d[0]);
+                if (NMMA > 16) tmem_ld16(taddr + 16, d[1]);
+                if (NMMA > 32) tmem_ld16(taddr + 32, d[2]);
+                tmem_wait_ld();
+                reg_fence16(d[0]);
+                if (NMMA > 16) reg_fence16(d[1]);
+                if (NMMA > 32) reg_fence16(d[2]);
+                tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(sfree(c));
+                if (lane == 0) mbar_arrive(empty_t(b));
+                const float4 *cg = cs + gg * (kConstFloatsPerGroup / 4);
+                if (debug) {
+                    if (kb * gpk + gg == p.dbg_group && n < N) {
+                        if (half == 0) debug_rows<kMaxM, R, 0>(d, cg, rows_valid, p.dbg_y123, M, N, m0, n);
+                        else debug_rows<kMaxM, R, 1>(d, cg, rows_valid, p.dbg_y123, M, N, m0, n);
+                    }
+                    continue;
+                }
+                if (half == 0) combine_rows<kMaxM, R, 0, kZp>(d, cg, s_n, f_n, rows_valid, yacc);
+                else combine_rows<kMaxM, R, 1, kZp>(d, cg, s_n, f_n, rows_valid, yacc);
             }
-            ok = !named_bar_or(kEpiBarrierId, kNumEpiWarps * 32, !ok);
+            if (!ok) continue;
+            // the k-block's MMAs have completed (its last full_t wait saw them) and its constants are read
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_p(se));
         }
+        // all workers take the same path from here on (named barriers below)
+        ok = !named_bar_or(kWorkBarrierId, kWorkThreads, !ok);
 
         if (ok && !debug) {
+            const float bias_n = p.bias != nullptr && n < N ? __half2float(p.bias[n]) : 0.0f;
             if (p.reduce == kReduceNone) {
 #pragma unroll
-                for (int m = 0; m < kMaxM; ++m)
+                for (int r = 0; r < R; ++r) {
+                    const int m = half * R + r;
                     if (m < rows_valid && n < N)
                         p.y[static_cast<size_t>(m0 + m) * N + n] =
-                            __float2half_rn(p.bias != nullptr ? yacc[m] + bias_n : yacc[m]);
+                            __float2half_rn(p.bias != nullptr ? yacc[r] + bias_n : yacc[r]);
+                }
             } else if (p.reduce == kReduceCluster) {
-                // this slice's partial sums go to shared memory (the converted-weight ring is idle by now); the
+                // this slice's partial sums go to shared memory (the converted-weight slots are idle by now); the
                 // cluster reduces them after the cluster barrier below
                 float *red = reinterpret_cast<float *>(a_ring);
 #pragma unroll
-                for (int m = 0; m < kMaxM; ++m) red[m * kTileN + n_local] = yacc[m];
+                for (int r = 0; r < R; ++r) {
+                    const int m = half * R + r;
+                    if (m < kMaxM) red[m * kTileN + n_local] = yacc[r];
+                }
             } else {
                 float *part = p.ws_part + static_cast<size_t>(sp) * M * N;
 #pragma unroll
-                for (int m = 0; m < kMaxM; ++m)
-                    if (m < rows_valid && n < N) part[static_cast<size_t>(m0 + m) * N + n] = yacc[m];
+                for (int r = 0; r < R; ++r) {
+                    const int m = half * R + r;
+                    if (m < rows_valid && n < N) part[static_cast<size_t>(m0 + m) * N + n] = yacc[r];
+                }
                 __threadfence();
-                named_bar_sync(kEpiBarrierId, kNumEpiWarps * 32);
-                if (et == 0) {
+                named_bar_sync(kWorkBarrierId, kWorkThreads);
+                if (wt == 0) {
                     const uint32_t prev = atomicAdd(p.ws_count + static_cast<size_t>(mt) * p.n_tiles + nt, 1u);
                     *last_flag = (prev == static_cast<uint32_t>(p.splits - 1));
                 }
-                named_bar_sync(kEpiBarrierId, kNumEpiWarps * 32);
+                named_bar_sync(kWorkBarrierId, kWorkThreads);
                 if (*last_flag) {
                     __threadfence();
-                    for (int m = 0; m < rows_valid; ++m) {
-                        if (n >= N) break;
+                    // the two warps of a lane quarter take alternate rows
+                    for (int m = half; m < rows_valid && n < N; m += 2) {
                         const float *src = p.ws_part + static_cast<size_t>(m0 + m) * N + n;
                         const size_t slice = static_cast<size_t>(M) * N;
                         float acc = 0.0f;
@@ -712,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         if (p.bias != nullptr) acc += bias_n;
                         p.y[static_cast<size_t>(m0 + m) * N + n] = __float2half_rn(acc);
                     }
-                    if (et == 0) p.ws_count[static_cast<size_t>(mt) * p.n_tiles + nt] = 0u;
+                    if (wt == 0) p.ws_count[static_cast<size_t>(mt) * p.n_tiles + nt] = 0u;
                 }
             }
         }
@@ -722,13 +738,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         // every thread of every CTA of the cluster takes part in both barriers (warps reconverged first)
         __syncwarp();
         cluster_sync_all();                                      // all partial sums are in shared memory
-        if (warp >= kEpiWarp0) {
+        if (warp >= kWorkWarp0) {
+            const int half = (warp - kWorkWarp0) >> 2;
             const int n_local = (warp & 3) * 32 + lane;
             const int n = nt * kTileN + n_local;
             const int rows_valid = min(p.m_sub, M - m0);
             const uint32_t red = smem_addr(a_ring);
-            // CTA r of the cluster finishes rows r, r + S, ...; every row sums the slices in slice order
-            for (int m = static_cast<int>(cluster_ctarank()); m < rows_valid && n < N; m += p.splits) {
+            // CTA r of the cluster finishes rows r, r + S, ... (alternating between the two warps of a lane
+            // quarter); every row sums the slices in slice order
+            for (int m = static_cast<int>(cluster_ctarank()) + half * p.splits; m < rows_valid && n < N;
+                 m += 2 * p.splits) {
                 float v[kMaxClusterSplits];
                 const uint32_t off = static_cast<uint32_t>((m * kTileN + n_local) * 4);
 #pragma unroll

@@ -39,18 +39,11 @@ __device__ __forceinline__ void mbar_fence_init() {
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile(
-        "{\n\t.reg .b64 st;\n\t"
-        "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
-        : "memory");
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile(
-        "{\n\t.reg .b64 st;\n\t"
-        "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
-        "r"(bytes)
-        : "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
 // true once the phase with the given parity has completed
@@ -66,6 +59,21 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same test, letting the hardware suspend the thread until the phase completes or `hint_ns` passes, so that a
+// waiting warp takes no issue slots from the warps doing work on its SM sub-partition.
+constexpr uint32_t kSuspendHintNs = 20000;
+__device__ __forceinline__ bool mbar_test_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns = kSuspendHintNs) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait. Returns false (and raises *abort) when the limit passes; returns false at once when *abort is
 // already raised by another thread of the CTA.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort, int site,
@@ -73,7 +81,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_test(bar, parity)) return true;
+        if (mbar_test_suspend(bar, parity)) return true;
         if (*abort) return false;
         if (globaltimer_ns() - t0 > limit_ns) {
             *abort = 1;
@@ -95,13 +103,19 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, vo
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_test(bar, parity)) {
+    while (!mbar_test_suspend(bar, parity)) {
         if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
     }
     return true;
 }
 
 // ------------------------------------------------------------------------------------------------ named barriers
+
+// Arrival on a named barrier without waiting (the warp must be converged); completes when `nthreads` threads,
+// counting those that wait on it with named_bar_sync, have arrived.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -189,6 +203,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
         "{%2, %3}], [%4], %5;" ::"r"(dst),
         "l"(tmap), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
         : "memory");
+}
+
+// 16 bytes from global memory that this kernel does not write, not kept in L1, with an L2 eviction policy
+__device__ __forceinline__ uint4 ldg_stream16(const void *p, uint64_t policy) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(policy));
+    return v;
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {

@@ -62,7 +62,7 @@ wqbmm_status check_shape(const Shape &s) {
     return WQBMM_OK;
 }
 
-constexpr int64_t kLargeM = 64;     // from this many rows on, x is unfolded once by a pre-pass (large-M path)
+constexpr int64_t kLargeM = 64;     // from this many rows on: the pre-pass and the 128 x 128 tile GEMM (large-M path)
 constexpr int64_t kGemvMaxM = kGemvMaxRows;   // up to this many rows: the dp4a matrix-vector path
 
 // Small-M path: rows of x per CTA, the MMA N (three stacked planes padded to 16, 32 or 48 rows), the split over K.
@@ -202,14 +202,14 @@ template <int NMMA, bool kZp>
 wqbmm_status launch_msd(const RunParams &rp, const Plan &plan, DeviceInfo *info, cudaStream_t stream) {
     constexpr int idx = (kZp ? 3 : 0) + NMMA / 16 - 1;
     using C = Cfg<NMMA>;
-    const int smem = SmallLayout(C::kBTileBytes, C::kOffConst, rp.G, kZp).smem_bytes;
+    const int smem = SmallLayout(C::kBTileBytes, C::kOffStages, rp.G, kZp).smem_bytes;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         if (!info->smem_set[idx]) {
             // the limit covers every group size (G = 32 has the largest layout)
             int most = 0;
             for (int g : {32, 64, 128}) {
-                const int b = SmallLayout(C::kBTileBytes, C::kOffConst, g, kZp).smem_bytes;
+                const int b = SmallLayout(C::kBTileBytes, C::kOffStages, g, kZp).smem_bytes;
                 most = b > most ? b : most;
             }
             if (cudaFuncSetAttribute(msd_kernel<NMMA, kZp>, cudaFuncAttributeMaxDynamicSharedMemorySize, most) !=
