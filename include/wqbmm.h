@@ -14,6 +14,8 @@
  *   y[m, n] = sum over the groups of Y_group, rounded once to fp16 (nearest-even).
  * The unfold runs in IEEE binary32 with the constants 7.49f and 14.98f, every operation rounded on its own and the
  * division correctly rounded; "round" is half-to-even. A group whose A_max is 0 contributes 0.
+ * Per-channel quantization is the case G = K: one group spans each row, A_max is the row's maximum and
+ * antiquant_scale (and the zero points of wqbmm_run_ex) have one row, [1, N].
  *
  * Weight format: the caller's int4 weights are packed two per byte along K (page section 4.3): uint8 [K/2, N], byte
  * (kk, n) holds w[2kk, n] in its low nibble and w[2kk+1, n] in its high nibble, two's complement. Before the first
@@ -62,7 +64,8 @@ typedef enum {
 } wqbmm_status;
 
 /* Shape rules shared by the entry points that take (M, K, N, G):
- *   1 <= M, K, N <= 2^31 - 1;  G in {32, 64, 128};  K % G == 0;  N % 8 == 0;  M * N, M * K < 2^62.
+ *   1 <= M, K, N <= 2^31 - 1;  G in {32, 64, 128}, or G == K with K % 32 == 0 (per channel);  K % G == 0;
+ *   N % 8 == 0;  M * N, M * K < 2^62.
  * Alignment rules: x, antiquant_scale, y, the prepacked weights and the workspace start on 16-byte boundaries. */
 
 /*
@@ -100,7 +103,9 @@ WQBMM_API wqbmm_status wqbmm_prepack_weight_nk(const uint8_t *w_packed_nk, void 
  * 3 <= M < 64 the planes as the tensor cores' operand image (16, 32 or 48 rows of 128 bytes per row tile of up to 16
  * rows and per 128 k) and 128 floats of constants per row tile and group, then split-K partial sums and per-tile
  * arrival counters (only shapes whose split over K is wider than one thread-block cluster need those); for M >= 64
- * the planes (3 bytes per element of x, rows padded to a multiple of 128) and the constants.
+ * the planes (3 bytes per element of x, rows padded to a multiple of 128) and the constants. Per channel it also
+ * holds each row's A_max and, for M >= 3, the scale and zero-point rows repeated once per 128 k (or 64 or 32 when K
+ * is not a multiple of 128).
  * It must be zero-filled once before its first use; every successful run leaves the counters at zero again, so the
  * same workspace can be reused by later runs on the same stream without clearing. Runs that execute concurrently must
  * use different workspaces.
@@ -159,7 +164,8 @@ WQBMM_API wqbmm_status wqbmm_debug_unfold(const void *x, int64_t M, int64_t K, i
  * kernel wqbmm_run would pick for this M, restricted to the k-block that holds group g.
  *   y123       device, int32 [3, M, N]: Y_i[m, n] of group g at y123[(i * M + m) * N + n]
  *   workspace  device, wqbmm_workspace_bytes(M, K, N, G) bytes
- * 0 <= g < K/G. Errors: NULLPTR, INVALID (also a workspace too small), UNSUPPORTED_ARCH, CUDA.
+ * 0 <= g < K/G; G in {32, 64, 128} (per-channel partials are not exposed: INVALID). Errors: NULLPTR, INVALID (also
+ * a workspace too small), UNSUPPORTED_ARCH, CUDA.
  */
 WQBMM_API wqbmm_status wqbmm_debug_group_partials(const void *x, const void *w_prepacked, int64_t M, int64_t K,
                                                   int64_t N, int64_t G, int64_t g, int32_t *y123, void *workspace,

@@ -73,6 +73,24 @@ def test_workspace_bytes():
     # workspace: 160 x 3 x 256 fp32 partial sums + one 256-byte block of counters after the unfolded x
     assert wq.wqbmm_workspace_bytes(3, 65536, 256, 128) == 512 * 16 * 128 + 512 * 512 + 160 * 3 * 256 * 4 + 256
     assert wq.wqbmm_workspace_bytes(40, 1024, 28672, 128) == 3 * 8 * 48 * 128 + 3 * 8 * 512
+
+
+def _a256(v):
+    return (v + 255) // 256 * 256
+
+
+def test_workspace_bytes_per_channel():
+    # G = K: the kernels work in 128-k sub-groups with each row's A_max; the decode path adds the row maxima,
+    # the others also the scale and zero-point rows repeated per sub-group
+    assert wq.wqbmm_workspace_bytes(1, 4096, 4096, 4096) == 3 * 4096 + 16 * 32 + _a256(4)
+    assert wq.wqbmm_workspace_bytes(8, 4096, 11008, 4096) == (32 * 32 * 128 + 32 * 512 + _a256(8 * 4) +
+                                                               2 * _a256(32 * 11008 * 2))
+    assert wq.wqbmm_workspace_bytes(256, 1024, 392, 1024) == (3 * 256 * 1024 + 16 * 256 * 8 + _a256(256 * 4) +
+                                                                2 * _a256(8 * 392 * 2))
+    # K not a multiple of 128: sub-groups of 32
+    assert wq.wqbmm_workspace_bytes(2, 352, 136, 352) == _a256(2 * 3 * 384) + _a256(2 * 11 * 16) + _a256(8)
+    # G = K = 64 is an ordinary group (same arithmetic): no per-channel extras
+    assert wq.wqbmm_workspace_bytes(1, 64, 128, 64) == 256 * 2 + 256
     # M >= 64: x unfolded once into three planes of 128-row tiles (3 bytes per element of x, rows padded to 128)
     # plus 16 bytes of combine constants per padded row and group
     assert wq.wqbmm_workspace_bytes(2048, 8192, 28672, 64) == 3 * 2048 * 8192 + 16 * 2048 * 128
@@ -110,7 +128,7 @@ CASES = [
     ("run_negative_k", lambda L: L.wqbmm_run(A, A, A, A, 1, -128, 128, 128, A, 1 << 20, None), INVALID),
     ("run_k_not_multiple_of_group", lambda L: L.wqbmm_run(A, A, A, A, 1, 160, 128, 128, A, 1 << 20, None),
      INVALID),
-    ("run_group_not_supported", lambda L: L.wqbmm_run(A, A, A, A, 1, 256, 128, 256, A, 1 << 20, None), INVALID),
+    ("run_group_not_supported", lambda L: L.wqbmm_run(A, A, A, A, 1, 192, 128, 96, A, 1 << 20, None), INVALID),
     ("run_n_ragged_by_4", lambda L: L.wqbmm_run(A, A, A, A, 1, 128, 132, 128, A, 1 << 20, None), INVALID),
     ("run_m_too_large", lambda L: L.wqbmm_run(A, A, A, A, 1 << 31, 128, 128, 128, A, 1 << 20, None), INVALID),
     ("run_misaligned_x", lambda L: L.wqbmm_run(MIS, A, A, A, 1, 128, 128, 128, A, 1 << 20, None), INVALID),
@@ -128,6 +146,12 @@ CASES = [
     ("run_ex_misaligned_bias",
      lambda L: L.wqbmm_run_ex(A, A, A, None, MIS, A, 200, 128, 128, 128, A, 1 << 20, None), INVALID),
     ("run_ex_bad_group", lambda L: L.wqbmm_run_ex(A, A, A, A, A, A, 8, 128, 128, 16, A, 1 << 20, None), INVALID),
+    ("run_per_channel_k_not_multiple_of_32",
+     lambda L: L.wqbmm_run(A, A, A, A, 1, 100, 128, 100, A, 1 << 20, None), INVALID),
+    ("run_group_larger_than_128_not_k", lambda L: L.wqbmm_run(A, A, A, A, 1, 512, 128, 256, A, 1 << 20, None),
+     INVALID),
+    ("partials_per_channel_not_exposed",
+     lambda L: L.wqbmm_debug_group_partials(A, A, 1, 256, 128, 256, 0, A, A, 1 << 20, None), INVALID),
     ("run_ex_null_workspace_needed",
      lambda L: L.wqbmm_run_ex(A, A, A, A, A, A, 1, 65536, 256, 128, None, 0, None), NULLPTR),
     ("unfold_null_planes", lambda L: L.wqbmm_debug_unfold(A, 1, 128, 128, None, A, None), NULLPTR),

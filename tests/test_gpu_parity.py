@@ -453,3 +453,45 @@ def test_run_ex_mid_workload_sampled_rows(dev):
     rows = I.sample_rows(wl, 8)
     ref = oracle.msd_matmul_ex(x, wp, sc, wl.G, zero_point=zp, bias=bias, mode=oracle.MODE_D, rows=rows)
     assert_within_tolerance(y[rows], ref, wl.name)
+
+
+# ------------------------------------------------------------------------------------------- per channel (G = K)
+
+PC_CASES = [
+    # M, K, N, zero-point kind (None: none), bias
+    (1, 4096, 520, None, False),      # decode kernel: one scale row serves every 128-k sub-group
+    (2, 1024, 1000, "frac", True),
+    (3, 2048, 264, None, False),      # small-M tensor-core kernel
+    (8, 4096, 1000, "int", True),
+    (16, 1024, 256, "frac", False),   # cluster-reduced split-K
+    (3, 65536, 256, None, True),      # split-K through the workspace
+    (64, 1024, 264, None, False),     # large-M pre-pass + tiles
+    (130, 512, 256, "frac", True),
+    (4, 352, 136, None, False),       # K not a multiple of 128: sub-groups of 32
+    (200, 160, 264, "int", True),
+]
+
+
+@pytest.mark.parametrize("M,K,N,zkind,with_bias", PC_CASES)
+def test_per_channel_matches_oracle(dev, M, K, N, zkind, with_bias):
+    """G = K: A_max over each whole row, one scale (and zero-point) row; against the oracle run with one group."""
+    wl = I.small_case(M, K, N, K, seed=5 * M + K + N, x_dist="t3_clip60" if M % 2 else "normal")
+    x, wp, sc = I.make_inputs(wl)
+    assert sc.shape == (1, N)
+    zp = None if zkind is None else I.make_zero_point(wl, zkind)
+    bias = I.make_bias(wl) if with_bias else None
+    y = gpu_run_ex(x, wp, sc, zp, bias, K, dev)
+    for mode, what in ((oracle.MODE_D, "binary64 oracle"), (oracle.MODE_F, "binary32-unfold oracle")):
+        ref = oracle.msd_matmul_ex(x, wp, sc, K, zero_point=zp, bias=bias, mode=mode)
+        assert_within_tolerance(y, ref, what)
+
+
+@pytest.mark.parametrize("M,K", [(9, 1024), (3, 352), (2, 4096)])
+def test_unfold_bit_exact_per_channel(dev, M, K):
+    x = I.make_x(I.small_case(M, K, 8, K, seed=K + M, x_dist="t3_clip60"))
+    planes = torch.empty((3, M, K), dtype=torch.int8, device=dev)
+    amax = torch.empty((M, 1), dtype=torch.float32, device=dev)
+    wq.wqbmm_debug_unfold(to_dev(x, dev), M, K, K, planes, amax)
+    p_ref, a_ref = oracle.unfold(x, K, oracle.MODE_F)
+    np.testing.assert_array_equal(amax.cpu().numpy(), a_ref.astype(np.float32))
+    np.testing.assert_array_equal(planes.cpu().numpy(), p_ref)

@@ -77,7 +77,8 @@ struct GemmParams {
 // holds the plane sums {S1, S2, S3, 0} instead.
 __global__ void __launch_bounds__(256) unfold_planes_kernel(const __half *__restrict__ x, int M, int K, int G,
                                                             int kb_total, uint8_t *__restrict__ planes,
-                                                            float4 *__restrict__ consts, int debug) {
+                                                            float4 *__restrict__ consts, int debug,
+                                                            const float *__restrict__ row_amax) {
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);        // row within the padded rows
@@ -90,6 +91,7 @@ __global__ void __launch_bounds__(256) unfold_planes_kernel(const __half *__rest
     load_x4(x, M, K, row, kbase, v);
     float am = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
     am = group_absmax(am, lpg);
+    if (row_amax != nullptr) am = row < M ? row_amax[row] : 0.0f;   // per channel: the whole row's maximum
     float a1[4], a2[4], a3[4];
     msd_unfold4(v, am, a1, a2, a3);
     const int s1 = group_isum(__float2int_rn((a1[0] + a1[1]) + (a1[2] + a1[3])), lpg);

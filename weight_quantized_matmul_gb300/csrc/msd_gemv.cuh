@@ -31,7 +31,8 @@ constexpr float kDotUnitInv = 1.0f / 16.0f;          // the dot products come ou
 // constants to [row][group] (float4).
 __global__ void __launch_bounds__(128) gemv_unfold_kernel(const __half *__restrict__ x, int M, int K, int G,
                                                           int kb_total, int8_t *__restrict__ planes,
-                                                          float4 *__restrict__ consts, int debug) {
+                                                          float4 *__restrict__ consts, int debug,
+                                                          const float *__restrict__ row_amax) {
     pdl_launch_dependents();
     pdl_wait();                                        // x may be the preceding kernel's output
     const int lane = threadIdx.x & 31;
@@ -43,6 +44,7 @@ __global__ void __launch_bounds__(128) gemv_unfold_kernel(const __half *__restri
     load_x4(x, M, K, row, kb * kKBlock + lane * 4, v);
     float am = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
     am = group_absmax(am, lpg);
+    if (row_amax != nullptr) am = row_amax[row];                     // per channel: the whole row's maximum
     float a1[4], a2[4], a3[4];
     msd_unfold4(v, am, a1, a2, a3);
     const int s1 = group_isum(__float2int_rn((a1[0] + a1[1]) + (a1[2] + a1[3])), lpg);
@@ -82,6 +84,8 @@ struct GemvParams {
     const uint8_t *w;           // prepacked tiles
     const __half *scale;        // [K/G, N]
     const __half *zp;           // [K/G, N] zero points (kernel instantiated with kZp), else null
+    int group_stride;           // elements between the scale (zero-point) rows of consecutive groups: N, or 0 when
+                                // one row serves every sub-group (per-channel quantization)
     const __half *bias;         // [N] or null
     const int8_t *planes;       // from gemv_unfold_kernel
     const float4 *consts;
@@ -198,12 +202,11 @@ __global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvPar
             for (int j = 0; j < kGemvKbPerPass; ++j) {
                 const int g = ((kw0 + j) * kKBlock + chunk * 32) / G;
                 const bool in = j < nkb && g < Gn;
-                sab[j] = in && n_a < N ? __ldg(reinterpret_cast<const __half2 *>(p.scale + static_cast<size_t>(g) * N + n_a))
-                                       : __half2(0.0f, 0.0f);
+                const size_t row_at = static_cast<size_t>(g) * p.group_stride + n_a;
+                sab[j] = in && n_a < N ? __ldg(reinterpret_cast<const __half2 *>(p.scale + row_at)) : __half2(0.0f, 0.0f);
                 if constexpr (kZp) {
                     const bool first = in && n_a < N && (chunk & (lpg_chunks - 1)) == 0;
-                    zab[j] = first ? __ldg(reinterpret_cast<const __half2 *>(p.zp + static_cast<size_t>(g) * N + n_a))
-                                   : __half2(0.0f, 0.0f);
+                    zab[j] = first ? __ldg(reinterpret_cast<const __half2 *>(p.zp + row_at)) : __half2(0.0f, 0.0f);
                 }
             }
         }

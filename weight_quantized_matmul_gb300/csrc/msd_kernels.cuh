@@ -3,6 +3,8 @@
 // Kernels:
 //   prepack_kernel      packed int4 [K/2, N] -> 128x128 tiles, output-column-major, offset-binary nibbles
 //   unfold_debug_kernel steps 1-8 to global memory (int8 planes, float A_max), same arithmetic as the run kernel
+//   per_channel_prep_kernel  per-channel quantization (one group of all K): each row's A_max, and the scale and
+//                       zero-point rows repeated once per 128-k sub-group for the kernels that load them as tiles
 //   unfold_small_kernel steps 1-8 once per (row tile, 128 k): the three planes as E4M3 bytes in the MMA's B operand
 //                       image (NMMA rows x 128 k, 128-byte swizzle), and per (row, group) the combine constants
 //   msd_kernel<NMMA>    steps 9-11: per CTA one 128-column tile of y, a tile of rows and a K-slice
@@ -16,12 +18,11 @@
 //   warp 0      TMA producer: per 128 k, bulk copies of the packed weight tile (8 KB), of the planes image and of
 //               the constants, and 2-D tensor copies of the scale (and zero-point) tile, into a ring of load stages
 //   warp 1      TMEM owner and single-thread MMA issuer (tcgen05.mma kind::f8f6f4, E4M3 x E4M3 -> F32); the planes
-//               are read in place in the load stage, whose release waits for the MMAs
-//   warps 2-5   operand builders, per k-block: int4 (offset binary) -> E4M3 for half of the weight tile (128-byte-
-//               swizzled K-major layout), the combine constants, scales and zero points into an operand slot
-//   warps 6-9   the other half of each weight tile, then the epilogue of the previous k-block: TMEM -> registers,
-//               Y_i = D_i - 8 S_i folded into the combine, scale, accumulate; releasing an operand slot after its
-//               epilogue (which has seen all of that k-block's MMAs complete)
+//               are read in place in the load stage
+//   warps 2-9   workers: per k-block, int4 (offset binary) -> E4M3 for the weight tile (128-byte-swizzled K-major
+//               layout) into one of two operand slots, then the epilogue of the previous k-block: TMEM ->
+//               registers, Y_i = D_i - 8 S_i folded into the combine, scale, accumulate; the load stage is released
+//               after its epilogue (which has seen all of that k-block's MMAs complete)
 // Split-K (when there are too few column tiles to fill the GPU): up to 8 K-slices of a tile form a thread-block
 // cluster and reduce through distributed shared memory; more slices reduce through a global workspace. Either way
 // the slices are summed in slice order, so the result does not depend on timing.
@@ -273,9 +274,10 @@ __global__ void prepack_kernel(const uint8_t *__restrict__ in, uint8_t *__restri
     }
 }
 
-// One warp per (row, 128-k block): the same lane mapping and arithmetic as the run kernel's unfold.
+// One warp per (row, 128-k block): the same lane mapping and arithmetic as the run kernel's unfold. row_amax (per
+// channel: one group of all K) replaces the group maximum when given; amax_out then has one value per row.
 __global__ void unfold_debug_kernel(const __half *__restrict__ x, int M, int K, int G, int8_t *__restrict__ planes,
-                                    float *__restrict__ amax_out) {
+                                    float *__restrict__ amax_out, const float *__restrict__ row_amax) {
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x;
     const int kwarp = (blockIdx.y * (blockDim.x / 32) + threadIdx.x / 32) * kKBlock;
@@ -284,9 +286,10 @@ __global__ void unfold_debug_kernel(const __half *__restrict__ x, int M, int K, 
     const bool valid = kbase < K;                                    // lanes past K compute on zeros, store nothing
     float v[4];
     load_x4(x, M, K, row, kbase, v);
-    const int lpg = G / 4;
+    const int lpg = G < kKBlock ? G / 4 : 32;
     float am = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
     am = group_absmax(am, lpg);
+    if (row_amax != nullptr) am = row_amax[row];
     float a1[4], a2[4], a3[4];
     msd_unfold4(v, am, a1, a2, a3);
     if (!valid) return;
@@ -298,7 +301,57 @@ __global__ void unfold_debug_kernel(const __half *__restrict__ x, int M, int K, 
         planes[plane + base + j] = static_cast<int8_t>(__float2int_rn(a2[j]));
         planes[2 * plane + base + j] = static_cast<int8_t>(__float2int_rn(a3[j]));
     }
-    if ((lane & (lpg - 1)) == 0) amax_out[static_cast<size_t>(row) * (K / G) + kbase / G] = am;
+    if (amax_out != nullptr && (lane & (lpg - 1)) == 0) amax_out[static_cast<size_t>(row) * (K / G) + kbase / G] = am;
+}
+
+// Per-channel quantization (one group spanning all of K; the kernels then work in sub-groups of gs k with the
+// row's A_max). Blocks [0, M): A_max of row m = max |x[m, k]| over all k (exact: a maximum of fp16 magnitudes).
+// Blocks [M, M + gridDim.x - M): scale (and zero-point) row 0 copied to rows 0 .. reps - 1 of scale_rep / zp_rep,
+// for the kernels that load scales as [sub-group, column] tiles (null: not needed).
+__global__ void __launch_bounds__(256) per_channel_prep_kernel(const __half *__restrict__ x, int M, int K,
+                                                               float *__restrict__ row_amax,
+                                                               const __half *__restrict__ scale,
+                                                               const __half *__restrict__ zp, int N, int reps,
+                                                               __half *__restrict__ scale_rep,
+                                                               __half *__restrict__ zp_rep) {
+    pdl_launch_dependents();
+    pdl_wait();              // x may be the preceding kernel's output, which may also still read these buffers
+    if (static_cast<int>(blockIdx.x) >= M) {
+        if (scale_rep == nullptr) return;
+        const int nb = gridDim.x - M;
+        const size_t total = static_cast<size_t>(reps) * N;
+        for (size_t i = static_cast<size_t>(blockIdx.x - M) * blockDim.x + threadIdx.x; i < total;
+             i += static_cast<size_t>(nb) * blockDim.x) {
+            const int n = static_cast<int>(i % N);
+            scale_rep[i] = scale[n];
+            if (zp_rep != nullptr) zp_rep[i] = zp[n];
+        }
+        return;
+    }
+    const int m = blockIdx.x;
+    __shared__ float red[8];
+    float am = 0.0f;
+    for (int k = threadIdx.x * 8; k < K; k += blockDim.x * 8) {
+        if (k + 8 <= K) {
+            const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(x + static_cast<size_t>(m) * K + k));
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[j]));
+                am = fmaxf(am, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+        } else {
+            for (int kk = k; kk < K; ++kk) am = fmaxf(am, fabsf(__half2float(x[static_cast<size_t>(m) * K + kk])));
+        }
+    }
+    for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = am;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float r = red[0];
+        for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) r = fmaxf(r, red[w]);
+        row_amax[m] = r;
+    }
 }
 
 __global__ void wait_timeout_kernel(uint64_t limit_ns) {
@@ -324,7 +377,8 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns) {
 // correction 8 sum_i c_i A_max S_i, then the plane sums S_i (read by debug runs) and a zero: [row][8] per group.
 __global__ void __launch_bounds__(512) unfold_small_kernel(const __half *__restrict__ x, int M, int K, int G,
                                                            int kb_total, int m_sub, int nmma,
-                                                           uint8_t *__restrict__ planes, float *__restrict__ consts) {
+                                                           uint8_t *__restrict__ planes, float *__restrict__ consts,
+                                                           const float *__restrict__ row_amax) {
     pdl_launch_dependents();
     pdl_wait();                  // x may be the preceding kernel's output, which may also still read the planes
     const int lane = threadIdx.x & 31, r = threadIdx.x >> 5;
@@ -334,7 +388,8 @@ __global__ void __launch_bounds__(512) unfold_small_kernel(const __half *__restr
     const bool live = r < m_sub && m < M;
     float v[4];
     load_x4(x, live ? M : 0, K, m, kb * kKBlock + lane * 4, v);     // a dead row slot reads zeros
-    const float am = group_absmax(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))), lpg);
+    float am = group_absmax(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))), lpg);
+    if (row_amax != nullptr) am = live ? row_amax[m] : 0.0f;       // per channel: the whole row's maximum
     float a1[4], a2[4], a3[4];
     msd_unfold4(v, am, a1, a2, a3);
     // plane sums of a lane (each in [-28, 28]): planes 1 and 2 packed in one word so one reduction serves both

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cstdint>
 #include <mutex>
@@ -32,23 +33,32 @@ struct DeviceInfo {
 std::mutex g_mutex;
 DeviceInfo g_devices[kMaxDevices];
 
+// G is the group size the kernels work with. Per-channel quantization (the caller's G = K, one group of all K, above
+// 128) runs as sub-groups of 128, 64 or 32 k with each row's A_max and the one scale (zero-point) row: the integer
+// products and the combine are linear, so the sum over the sub-groups is the per-channel result.
 struct Shape {
     int64_t M, K, N, G;
+    bool pc = false;
 };
 
-// Device pointers of one product; zp and bias may be null.
+// Device pointers of one product; zp and bias may be null. row_amax: per-channel A_max (else null);
+// group_stride: elements between the scale rows of consecutive groups as the decode kernel reads them.
 struct Operands {
     const void *x, *w, *scale, *zp, *bias;
     void *y;
+    const float *row_amax = nullptr;
+    int group_stride = 0;
 };
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+bool group_size_ok(int64_t G) { return G == 32 || G == 64 || G == 128; }
+
 wqbmm_status check_kng(int64_t K, int64_t N, int64_t G) {
     if (K < 1 || N < 1 || K > INT_MAX || N > INT_MAX) return WQBMM_ERR_INVALID;
-    if (G != 32 && G != 64 && G != 128) return WQBMM_ERR_INVALID;
+    if (!group_size_ok(G) && !(G == K && K % 32 == 0)) return WQBMM_ERR_INVALID;     // groups, or per channel
     if (K % G != 0 || N % 8 != 0) return WQBMM_ERR_INVALID;
     if (ceil_div(K, kKBlock) > 65535) return WQBMM_ERR_INVALID;    // prepack grid.y
     return WQBMM_OK;
@@ -60,6 +70,16 @@ wqbmm_status check_shape(const Shape &s) {
     if (s.M < 1 || s.M > INT_MAX) return WQBMM_ERR_INVALID;
     if (s.M > (INT64_C(1) << 62) / s.N || s.M > (INT64_C(1) << 62) / s.K) return WQBMM_ERR_INVALID;
     return WQBMM_OK;
+}
+
+// The kernels' view of the caller's (M, K, N, G), after check_shape succeeded.
+Shape kernel_shape(int64_t M, int64_t K, int64_t N, int64_t G) {
+    Shape s{M, K, N, G};
+    if (!group_size_ok(G)) {                            // G = K: per channel
+        s.pc = true;
+        s.G = K % 128 == 0 ? 128 : (K % 64 == 0 ? 64 : 32);
+    }
+    return s;
 }
 
 constexpr int64_t kLargeM = 64;     // from this many rows on: the pre-pass and the 128 x 128 tile GEMM (large-M path)
@@ -131,7 +151,7 @@ size_t small_consts_bytes(const Shape &s, const Plan &p) {
     return static_cast<size_t>(p.m_tiles) * (s.K / s.G) * kConstFloatsPerGroup * sizeof(float);
 }
 
-size_t workspace_for(const Shape &s, const Plan &p) {
+size_t path_workspace(const Shape &s, const Plan &p) {
     if (p.gemv) return align256(gemv_planes_bytes(s, p)) + align256(static_cast<size_t>(s.M) * (s.K / s.G) * 16);
     if (p.large) return align256(planes_bytes(p)) + align256(consts_bytes(s, p));
     const size_t unfolded = align256(small_planes_bytes(p)) + align256(small_consts_bytes(s, p));
@@ -139,6 +159,16 @@ size_t workspace_for(const Shape &s, const Plan &p) {
     return unfolded + align256(static_cast<size_t>(p.splits) * s.M * s.N * sizeof(float)) +
            align256(static_cast<size_t>(p.m_tiles) * p.n_tiles * sizeof(uint32_t));
 }
+
+// Per channel, after the path's own workspace: the rows' A_max (float [M]) and, for the paths that load scales as
+// tiles, the scale and zero-point rows repeated once per sub-group (fp16 [K/G, N] each).
+size_t scale_rep_bytes(const Shape &s) { return align256(static_cast<size_t>(s.K / s.G) * s.N * 2); }
+size_t per_channel_workspace(const Shape &s, const Plan &p) {
+    if (!s.pc) return 0;
+    return align256(static_cast<size_t>(s.M) * sizeof(float)) + (p.gemv ? 0 : 2 * scale_rep_bytes(s));
+}
+
+size_t workspace_for(const Shape &s, const Plan &p) { return path_workspace(s, p) + per_channel_workspace(s, p); }
 
 // ------------------------------------------------------------------------------------------------ tensor maps
 
@@ -256,8 +286,8 @@ wqbmm_status launch_small_zp(const RunParams &rp, const Plan &plan, DeviceInfo *
 
 // Small-M path: the unfold pre-pass writes the planes images and constants into the workspace, then the tensor-core
 // kernel runs under programmatic launch.
-wqbmm_status launch_small(const void *x, const RunParams &rp, const Plan &plan, DeviceInfo *info,
-                          cudaStream_t stream) {
+wqbmm_status launch_small(const void *x, const float *row_amax, const RunParams &rp, const Plan &plan,
+                          DeviceInfo *info, cudaStream_t stream) {
     if (plan.m_tiles > 65535 || plan.splits > 65535) return WQBMM_ERR_INVALID;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -269,8 +299,8 @@ wqbmm_status launch_small(const void *x, const RunParams &rp, const Plan &plan, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, unfold_small_kernel, static_cast<const __half *>(x), rp.M, rp.K, rp.G, plan.kb_total,
-                           plan.m_sub, plan.nmma, const_cast<uint8_t *>(rp.planes),
-                           const_cast<float *>(rp.consts)) != cudaSuccess)
+                           plan.m_sub, plan.nmma, const_cast<uint8_t *>(rp.planes), const_cast<float *>(rp.consts),
+                           row_amax) != cudaSuccess)
         return WQBMM_ERR_CUDA;
     // debug runs read no zero points (they expose the integer partials of the plain weights)
     return rp.zp != nullptr && rp.dbg_group < 0 ? launch_small_zp<true>(rp, plan, info, stream)
@@ -302,7 +332,7 @@ wqbmm_status launch_large(const Shape &s, const Plan &plan, const Operands &op, 
     const dim3 ugrid(static_cast<unsigned>(plan.m_tiles * kGemmTileM / 8), static_cast<unsigned>(plan.kb_total));
     unfold_planes_kernel<<<ugrid, 256, 0, stream>>>(static_cast<const __half *>(op.x), static_cast<int>(s.M),
                                                     static_cast<int>(s.K), static_cast<int>(s.G), plan.kb_total,
-                                                    planes, consts, dbg_group >= 0 ? 1 : 0);
+                                                    planes, consts, dbg_group >= 0 ? 1 : 0, op.row_amax);
     if (cudaPeekAtLastError() != cudaSuccess) return WQBMM_ERR_CUDA;
     CUtensorMap tmap_s{}, tmap_z{};
     if (!dbg && !fp16_tensor_map(&tmap_s, op.scale, s.K / s.G, s.N, static_cast<int>(kKBlock / s.G), kGemmTileN))
@@ -375,12 +405,13 @@ wqbmm_status launch_gemv(const Shape &s, const Plan &plan, const Operands &op, v
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, gemv_unfold_kernel, static_cast<const __half *>(op.x), static_cast<int>(s.M),
                            static_cast<int>(s.K), static_cast<int>(s.G), plan.kb_total, planes, consts,
-                           dbg_group >= 0 ? 1 : 0) != cudaSuccess)
+                           dbg_group >= 0 ? 1 : 0, op.row_amax) != cudaSuccess)
         return WQBMM_ERR_CUDA;
     GemvParams gp{};
     gp.w = static_cast<const uint8_t *>(op.w);
     gp.scale = static_cast<const __half *>(op.scale);
     gp.zp = static_cast<const __half *>(op.zp);
+    gp.group_stride = op.group_stride;
     gp.bias = static_cast<const __half *>(op.bias);
     gp.planes = planes;
     gp.consts = consts;
@@ -414,8 +445,51 @@ wqbmm_status launch_gemv(const Shape &s, const Plan &plan, const Operands &op, v
 
 // Launches one product (or, with dbg_group >= 0, the integer partials of one group) planned by `plan` on the current
 // device. `workspace` holds workspace_for(shape, plan) bytes; `clear_counters` clears the split-K counters first.
-wqbmm_status dispatch(const Operands &op, const Shape &s, const Plan &plan, void *workspace, bool clear_counters,
+// Per channel: each row's A_max and (for the paths that load scale tiles) the repeated scale and zero-point rows,
+// into the workspace after the path's own part, by one kernel under programmatic launch.
+wqbmm_status per_channel_prep(const Shape &s, const Plan &plan, Operands *op, void *workspace, cudaStream_t stream) {
+    uint8_t *base = static_cast<uint8_t *>(workspace) + path_workspace(s, plan);
+    float *row_amax = reinterpret_cast<float *>(base);
+    __half *scale_rep = nullptr, *zp_rep = nullptr;
+    if (!plan.gemv) {
+        scale_rep = reinterpret_cast<__half *>(base + align256(static_cast<size_t>(s.M) * sizeof(float)));
+        if (op->zp != nullptr) zp_rep = reinterpret_cast<__half *>(reinterpret_cast<uint8_t *>(scale_rep) +
+                                                                   scale_rep_bytes(s));
+    }
+    const int reps = static_cast<int>(s.K / s.G);
+    const int copy_blocks = plan.gemv ? 0 : static_cast<int>(std::min<int64_t>(ceil_div(int64_t(reps) * s.N, 256), 1024));
+    if (s.M + copy_blocks > INT_MAX) return WQBMM_ERR_INVALID;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(s.M + copy_blocks), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, per_channel_prep_kernel, static_cast<const __half *>(op->x), static_cast<int>(s.M),
+                           static_cast<int>(s.K), row_amax, static_cast<const __half *>(op->scale),
+                           static_cast<const __half *>(op->zp), static_cast<int>(s.N), reps, scale_rep,
+                           zp_rep) != cudaSuccess)
+        return WQBMM_ERR_CUDA;
+    op->row_amax = row_amax;
+    if (!plan.gemv) {
+        op->scale = scale_rep;
+        if (op->zp != nullptr) op->zp = zp_rep;
+    }
+    op->group_stride = 0;                               // the decode kernel reads the one scale row for every group
+    return WQBMM_OK;
+}
+
+wqbmm_status dispatch(const Operands &op_in, const Shape &s, const Plan &plan, void *workspace, bool clear_counters,
                       int dbg_group, int32_t *dbg_y123, DeviceInfo *info, cudaStream_t stream) {
+    Operands op = op_in;
+    op.group_stride = static_cast<int>(s.N);
+    if (s.pc) {
+        const wqbmm_status st = per_channel_prep(s, plan, &op, workspace, stream);
+        if (st != WQBMM_OK) return st;
+    }
     if (plan.gemv) return launch_gemv(s, plan, op, workspace, dbg_group, dbg_y123, info, stream);
     if (plan.large) return launch_large(s, plan, op, workspace, dbg_group, dbg_y123, info, stream);
     RunParams rp{};
@@ -449,7 +523,7 @@ wqbmm_status dispatch(const Operands &op, const Shape &s, const Plan &plan, void
     rp.kb_total = plan.kb_total;
     rp.reduce = plan.reduce;
     rp.dbg_group = dbg_group;
-    return launch_small(op.x, rp, plan, info, stream);
+    return launch_small(op.x, op.row_amax, rp, plan, info, stream);
 }
 
 // Scratch for wqbmm_run_static_scratch: a fixed device array instead of a caller workspace. Host code must not
@@ -532,9 +606,9 @@ wqbmm_status wqbmm_prepack_weight_nk(const uint8_t *w_packed_nk, void *w_prepack
 
 wqbmm_status wqbmm_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t G, size_t *bytes) {
     if (!bytes) return WQBMM_ERR_NULLPTR;
-    const Shape s{M, K, N, G};
-    const wqbmm_status st = check_shape(s);
+    const wqbmm_status st = check_shape(Shape{M, K, N, G});
     if (st != WQBMM_OK) return st;
+    const Shape s = kernel_shape(M, K, N, G);
     *bytes = workspace_for(s, make_plan(s, kPlanSms));
     return WQBMM_OK;
 }
@@ -550,9 +624,9 @@ wqbmm_status wqbmm_run_ex(const void *x, const void *w_prepacked, const void *an
                           const void *zero_point, const void *bias, void *y, int64_t M, int64_t K, int64_t N,
                           int64_t G, void *workspace, size_t workspace_bytes, wqbmm_stream_t stream) {
     if (!x || !w_prepacked || !antiquant_scale || !y) return WQBMM_ERR_NULLPTR;
-    const Shape s{M, K, N, G};
-    wqbmm_status st = check_shape(s);
+    wqbmm_status st = check_shape(Shape{M, K, N, G});
     if (st != WQBMM_OK) return st;
+    const Shape s = kernel_shape(M, K, N, G);
     if (!aligned16(x) || !aligned16(w_prepacked) || !aligned16(antiquant_scale) || !aligned16(y) ||
         !aligned16(zero_point) || !aligned16(bias))
         return WQBMM_ERR_INVALID;
@@ -571,9 +645,9 @@ wqbmm_status wqbmm_run_ex(const void *x, const void *w_prepacked, const void *an
 wqbmm_status wqbmm_run_static_scratch(const void *x, const void *w_prepacked, const void *antiquant_scale, void *y,
                                       int64_t M, int64_t K, int64_t N, int64_t G, wqbmm_stream_t stream) {
     if (!x || !w_prepacked || !antiquant_scale || !y) return WQBMM_ERR_NULLPTR;
-    const Shape s{M, K, N, G};
-    wqbmm_status st = check_shape(s);
+    wqbmm_status st = check_shape(Shape{M, K, N, G});
     if (st != WQBMM_OK) return st;
+    const Shape s = kernel_shape(M, K, N, G);
     if (!aligned16(x) || !aligned16(w_prepacked) || !aligned16(antiquant_scale) || !aligned16(y))
         return WQBMM_ERR_INVALID;
     int dev;
@@ -592,17 +666,27 @@ wqbmm_status wqbmm_run_static_scratch(const void *x, const void *w_prepacked, co
 wqbmm_status wqbmm_debug_unfold(const void *x, int64_t M, int64_t K, int64_t G, int8_t *planes, float *amax,
                                 wqbmm_stream_t stream) {
     if (!x || !planes || !amax) return WQBMM_ERR_NULLPTR;
-    const Shape s{M, K, 8, G};
-    wqbmm_status st = check_shape(s);
+    wqbmm_status st = check_shape(Shape{M, K, 8, G});
     if (st != WQBMM_OK) return st;
+    const Shape s = kernel_shape(M, K, 8, G);
     if (!aligned16(x)) return WQBMM_ERR_INVALID;
     int dev;
     DeviceInfo *info;
     if ((st = current_device(&dev, &info)) != WQBMM_OK) return st;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (s.pc) {
+        // per channel: amax receives each row's A_max (one group per row), which the unfold then reads
+        per_channel_prep_kernel<<<static_cast<unsigned>(M), 256, 0, cs>>>(static_cast<const __half *>(x),
+                                                                          static_cast<int>(M), static_cast<int>(K),
+                                                                          amax, nullptr, nullptr, 8, 0, nullptr,
+                                                                          nullptr);
+        if (cudaPeekAtLastError() != cudaSuccess) return WQBMM_ERR_CUDA;
+    }
     constexpr int kWarps = 4;
     const dim3 grid(static_cast<unsigned>(M), static_cast<unsigned>(ceil_div(ceil_div(K, kKBlock), kWarps)));
-    unfold_debug_kernel<<<grid, kWarps * 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const __half *>(x), static_cast<int>(M), static_cast<int>(K), static_cast<int>(G), planes, amax);
+    unfold_debug_kernel<<<grid, kWarps * 32, 0, cs>>>(static_cast<const __half *>(x), static_cast<int>(M),
+                                                      static_cast<int>(K), static_cast<int>(s.G), planes,
+                                                      s.pc ? nullptr : amax, s.pc ? amax : nullptr);
     return cudaPeekAtLastError() == cudaSuccess ? WQBMM_OK : WQBMM_ERR_CUDA;
 }
 
@@ -613,6 +697,7 @@ wqbmm_status wqbmm_debug_group_partials(const void *x, const void *w_prepacked, 
     const Shape s{M, K, N, G};
     wqbmm_status st = check_shape(s);
     if (st != WQBMM_OK) return st;
+    if (!group_size_ok(G)) return WQBMM_ERR_INVALID;     // per channel (G = K > 128): not exposed
     if (g < 0 || g >= K / G) return WQBMM_ERR_INVALID;
     if (!aligned16(x) || !aligned16(w_prepacked)) return WQBMM_ERR_INVALID;
     if (workspace && !aligned16(workspace)) return WQBMM_ERR_INVALID;
