@@ -150,6 +150,23 @@ WQBMM_API wqbmm_status wqbmm_run_ex(const void *x, const void *w_prepacked, cons
                                     wqbmm_stream_t stream);
 
 /*
+ * A batch of products with shared weights (the operator's batched x, BatchMatmul with one weight): for b in
+ * [0, batch), y_b = MSD matmul of x_b with the weights, x_b = x + b * x_batch_stride (fp16 [M, K], row stride K) and
+ * y_b = y + b * y_batch_stride (fp16 [M, N], row stride N); strides count elements. Rows are independent, so when
+ * the batches are contiguous (x_batch_stride == M * K and y_batch_stride == M * N) this is one product of batch * M
+ * rows; otherwise one product per batch item is enqueued on `stream`, all using the same workspace one after the
+ * other. The workspace must hold wqbmm_workspace_bytes(batch * M, K, N, G) bytes when contiguous, else
+ * wqbmm_workspace_bytes(M, K, N, G). zero_point and bias as for wqbmm_run_ex (may be null).
+ * Errors as for wqbmm_run_ex; also INVALID for batch < 1, a stride smaller than one item, a stride that breaks the
+ * 16-byte alignment of x_b or y_b, or a batch whose rows overflow the shape rules.
+ */
+WQBMM_API wqbmm_status wqbmm_run_batched(const void *x, const void *w_prepacked, const void *antiquant_scale,
+                                         const void *zero_point, const void *bias, void *y, int64_t batch,
+                                         int64_t M, int64_t K, int64_t N, int64_t G, int64_t x_batch_stride,
+                                         int64_t y_batch_stride, void *workspace, size_t workspace_bytes,
+                                         wqbmm_stream_t stream);
+
+/*
  * Exposes steps 1-8 exactly as the run kernel computes them (for bit-exact checks).
  *   x       device, fp16 [M, K]
  *   planes  device, int8 [3, M, K]: plane i of row m at planes[(i * M + m) * K + k], values in [-7, 7]

@@ -146,6 +146,17 @@ CASES = [
     ("run_ex_misaligned_bias",
      lambda L: L.wqbmm_run_ex(A, A, A, None, MIS, A, 200, 128, 128, 128, A, 1 << 20, None), INVALID),
     ("run_ex_bad_group", lambda L: L.wqbmm_run_ex(A, A, A, A, A, A, 8, 128, 128, 16, A, 1 << 20, None), INVALID),
+    ("batched_zero_batch",
+     lambda L: L.wqbmm_run_batched(A, A, A, None, None, A, 0, 2, 128, 128, 128, 256, 256, A, 1 << 20, None), INVALID),
+    ("batched_x_stride_too_small",
+     lambda L: L.wqbmm_run_batched(A, A, A, None, None, A, 2, 2, 128, 128, 128, 200, 256, A, 1 << 20, None), INVALID),
+    ("batched_y_stride_unaligned",
+     lambda L: L.wqbmm_run_batched(A, A, A, None, None, A, 2, 2, 128, 128, 128, 256, 260, A, 1 << 20, None), INVALID),
+    ("batched_null_x",
+     lambda L: L.wqbmm_run_batched(None, A, A, None, None, A, 2, 2, 128, 128, 128, 256, 256, A, 1 << 20, None),
+     NULLPTR),
+    ("batched_bad_group",
+     lambda L: L.wqbmm_run_batched(A, A, A, None, None, A, 2, 2, 192, 128, 96, 512, 512, A, 1 << 20, None), INVALID),
     ("run_per_channel_k_not_multiple_of_32",
      lambda L: L.wqbmm_run(A, A, A, A, 1, 100, 128, 100, A, 1 << 20, None), INVALID),
     ("run_group_larger_than_128_not_k", lambda L: L.wqbmm_run(A, A, A, A, 1, 512, 128, 256, A, 1 << 20, None),
@@ -194,3 +205,7 @@ def test_no_device_is_a_cuda_error(lib):
     assert lib.wqbmm_run(A, A, A, A, 2048, 8192, 28672, 64, A, 1 << 30, None) == wq.ERR_CUDA
     assert lib.wqbmm_run_ex(A, A, A, A, A, A, 8, 4096, 11008, 128, A, 1 << 30, None) == wq.ERR_CUDA
     assert lib.wqbmm_run_ex(A, A, A, None, None, A, 1, 4096, 4096, 128, A, 1 << 30, None) == wq.ERR_CUDA
+    assert lib.wqbmm_run_batched(A, A, A, None, None, A, 4, 2, 4096, 4096, 128, 8192, 8192, A, 1 << 30,
+                                 None) == wq.ERR_CUDA
+    assert lib.wqbmm_run_batched(A, A, A, None, None, A, 4, 2, 4096, 4096, 128, 9216, 8192, A, 1 << 30,
+                                 None) == wq.ERR_CUDA

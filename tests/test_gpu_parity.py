@@ -495,3 +495,47 @@ def test_unfold_bit_exact_per_channel(dev, M, K):
     p_ref, a_ref = oracle.unfold(x, K, oracle.MODE_F)
     np.testing.assert_array_equal(amax.cpu().numpy(), a_ref.astype(np.float32))
     np.testing.assert_array_equal(planes.cpu().numpy(), p_ref)
+
+
+# ------------------------------------------------------------------------------------------- batched x, shared weights
+
+@pytest.mark.parametrize("B,M,K,N,G", [(3, 5, 1024, 264, 64), (2, 1, 4096, 520, 128), (4, 40, 512, 256, 128)])
+def test_batched_x_matches_oracle(dev, B, M, K, N, G):
+    """x [B, M, K] with one weight: the binding folds the batch into rows; the oracle sees the same rows."""
+    wl = I.small_case(B * M, K, N, G, seed=B * 100 + M)
+    x, wp, sc = I.make_inputs(wl)
+    w_pre = wq.prepack_weight(to_dev(wp, dev), K, N, G)
+    y = wq.msd_matmul(to_dev(x.reshape(B, M, K), dev), w_pre, to_dev(sc, dev), G)
+    assert tuple(y.shape) == (B, M, N)
+    ref = oracle.msd_matmul(x, wp, sc, G, mode=oracle.MODE_D).reshape(B, M, N)
+    assert_within_tolerance(y.cpu().numpy(), ref, "batched")
+
+
+@pytest.mark.parametrize("B,M,K,N,G", [(3, 5, 1024, 264, 64), (2, 70, 256, 128, 128)])
+def test_batched_strided_matches_oracle(dev, B, M, K, N, G):
+    """Batches with gaps between them (x padded by 2 rows, y by 1 row per item): each item is its own product, the
+    gaps of y stay untouched; the contiguous form of the same batch equals one product of B * M rows bit for bit."""
+    wl = I.small_case(B * M, K, N, G, seed=B * 7 + M)
+    x, wp, sc = I.make_inputs(wl)
+    zp, bias = I.make_zero_point(wl, "frac"), I.make_bias(wl)
+    w_pre = wq.prepack_weight(to_dev(wp, dev), K, N, G)
+    xpad = np.zeros((B, M + 2, K), dtype=np.float16)
+    xpad[:, :M] = x.reshape(B, M, K)
+    xd = to_dev(xpad, dev)
+    y = torch.full((B, M + 1, N), 3.0, dtype=torch.float16, device=dev)
+    ws = wq.allocate_workspace(M, K, N, G, dev)
+    wq.wqbmm_run_batched(xd, w_pre, to_dev(sc, dev), to_dev(zp, dev), to_dev(bias, dev), y, B, M, K, N, G,
+                         (M + 2) * K, (M + 1) * N, ws)
+    got = y.cpu().numpy()
+    assert (got[:, M] == 3.0).all()
+    for b in range(B):
+        ref = oracle.msd_matmul_ex(x[b * M:(b + 1) * M], wp, sc, G, zero_point=zp, bias=bias, mode=oracle.MODE_D)
+        assert_within_tolerance(got[b, :M], ref, f"item {b}")
+    # contiguous: one product of B * M rows
+    xc = to_dev(x, dev)
+    yc = torch.empty((B * M, N), dtype=torch.float16, device=dev)
+    yo = torch.empty((B * M, N), dtype=torch.float16, device=dev)
+    wsc = wq.allocate_workspace(B * M, K, N, G, dev)
+    wq.wqbmm_run_batched(xc, w_pre, to_dev(sc, dev), None, None, yc, B, M, K, N, G, M * K, M * N, wsc)
+    wq.wqbmm_run(xc, w_pre, to_dev(sc, dev), yo, B * M, K, N, G, wsc)
+    np.testing.assert_array_equal(yc.cpu().numpy().view(np.uint16), yo.cpu().numpy().view(np.uint16))

@@ -16,7 +16,7 @@ __all__ = [
     "wqbmm_workspace_bytes", "wqbmm_run", "wqbmm_debug_unfold", "wqbmm_debug_group_partials",
     "wqbmm_read_device_status", "wqbmm_debug_wait_timeout", "wqbmm_status_string", "prepack_weight",
     "allocate_workspace", "msd_matmul", "SYMBOLS", "wqbmm_run_static_scratch", "wqbmm_prepack_weight_nk",
-    "prepack_weight_nk", "wqbmm_run_ex",
+    "prepack_weight_nk", "wqbmm_run_ex", "wqbmm_run_batched",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -31,6 +31,7 @@ SYMBOLS = (
     "wqbmm_prepacked_weight_bytes", "wqbmm_prepack_weight", "wqbmm_workspace_bytes", "wqbmm_run",
     "wqbmm_debug_unfold", "wqbmm_debug_group_partials", "wqbmm_read_device_status", "wqbmm_debug_wait_timeout",
     "wqbmm_status_string", "wqbmm_run_static_scratch", "wqbmm_prepack_weight_nk", "wqbmm_run_ex",
+    "wqbmm_run_batched",
 )
 
 
@@ -61,6 +62,7 @@ def load_library():
                 "wqbmm_workspace_bytes": [i64, i64, i64, i64, ctypes.POINTER(sz)],
                 "wqbmm_run": [p, p, p, p, i64, i64, i64, i64, p, sz, p],
                 "wqbmm_run_ex": [p, p, p, p, p, p, i64, i64, i64, i64, p, sz, p],
+                "wqbmm_run_batched": [p, p, p, p, p, p, i64, i64, i64, i64, i64, i64, i64, p, sz, p],
                 "wqbmm_debug_unfold": [p, i64, i64, i64, p, p, p],
                 "wqbmm_debug_group_partials": [p, p, i64, i64, i64, i64, i64, p, p, sz, p],
                 "wqbmm_read_device_status": [ctypes.POINTER(ctypes.c_int32), ctypes.c_int, p],
@@ -143,6 +145,16 @@ def wqbmm_run_ex(x, w_prepacked, antiquant_scale, zero_point, bias, y, M: int, K
                                         _stream(stream)), "wqbmm_run_ex")
 
 
+def wqbmm_run_batched(x, w_prepacked, antiquant_scale, zero_point, bias, y, batch: int, M: int, K: int, N: int,
+                      G: int, x_batch_stride: int, y_batch_stride: int, workspace=None,
+                      workspace_bytes: int | None = None, stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().wqbmm_run_batched(_ptr(x), _ptr(w_prepacked), _ptr(antiquant_scale), _ptr(zero_point),
+                                             _ptr(bias), _ptr(y), batch, M, K, N, G, x_batch_stride, y_batch_stride,
+                                             _ptr(workspace), workspace_bytes, _stream(stream)), "wqbmm_run_batched")
+
+
 def wqbmm_run_static_scratch(x, w_prepacked, antiquant_scale, y, M: int, K: int, N: int, G: int,
                              stream=None) -> None:
     """wqbmm_run without a caller workspace: the library's fixed 2 MiB device scratch is used instead (for callers
@@ -206,13 +218,20 @@ def allocate_workspace(M: int, K: int, N: int, G: int, device):
 
 def msd_matmul(x, w_prepacked, antiquant_scale, G: int, y=None, workspace=None, stream=None, zero_point=None,
                bias=None):
-    """y [M, N] fp16 = MSD matmul of x [M, K] fp16 with prepacked int4 weights and antiquant_scale [K/G, N] fp16;
-    optionally with zero points [K/G, N] fp16 (weights (w - zp) * scale) and a bias [N] fp16."""
+    """y [..., N] fp16 = MSD matmul of x [..., K] fp16 (any leading batch dimensions, contiguous) with prepacked int4
+    weights and antiquant_scale [K/G, N] fp16 (G = K: per channel, [1, N]); optionally with zero points [K/G, N] fp16
+    (weights (w - zp) * scale) and a bias [N] fp16."""
     import torch
-    M, K = x.shape
+    lead = tuple(x.shape[:-1])
+    K = x.shape[-1]
+    M = 1
+    for d in lead:
+        M *= d
     N = antiquant_scale.shape[1]
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
     if y is None:
-        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+        y = torch.empty(lead + (N,), dtype=torch.float16, device=x.device)
     if workspace is None:
         workspace = allocate_workspace(M, K, N, G, x.device)
     if zero_point is None and bias is None:

@@ -642,6 +642,34 @@ wqbmm_status wqbmm_run_ex(const void *x, const void *w_prepacked, const void *an
     return dispatch(op, s, plan, workspace, false, -1, nullptr, info, reinterpret_cast<cudaStream_t>(stream));
 }
 
+wqbmm_status wqbmm_run_batched(const void *x, const void *w_prepacked, const void *antiquant_scale,
+                               const void *zero_point, const void *bias, void *y, int64_t batch, int64_t M,
+                               int64_t K, int64_t N, int64_t G, int64_t x_batch_stride, int64_t y_batch_stride,
+                               void *workspace, size_t workspace_bytes, wqbmm_stream_t stream) {
+    if (!x || !w_prepacked || !antiquant_scale || !y) return WQBMM_ERR_NULLPTR;
+    if (batch < 1 || M < 1 || K < 1 || N < 1) return WQBMM_ERR_INVALID;
+    if (M > INT64_MAX / K || M > INT64_MAX / N) return WQBMM_ERR_INVALID;
+    if (x_batch_stride < M * K || y_batch_stride < M * N) return WQBMM_ERR_INVALID;
+    if (x_batch_stride % 8 != 0 || y_batch_stride % 8 != 0) return WQBMM_ERR_INVALID;   // 16-byte alignment
+    if (x_batch_stride == M * K && y_batch_stride == M * N) {
+        if (M > INT64_MAX / batch) return WQBMM_ERR_INVALID;
+        return wqbmm_run_ex(x, w_prepacked, antiquant_scale, zero_point, bias, y, batch * M, K, N, G, workspace,
+                            workspace_bytes, stream);
+    }
+    if (batch - 1 > INT64_MAX / x_batch_stride / 2 || batch - 1 > INT64_MAX / y_batch_stride / 2)
+        return WQBMM_ERR_INVALID;
+    // validate the shape once before enqueuing anything
+    wqbmm_status st = check_shape(Shape{M, K, N, G});
+    if (st != WQBMM_OK) return st;
+    for (int64_t b = 0; b < batch; ++b) {
+        st = wqbmm_run_ex(static_cast<const __half *>(x) + b * x_batch_stride, w_prepacked, antiquant_scale,
+                          zero_point, bias, static_cast<__half *>(y) + b * y_batch_stride, M, K, N, G, workspace,
+                          workspace_bytes, stream);
+        if (st != WQBMM_OK) return st;
+    }
+    return WQBMM_OK;
+}
+
 wqbmm_status wqbmm_run_static_scratch(const void *x, const void *w_prepacked, const void *antiquant_scale, void *y,
                                       int64_t M, int64_t K, int64_t N, int64_t G, wqbmm_stream_t stream) {
     if (!x || !w_prepacked || !antiquant_scale || !y) return WQBMM_ERR_NULLPTR;
