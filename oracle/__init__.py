@@ -48,8 +48,11 @@ def _bind(path: str):
     lib.oracle_direct_rows.argtypes = [p, p, p, i64, i64, i64, i64, p, i64, p]
     lib.oracle_msd_rows_ex.argtypes = [p, p, p, p, p, i64, i64, i64, i64, ctypes.c_int, p, i64, p]
     lib.oracle_direct_rows_ex.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, i64, p]
+    lib.oracle_msd_rows_w8.argtypes = [p, p, p, p, p, i64, i64, i64, i64, ctypes.c_int, p, i64, p]
+    lib.oracle_direct_rows_w8.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, i64, p]
     for f in ("oracle_decode_int4", "oracle_unfold", "oracle_group_partials", "oracle_msd_rows",
-              "oracle_direct_rows"):
+              "oracle_direct_rows", "oracle_msd_rows_ex", "oracle_direct_rows_ex", "oracle_msd_rows_w8",
+              "oracle_direct_rows_w8"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -179,6 +182,42 @@ class Oracle:
                                                  M, K, N, G, _ptr(r), len(r), _ptr(out)), "direct_matmul_ex")
         return out
 
+    def msd_matmul_w8(self, x: np.ndarray, w8: np.ndarray, scale: np.ndarray, G: int, zero_point=None, bias=None,
+                      mode: int = MODE_D, rows=None):
+        """Steps 1-11 with int8 weights w8 [K, N] (and optional zero points / bias): float64 [len(rows), N]."""
+        xb = _as_half_bits(x)
+        sb = _as_half_bits(scale)
+        zb = None if zero_point is None else _as_half_bits(zero_point)
+        bb = None if bias is None else _as_half_bits(np.asarray(bias).reshape(-1))
+        M, K = xb.shape
+        N = sb.shape[1]
+        w8 = np.ascontiguousarray(w8, dtype=np.int8)
+        assert w8.shape == (K, N)
+        r = _rows(M, rows)
+        out = np.empty((len(r), N), dtype=np.float64)
+        _check(self._lib().oracle_msd_rows_w8(_ptr(xb), _ptr(w8), _ptr(sb), None if zb is None else _ptr(zb),
+                                              None if bb is None else _ptr(bb), M, K, N, G, mode, _ptr(r), len(r),
+                                              _ptr(out)), "msd_matmul_w8")
+        return out
+
+    def direct_matmul_w8(self, x: np.ndarray, w8: np.ndarray, scale: np.ndarray, G: int, zero_point=None,
+                         bias=None, rows=None):
+        """x . ((w8 - zp) * scale) + bias in binary64: float64 [len(rows), N]."""
+        xb = _as_half_bits(x)
+        sb = _as_half_bits(scale)
+        zb = None if zero_point is None else _as_half_bits(zero_point)
+        bb = None if bias is None else _as_half_bits(np.asarray(bias).reshape(-1))
+        M, K = xb.shape
+        N = sb.shape[1]
+        w8 = np.ascontiguousarray(w8, dtype=np.int8)
+        assert w8.shape == (K, N)
+        r = _rows(M, rows)
+        out = np.empty((len(r), N), dtype=np.float64)
+        _check(self._lib().oracle_direct_rows_w8(_ptr(xb), _ptr(w8), _ptr(sb), None if zb is None else _ptr(zb),
+                                                 None if bb is None else _ptr(bb), M, K, N, G, _ptr(r), len(r),
+                                                 _ptr(out)), "direct_matmul_w8")
+        return out
+
     def direct_matmul(self, x: np.ndarray, w_packed: np.ndarray, scale: np.ndarray, G: int, rows=None):
         """x . (w * scale) in binary64: float64 [len(rows), N]."""
         xb = _as_half_bits(x)
@@ -212,3 +251,5 @@ msd_matmul = _default.msd_matmul
 direct_matmul = _default.direct_matmul
 msd_matmul_ex = _default.msd_matmul_ex
 direct_matmul_ex = _default.direct_matmul_ex
+msd_matmul_w8 = _default.msd_matmul_w8
+direct_matmul_w8 = _default.direct_matmul_w8

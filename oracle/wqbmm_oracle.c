@@ -35,6 +35,10 @@
  * stands for (w - zp[g, n]) * scale[g, n], so step 9 becomes Y_i = A_i . (W_g - zp_g) = A_i . W_g - zp_g * S_i with
  * S_i the sum of plane i over the group (the planes do not change), and an optional bias[n] is added to the sum of
  * step 11.
+ *
+ * Int8 weights (W8: the weight dtype INT8 of the page "aclnnCalculateMatmulWeightSizeV2 接口详解", parameter table and
+ * calling example with an INT8 weight of shape {32, 16}): the same steps with w an int8 [K, N] matrix, row-major,
+ * in [-128, 127]; step 9 is then bounded by 7 * 128 * G.
  */
 #include <math.h>
 #include <stdint.h>
@@ -435,5 +439,100 @@ int oracle_direct_rows_ex(const uint16_t *x, const uint8_t *w_packed, const uint
                 yr[n] += oracle_half_to_double(bias[n]);
     }
     free(w);
+    return ORACLE_OK;
+}
+
+/*
+ * Steps 1-11 with int8 weights [K, N] (row-major), optional zero points and bias, for selected rows:
+ * y[r * N + n] (binary64). Same steps as oracle_msd_rows_ex; only step 9 reads int8 weights.
+ */
+int oracle_msd_rows_w8(const uint16_t *x, const int8_t *w8, const uint16_t *scale, const uint16_t *zp,
+                       const uint16_t *bias, int64_t M, int64_t K, int64_t N, int64_t G, int mode,
+                       const int64_t *rows, int64_t nrows, double *y)
+{
+    if (!x || !w8 || !scale || !rows || !y || N <= 0 || nrows <= 0)
+        return ORACLE_EINVAL;
+    int rc = check_shape(M, K, G, mode);
+    if (rc)
+        return rc;
+    if (G > (int64_t)(INT32_MAX / 896))             /* |Y_i| <= 7 * 128 * G */
+        return ORACLE_ERANGE;
+    int64_t Gn = K / G;
+    int8_t *a = (int8_t *)malloc((size_t)(3 * G));
+    int32_t *yi = (int32_t *)malloc((size_t)(3 * N) * sizeof(int32_t));
+    if (!a || !yi) {
+        free(a);
+        free(yi);
+        return ORACLE_ENOMEM;
+    }
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t m = rows[r];
+        if (m < 0 || m >= M) {
+            rc = ORACLE_EINVAL;
+            break;
+        }
+        double *yr = y + r * N;
+        for (int64_t n = 0; n < N; ++n)
+            yr[n] = 0.0;                                             /* Y^0 = 0 */
+        for (int64_t g = 0; g < Gn; ++g) {
+            double amax;
+            unfold_group(x + m * K + g * G, G, mode, &amax, a, a + G, a + 2 * G);   /* steps 1-8 */
+            group_products(a, a + G, a + 2 * G, w8 + g * G * N, G, N, yi, yi + N, yi + 2 * N);  /* step 9 */
+            double s1 = 0.0, s2 = 0.0, s3 = 0.0;                     /* plane sums S_i of the group */
+            for (int64_t k = 0; k < G; ++k) {
+                s1 += a[k];
+                s2 += a[G + k];
+                s3 += a[2 * G + k];
+            }
+            for (int64_t n = 0; n < N; ++n) {
+                double z = zp ? oracle_half_to_double(zp[g * N + n]) : 0.0;
+                double y1 = yi[n] - z * s1, y2 = yi[N + n] - z * s2, y3 = yi[2 * N + n] - z * s3;
+                double ygroup = (y1 / 7.49 + y2 / (7.49 * 14.98) + y3 / (7.49 * 14.98 * 14.98)) * amax
+                                * oracle_half_to_double(scale[g * N + n]);   /* step 10 */
+                yr[n] = ygroup + yr[n];                               /* step 11 */
+            }
+        }
+        if (bias)
+            for (int64_t n = 0; n < N; ++n)
+                yr[n] = yr[n] + oracle_half_to_double(bias[n]);
+    }
+    free(a);
+    free(yi);
+    return rc;
+}
+
+/*
+ * The plain dequantized matmul with int8 weights: y[r, n] = sum_k x[m, k] * (w8[k, n] - zp[k / G, n])
+ * * scale[k / G, n] + bias[n], binary64, for selected rows (zp and bias may be null).
+ */
+int oracle_direct_rows_w8(const uint16_t *x, const int8_t *w8, const uint16_t *scale, const uint16_t *zp,
+                          const uint16_t *bias, int64_t M, int64_t K, int64_t N, int64_t G, const int64_t *rows,
+                          int64_t nrows, double *y)
+{
+    if (!x || !w8 || !scale || !rows || !y || N <= 0 || nrows <= 0)
+        return ORACLE_EINVAL;
+    int rc = check_shape(M, K, G, ORACLE_MODE_D);
+    if (rc)
+        return rc;
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t m = rows[r];
+        if (m < 0 || m >= M)
+            return ORACLE_EINVAL;
+        double *yr = y + r * N;
+        for (int64_t n = 0; n < N; ++n)
+            yr[n] = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double xv = oracle_half_to_double(x[m * K + k]);
+            const int8_t *row = w8 + k * N;
+            int64_t g = k / G;
+            for (int64_t n = 0; n < N; ++n) {
+                double z = zp ? oracle_half_to_double(zp[g * N + n]) : 0.0;
+                yr[n] += xv * ((double)row[n] - z) * oracle_half_to_double(scale[g * N + n]);
+            }
+        }
+        if (bias)
+            for (int64_t n = 0; n < N; ++n)
+                yr[n] += oracle_half_to_double(bias[n]);
+    }
     return ORACLE_OK;
 }

@@ -7,6 +7,7 @@ import pytest
 
 import oracle
 import test_oracle_pins as P
+import test_oracle_w8 as W
 import test_oracle_zp_bias as Z
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "wqbmm_oracle.c")
@@ -36,6 +37,9 @@ MUTATIONS = [
     ("zero point added instead of subtracted", "double y1 = yi[n] - z * s1", "double y1 = yi[n] + z * s1"),
     ("zero point times the wrong plane sum", "s2 += a[G + k];", "s2 += a[k];"),
     ("bias dropped", "yr[n] = yr[n] + oracle_half_to_double(bias[n]);", "yr[n] = yr[n];"),
+    ("int8 weights of the wrong group", "w8 + g * G * N, G, N, yi", "w8 + g * N, G, N, yi"),
+    ("int8 weight read as unsigned", "const int8_t *row = w8 + k * N;",
+     "const uint8_t *row = (const uint8_t *)w8 + k * N;"),
 ]
 
 PINS = [
@@ -52,6 +56,8 @@ PINS = [
     lambda o: P.test_group_and_column_permutation_invariance(o),
     lambda o: Z.test_integer_zero_point_equals_shifted_weights(o, oracle.MODE_D, 1),
     lambda o: Z.test_bias_adds_itself(o),
+    lambda o: W.test_w8_in_int4_range_is_the_int4_path(o, oracle.MODE_D),
+    lambda o: W.test_w8_within_closed_form_bound(o, oracle.MODE_D),
 ]
 
 
