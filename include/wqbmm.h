@@ -150,6 +150,31 @@ WQBMM_API wqbmm_status wqbmm_run_ex(const void *x, const void *w_prepacked, cons
                                     wqbmm_stream_t stream);
 
 /*
+ * Int8 weights (W8; the weight dtype INT8 of the page "aclnnCalculateMatmulWeightSizeV2 接口详解"): the same eleven
+ * steps with w an int8 [K, N] matrix in [-128, 127], optional zero points and bias as for wqbmm_run_ex.
+ * Internally w = 16 hi + lo (hi = w >> 4, lo = w & 15) and every group becomes two int4 groups over the same
+ * planes of x (weights hi with scale 16 s and zero point -1/2; weights lo - 8 with scale s and the caller's zero
+ * point): s (16 (hi + 1/2) + lo - 8 - zp) = s (w - zp) exactly, so the int4 kernels compute the int8 product.
+ * G in {32, 64, 128} only (not per channel); 2K must satisfy the shape rules; |antiquant_scale| < 4096 (16 s is
+ * formed in fp16).
+ *   wqbmm_prepacked_weight_bytes_w8  host only: ceil(N/128) * ceil(2K/128) * 8192 bytes (= K * N, padded)
+ *   wqbmm_prepack_weight_w8          w8: device int8 [K, N] row-major -> prepacked tiles of the split weights
+ *   wqbmm_workspace_bytes_w8         host only: the workspace wqbmm_run_w8 needs (the int4 problem's, plus x
+ *                                    repeated per group [M, 2K] and the split scales and zero points)
+ *   wqbmm_run_w8                     y [M, N] fp16; x, antiquant_scale [K/G, N], zero_point [K/G, N] (or null),
+ *                                    bias [N] (or null) as for wqbmm_run_ex; workspace required
+ * Errors as for wqbmm_prepack_weight / wqbmm_workspace_bytes / wqbmm_run_ex.
+ */
+WQBMM_API wqbmm_status wqbmm_prepacked_weight_bytes_w8(int64_t K, int64_t N, int64_t G, size_t *bytes);
+WQBMM_API wqbmm_status wqbmm_prepack_weight_w8(const int8_t *w8, void *w_prepacked, int64_t K, int64_t N, int64_t G,
+                                               wqbmm_stream_t stream);
+WQBMM_API wqbmm_status wqbmm_workspace_bytes_w8(int64_t M, int64_t K, int64_t N, int64_t G, size_t *bytes);
+WQBMM_API wqbmm_status wqbmm_run_w8(const void *x, const void *w_prepacked, const void *antiquant_scale,
+                                    const void *zero_point, const void *bias, void *y, int64_t M, int64_t K,
+                                    int64_t N, int64_t G, void *workspace, size_t workspace_bytes,
+                                    wqbmm_stream_t stream);
+
+/*
  * A batch of products with shared weights (the operator's batched x, BatchMatmul with one weight): for b in
  * [0, batch), y_b = MSD matmul of x_b with the weights, x_b = x + b * x_batch_stride (fp16 [M, K], row stride K) and
  * y_b = y + b * y_batch_stride (fp16 [M, N], row stride N); strides count elements. Rows are independent, so when

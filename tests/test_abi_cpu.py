@@ -75,6 +75,16 @@ def test_workspace_bytes():
     assert wq.wqbmm_workspace_bytes(40, 1024, 28672, 128) == 3 * 8 * 48 * 128 + 3 * 8 * 512
 
 
+def test_w8_sizes():
+    # the split weights have 2K rows of int4: K * N bytes, padded to whole tiles
+    assert wq.wqbmm_prepacked_weight_bytes_w8(4096, 4096, 128) == 4096 * 4096
+    assert wq.wqbmm_prepacked_weight_bytes_w8(96, 1000, 32) == 8 * 2 * 8192
+    # workspace: the int4 problem's (M, 2K) plus x repeated [M, 2K] and the split scales and zero points
+    M, K, N, G = 1, 4096, 4096, 128
+    assert wq.wqbmm_workspace_bytes_w8(M, K, N, G) == (wq.wqbmm_workspace_bytes(M, 2 * K, N, G) + _a256(M * 2 * K * 2)
+                                                       + 2 * _a256(2 * (K // G) * N * 2))
+
+
 def _a256(v):
     return (v + 255) // 256 * 256
 
@@ -157,6 +167,14 @@ CASES = [
      NULLPTR),
     ("batched_bad_group",
      lambda L: L.wqbmm_run_batched(A, A, A, None, None, A, 2, 2, 192, 128, 96, 512, 512, A, 1 << 20, None), INVALID),
+    ("w8_size_per_channel_rejected", lambda L: L.wqbmm_prepacked_weight_bytes_w8(256, 128, 256, _sz()), INVALID),
+    ("w8_prepack_null", lambda L: L.wqbmm_prepack_weight_w8(None, A, 256, 128, 128, None), NULLPTR),
+    ("w8_prepack_misaligned", lambda L: L.wqbmm_prepack_weight_w8(A, MIS, 256, 128, 128, None), INVALID),
+    ("w8_run_null_workspace",
+     lambda L: L.wqbmm_run_w8(A, A, A, None, None, A, 1, 256, 128, 128, None, 0, None), NULLPTR),
+    ("w8_run_bad_group", lambda L: L.wqbmm_run_w8(A, A, A, None, None, A, 1, 256, 128, 256, A, 1 << 20, None),
+     INVALID),
+    ("w8_ws_null", lambda L: L.wqbmm_workspace_bytes_w8(1, 256, 128, 128, None), NULLPTR),
     ("run_per_channel_k_not_multiple_of_32",
      lambda L: L.wqbmm_run(A, A, A, A, 1, 100, 128, 100, A, 1 << 20, None), INVALID),
     ("run_group_larger_than_128_not_k", lambda L: L.wqbmm_run(A, A, A, A, 1, 512, 128, 256, A, 1 << 20, None),
@@ -207,5 +225,7 @@ def test_no_device_is_a_cuda_error(lib):
     assert lib.wqbmm_run_ex(A, A, A, None, None, A, 1, 4096, 4096, 128, A, 1 << 30, None) == wq.ERR_CUDA
     assert lib.wqbmm_run_batched(A, A, A, None, None, A, 4, 2, 4096, 4096, 128, 8192, 8192, A, 1 << 30,
                                  None) == wq.ERR_CUDA
+    assert lib.wqbmm_run_w8(A, A, A, None, None, A, 8, 4096, 11008, 128, A, 1 << 30, None) == wq.ERR_CUDA
+    assert lib.wqbmm_prepack_weight_w8(A, A, 4096, 4096, 128, None) == wq.ERR_CUDA
     assert lib.wqbmm_run_batched(A, A, A, None, None, A, 4, 2, 4096, 4096, 128, 9216, 8192, A, 1 << 30,
                                  None) == wq.ERR_CUDA

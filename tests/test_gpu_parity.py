@@ -539,3 +539,52 @@ def test_batched_strided_matches_oracle(dev, B, M, K, N, G):
     wq.wqbmm_run_batched(xc, w_pre, to_dev(sc, dev), None, None, yc, B, M, K, N, G, M * K, M * N, wsc)
     wq.wqbmm_run(xc, w_pre, to_dev(sc, dev), yo, B * M, K, N, G, wsc)
     np.testing.assert_array_equal(yc.cpu().numpy().view(np.uint16), yo.cpu().numpy().view(np.uint16))
+
+
+# ------------------------------------------------------------------------------------------- int8 weights (W8)
+
+def split_w8_packed(w8, G):
+    """The int4 form of int8 weights as documented for wqbmm_run_w8, restated with numpy: group g of w becomes
+    groups 2g (hi = w >> 4) and 2g + 1 (lo - 8 with lo = w & 15) of a [2K, N] int4 matrix, packed along k."""
+    K, N = w8.shape
+    w16 = w8.astype(np.int16)
+    hi = (w16 >> 4).reshape(K // G, G, N)
+    lo = ((w16 & 15) - 8).reshape(K // G, G, N)
+    return I.pack_int4_along_k(np.stack([hi, lo], axis=1).reshape(2 * K, N).astype(np.int8))
+
+
+@pytest.mark.parametrize("K,N,G", [(256, 128, 128), (640, 264, 64), (96, 1000, 32)])
+def test_prepack_w8_is_the_documented_split(dev, K, N, G):
+    w8 = I.make_w8(I.small_case(1, K, N, G, seed=K + N))
+    a = wq.prepack_weight_w8(to_dev(w8, dev), K, N, G).cpu().numpy()
+    b = wq.prepack_weight(to_dev(split_w8_packed(w8, G), dev), 2 * K, N, G).cpu().numpy()
+    np.testing.assert_array_equal(a, b)
+
+
+W8_CASES = [
+    # M, K, N, G, zero-point kind, bias
+    (1, 4096, 520, 128, None, False),       # decode kernel
+    (2, 1024, 1000, 32, "frac", True),
+    (3, 2048, 264, 64, None, True),         # small-M tensor-core kernel
+    (8, 4096, 1000, 128, "int", False),
+    (16, 1024, 256, 128, "frac", True),
+    (64, 512, 264, 64, None, False),        # large-M
+    (130, 384, 256, 128, "int", True),
+]
+
+
+@pytest.mark.parametrize("M,K,N,G,zkind,with_bias", W8_CASES)
+def test_w8_matches_oracle(dev, M, K, N, G, zkind, with_bias):
+    wl = I.small_case(M, K, N, G, seed=11 * M + K + N, x_dist="t3_clip60" if M % 2 else "normal")
+    x = I.make_x(wl)
+    sc = I.make_scale(wl)
+    w8 = I.make_w8(wl)
+    zp = None if zkind is None else (I.make_zero_point(wl, zkind) * 16).astype(np.float16)   # int8 range
+    bias = I.make_bias(wl) if with_bias else None
+    w_pre = wq.prepack_weight_w8(to_dev(w8, dev), K, N, G)
+    y = wq.msd_matmul_w8(to_dev(x, dev), w_pre, to_dev(sc, dev), G,
+                         zero_point=None if zp is None else to_dev(zp, dev),
+                         bias=None if bias is None else to_dev(bias, dev)).cpu().numpy()
+    for mode, what in ((oracle.MODE_D, "binary64 oracle"), (oracle.MODE_F, "binary32-unfold oracle")):
+        ref = oracle.msd_matmul_w8(x, w8, sc, G, zero_point=zp, bias=bias, mode=mode)
+        assert_within_tolerance(y, ref, what)

@@ -16,7 +16,8 @@ __all__ = [
     "wqbmm_workspace_bytes", "wqbmm_run", "wqbmm_debug_unfold", "wqbmm_debug_group_partials",
     "wqbmm_read_device_status", "wqbmm_debug_wait_timeout", "wqbmm_status_string", "prepack_weight",
     "allocate_workspace", "msd_matmul", "SYMBOLS", "wqbmm_run_static_scratch", "wqbmm_prepack_weight_nk",
-    "prepack_weight_nk", "wqbmm_run_ex", "wqbmm_run_batched",
+    "prepack_weight_nk", "wqbmm_run_ex", "wqbmm_run_batched", "wqbmm_prepacked_weight_bytes_w8",
+    "wqbmm_prepack_weight_w8", "wqbmm_workspace_bytes_w8", "wqbmm_run_w8", "prepack_weight_w8", "msd_matmul_w8",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -31,7 +32,8 @@ SYMBOLS = (
     "wqbmm_prepacked_weight_bytes", "wqbmm_prepack_weight", "wqbmm_workspace_bytes", "wqbmm_run",
     "wqbmm_debug_unfold", "wqbmm_debug_group_partials", "wqbmm_read_device_status", "wqbmm_debug_wait_timeout",
     "wqbmm_status_string", "wqbmm_run_static_scratch", "wqbmm_prepack_weight_nk", "wqbmm_run_ex",
-    "wqbmm_run_batched",
+    "wqbmm_run_batched", "wqbmm_prepacked_weight_bytes_w8", "wqbmm_prepack_weight_w8", "wqbmm_workspace_bytes_w8",
+    "wqbmm_run_w8",
 )
 
 
@@ -63,6 +65,10 @@ def load_library():
                 "wqbmm_run": [p, p, p, p, i64, i64, i64, i64, p, sz, p],
                 "wqbmm_run_ex": [p, p, p, p, p, p, i64, i64, i64, i64, p, sz, p],
                 "wqbmm_run_batched": [p, p, p, p, p, p, i64, i64, i64, i64, i64, i64, i64, p, sz, p],
+                "wqbmm_prepacked_weight_bytes_w8": [i64, i64, i64, ctypes.POINTER(sz)],
+                "wqbmm_prepack_weight_w8": [p, p, i64, i64, i64, p],
+                "wqbmm_workspace_bytes_w8": [i64, i64, i64, i64, ctypes.POINTER(sz)],
+                "wqbmm_run_w8": [p, p, p, p, p, p, i64, i64, i64, i64, p, sz, p],
                 "wqbmm_debug_unfold": [p, i64, i64, i64, p, p, p],
                 "wqbmm_debug_group_partials": [p, p, i64, i64, i64, i64, i64, p, p, sz, p],
                 "wqbmm_read_device_status": [ctypes.POINTER(ctypes.c_int32), ctypes.c_int, p],
@@ -155,6 +161,33 @@ def wqbmm_run_batched(x, w_prepacked, antiquant_scale, zero_point, bias, y, batc
                                              _ptr(workspace), workspace_bytes, _stream(stream)), "wqbmm_run_batched")
 
 
+def wqbmm_prepacked_weight_bytes_w8(K: int, N: int, G: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load_library().wqbmm_prepacked_weight_bytes_w8(K, N, G, ctypes.byref(out)),
+           "wqbmm_prepacked_weight_bytes_w8")
+    return out.value
+
+
+def wqbmm_prepack_weight_w8(w8, w_prepacked, K: int, N: int, G: int, stream=None) -> None:
+    _check(load_library().wqbmm_prepack_weight_w8(_ptr(w8), _ptr(w_prepacked), K, N, G, _stream(stream)),
+           "wqbmm_prepack_weight_w8")
+
+
+def wqbmm_workspace_bytes_w8(M: int, K: int, N: int, G: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load_library().wqbmm_workspace_bytes_w8(M, K, N, G, ctypes.byref(out)), "wqbmm_workspace_bytes_w8")
+    return out.value
+
+
+def wqbmm_run_w8(x, w_prepacked, antiquant_scale, zero_point, bias, y, M: int, K: int, N: int, G: int,
+                 workspace=None, workspace_bytes: int | None = None, stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().wqbmm_run_w8(_ptr(x), _ptr(w_prepacked), _ptr(antiquant_scale), _ptr(zero_point),
+                                        _ptr(bias), _ptr(y), M, K, N, G, _ptr(workspace), workspace_bytes,
+                                        _stream(stream)), "wqbmm_run_w8")
+
+
 def wqbmm_run_static_scratch(x, w_prepacked, antiquant_scale, y, M: int, K: int, N: int, G: int,
                              stream=None) -> None:
     """wqbmm_run without a caller workspace: the library's fixed 2 MiB device scratch is used instead (for callers
@@ -205,6 +238,28 @@ def prepack_weight_nk(w_packed_nk, K: int, N: int, G: int, stream=None):
     out = torch.empty(wqbmm_prepacked_weight_bytes(K, N, G), dtype=torch.uint8, device=w_packed_nk.device)
     wqbmm_prepack_weight_nk(w_packed_nk, out, K, N, G, stream)
     return out
+
+
+def prepack_weight_w8(w8, K: int, N: int, G: int, stream=None):
+    """int8 [K, N] weights on the GPU -> a new uint8 tensor of prepacked split (int4) tiles."""
+    import torch
+    out = torch.empty(wqbmm_prepacked_weight_bytes_w8(K, N, G), dtype=torch.uint8, device=w8.device)
+    wqbmm_prepack_weight_w8(w8, out, K, N, G, stream)
+    return out
+
+
+def msd_matmul_w8(x, w_prepacked, antiquant_scale, G: int, y=None, workspace=None, stream=None, zero_point=None,
+                  bias=None):
+    """y [M, N] fp16 = MSD matmul of x [M, K] fp16 with prepacked int8 weights (prepack_weight_w8)."""
+    import torch
+    M, K = x.shape
+    N = antiquant_scale.shape[1]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    if workspace is None:
+        workspace = torch.zeros(wqbmm_workspace_bytes_w8(M, K, N, G), dtype=torch.uint8, device=x.device)
+    wqbmm_run_w8(x, w_prepacked, antiquant_scale, zero_point, bias, y, M, K, N, G, workspace, None, stream)
+    return y
 
 
 def allocate_workspace(M: int, K: int, N: int, G: int, device):

@@ -304,6 +304,63 @@ __global__ void unfold_debug_kernel(const __half *__restrict__ x, int M, int K, 
     if (amax_out != nullptr && (lane & (lpg - 1)) == 0) amax_out[static_cast<size_t>(row) * (K / G) + kbase / G] = am;
 }
 
+// ------------------------------------------------------------------------------------------------ int8 weights
+// An int8 weight w = 16 hi + lo with hi = w >> 4 in [-8, 7] and lo = w & 15 in [0, 15]. Group g of the int8 problem
+// becomes groups 2g (weights hi, scale 16 s, zero point -1/2) and 2g + 1 (weights lo - 8, scale s, zero point zp)
+// of an int4 problem with 2K rows, whose x repeats each group of x twice: both groups see the same planes and A_max
+// and s (16 (hi + 1/2) + (lo - 8 - zp)) = s (w - zp), so the int4 path computes the int8 product exactly.
+
+// Prepacked int4 tiles of the split weights (2K rows) from int8 [K, N]: the layout of prepack_kernel.
+__global__ void prepack_w8_kernel(const int8_t *__restrict__ w8, uint8_t *__restrict__ out, int K, int N, int G,
+                                  int kb_total2) {
+    const int nt = blockIdx.x, kb = blockIdx.y;
+    uint8_t *dst = out + (static_cast<size_t>(nt) * kb_total2 + kb) * kPackedTileBytes;
+    auto nibble = [&](int k2, int n) -> uint32_t {
+        if (k2 >= 2 * K || n >= N) return 8u;                           // padding: weight 0
+        const int g = k2 / (2 * G), part = (k2 / G) & 1, kk = g * G + k2 % G;
+        const uint32_t b = static_cast<uint8_t>(w8[static_cast<size_t>(kk) * N + n]);
+        return part == 0 ? ((b ^ 0x80u) >> 4) & 15u : b & 15u;          // hi + 8, or (lo - 8) + 8
+    };
+    for (int idx = threadIdx.x; idx < kPackedTileBytes; idx += blockDim.x) {
+        const int r = idx / (kKBlock / 2), j = idx % (kKBlock / 2);
+        const int k0 = kb * kKBlock + 8 * (j >> 2) + (j & 3);
+        const int n = nt * kTileN + r;
+        dst[idx] = static_cast<uint8_t>(nibble(k0, n) | (nibble(k0 + 4, n) << 4));
+    }
+}
+
+// The int4 problem's x [M, 2K] (each group of x twice), scales [2 K/G, N] and zero points [2 K/G, N], into the
+// workspace. Grid-stride over both tasks.
+__global__ void __launch_bounds__(256) w8_prep_kernel(const __half *__restrict__ x, int M, int K, int G,
+                                                      const __half *__restrict__ scale, const __half *__restrict__ zp,
+                                                      int N, __half *__restrict__ x2, __half *__restrict__ scale2,
+                                                      __half *__restrict__ zp2) {
+    // no early release of the dependents: the main kernel fetches the scales and zero points written here before
+    // it waits for its own predecessor, so it must not start before this kernel has ended
+    pdl_wait();              // x may be the preceding kernel's output, which may also still read these buffers
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    // x2: 8 halves (16 bytes) at a time; G is a multiple of 32, so a piece never straddles a group
+    const size_t pieces = static_cast<size_t>(M) * (2 * K) / 8;
+    for (size_t i = tid; i < pieces; i += stride) {
+        const size_t e = i * 8;
+        const int m = static_cast<int>(e / (2 * K));
+        const int k2 = static_cast<int>(e % (2 * K));
+        const int g = k2 / (2 * G), kk = g * G + k2 % G;
+        *reinterpret_cast<uint4 *>(x2 + e) = *reinterpret_cast<const uint4 *>(x + static_cast<size_t>(m) * K + kk);
+    }
+    const int Gn = K / G;
+    const size_t cells = static_cast<size_t>(Gn) * N;
+    for (size_t i = tid; i < cells; i += stride) {
+        const int g = static_cast<int>(i / N), n = static_cast<int>(i % N);
+        const __half s = scale[i];
+        scale2[(2 * static_cast<size_t>(g)) * N + n] = __hmul(s, __float2half(16.0f));    // exact below 4096
+        scale2[(2 * static_cast<size_t>(g) + 1) * N + n] = s;
+        zp2[(2 * static_cast<size_t>(g)) * N + n] = __float2half(-0.5f);
+        zp2[(2 * static_cast<size_t>(g) + 1) * N + n] = zp != nullptr ? zp[i] : __float2half(0.0f);
+    }
+}
+
 // Per-channel quantization (one group spanning all of K; the kernels then work in sub-groups of gs k with the
 // row's A_max). Blocks [0, M): A_max of row m = max |x[m, k]| over all k (exact: a maximum of fp16 magnitudes).
 // Blocks [M, M + gridDim.x - M): scale (and zero-point) row 0 copied to rows 0 .. reps - 1 of scale_rep / zp_rep,
@@ -314,7 +371,8 @@ __global__ void __launch_bounds__(256) per_channel_prep_kernel(const __half *__r
                                                                const __half *__restrict__ zp, int N, int reps,
                                                                __half *__restrict__ scale_rep,
                                                                __half *__restrict__ zp_rep) {
-    pdl_launch_dependents();
+    // no early release of the dependents: the main kernels fetch the scale rows written here before they wait for
+    // their own predecessor, so they must not start before this kernel has ended
     pdl_wait();              // x may be the preceding kernel's output, which may also still read these buffers
     if (static_cast<int>(blockIdx.x) >= M) {
         if (scale_rep == nullptr) return;

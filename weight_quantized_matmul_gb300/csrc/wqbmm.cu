@@ -545,6 +545,25 @@ wqbmm_status static_scratch_address(int dev, void **addr) {
     return WQBMM_OK;
 }
 
+// Int8 weights run as an int4 problem with 2K rows (see prepack_w8_kernel): shape checks of both problems.
+wqbmm_status check_w8(int64_t K, int64_t N, int64_t G) {
+    if (!group_size_ok(G)) return WQBMM_ERR_INVALID;    // groups only: the two halves of a group need two scales
+    if (K < 1 || K > INT_MAX / 2) return WQBMM_ERR_INVALID;
+    const wqbmm_status st = check_kng(K, N, G);
+    return st != WQBMM_OK ? st : check_kng(2 * K, N, G);
+}
+
+// Layout of the int8 path's workspace: the int4 problem's own, then x2 [M, 2K], scale2 and zp2 [2 K/G, N].
+struct W8Workspace {
+    size_t path, x2, scale2, total;
+    W8Workspace(const Shape &s2, const Plan &plan) {
+        path = workspace_for(s2, plan);
+        x2 = align256(static_cast<size_t>(s2.M) * s2.K * 2);
+        scale2 = align256(static_cast<size_t>(s2.K / s2.G) * s2.N * 2);
+        total = path + x2 + 2 * scale2;
+    }
+};
+
 wqbmm_status prepack(const uint8_t *w_packed, void *w_prepacked, int64_t K, int64_t N, int64_t G, bool nk,
                      wqbmm_stream_t stream) {
     if (!w_packed || !w_prepacked) return WQBMM_ERR_NULLPTR;
@@ -602,6 +621,83 @@ wqbmm_status wqbmm_prepack_weight(const uint8_t *w_packed, void *w_prepacked, in
 wqbmm_status wqbmm_prepack_weight_nk(const uint8_t *w_packed_nk, void *w_prepacked, int64_t K, int64_t N, int64_t G,
                                      wqbmm_stream_t stream) {
     return prepack(w_packed_nk, w_prepacked, K, N, G, true, stream);
+}
+
+wqbmm_status wqbmm_prepacked_weight_bytes_w8(int64_t K, int64_t N, int64_t G, size_t *bytes) {
+    if (!bytes) return WQBMM_ERR_NULLPTR;
+    const wqbmm_status st = check_w8(K, N, G);
+    if (st != WQBMM_OK) return st;
+    *bytes = static_cast<size_t>(ceil_div(N, kTileN)) * ceil_div(2 * K, kKBlock) * kPackedTileBytes;
+    return WQBMM_OK;
+}
+
+wqbmm_status wqbmm_prepack_weight_w8(const int8_t *w8, void *w_prepacked, int64_t K, int64_t N, int64_t G,
+                                     wqbmm_stream_t stream) {
+    if (!w8 || !w_prepacked) return WQBMM_ERR_NULLPTR;
+    wqbmm_status st = check_w8(K, N, G);
+    if (st != WQBMM_OK) return st;
+    if (!aligned16(w_prepacked)) return WQBMM_ERR_INVALID;
+    int dev;
+    DeviceInfo *info;
+    if ((st = current_device(&dev, &info)) != WQBMM_OK) return st;
+    const int kb2 = static_cast<int>(ceil_div(2 * K, kKBlock));
+    const dim3 grid(static_cast<unsigned>(ceil_div(N, kTileN)), static_cast<unsigned>(kb2));
+    prepack_w8_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        w8, static_cast<uint8_t *>(w_prepacked), static_cast<int>(K), static_cast<int>(N), static_cast<int>(G), kb2);
+    return cudaPeekAtLastError() == cudaSuccess ? WQBMM_OK : WQBMM_ERR_CUDA;
+}
+
+wqbmm_status wqbmm_workspace_bytes_w8(int64_t M, int64_t K, int64_t N, int64_t G, size_t *bytes) {
+    if (!bytes) return WQBMM_ERR_NULLPTR;
+    wqbmm_status st = check_w8(K, N, G);
+    if (st != WQBMM_OK) return st;
+    if ((st = check_shape(Shape{M, 2 * K, N, G})) != WQBMM_OK) return st;
+    const Shape s2 = kernel_shape(M, 2 * K, N, G);
+    *bytes = W8Workspace(s2, make_plan(s2, kPlanSms)).total;
+    return WQBMM_OK;
+}
+
+wqbmm_status wqbmm_run_w8(const void *x, const void *w_prepacked, const void *antiquant_scale,
+                          const void *zero_point, const void *bias, void *y, int64_t M, int64_t K, int64_t N,
+                          int64_t G, void *workspace, size_t workspace_bytes, wqbmm_stream_t stream) {
+    if (!x || !w_prepacked || !antiquant_scale || !y) return WQBMM_ERR_NULLPTR;
+    wqbmm_status st = check_w8(K, N, G);
+    if (st != WQBMM_OK) return st;
+    if ((st = check_shape(Shape{M, 2 * K, N, G})) != WQBMM_OK) return st;
+    if (!aligned16(x) || !aligned16(w_prepacked) || !aligned16(antiquant_scale) || !aligned16(y) ||
+        !aligned16(zero_point) || !aligned16(bias))
+        return WQBMM_ERR_INVALID;
+    if (!workspace) return WQBMM_ERR_NULLPTR;
+    if (!aligned16(workspace)) return WQBMM_ERR_INVALID;
+    int dev;
+    DeviceInfo *info;
+    if ((st = current_device(&dev, &info)) != WQBMM_OK) return st;
+    const Shape s2 = kernel_shape(M, 2 * K, N, G);
+    const Plan plan = make_plan(s2, info->sms < kPlanSms ? info->sms : kPlanSms);
+    const W8Workspace L(s2, plan);
+    if (workspace_bytes < L.total) return WQBMM_ERR_INVALID;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    __half *x2 = reinterpret_cast<__half *>(ws + L.path);
+    __half *scale2 = reinterpret_cast<__half *>(ws + L.path + L.x2);
+    __half *zp2 = reinterpret_cast<__half *>(ws + L.path + L.x2 + L.scale2);
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    const int64_t work = std::max<int64_t>(M * 2 * K / 8, (K / G) * N);
+    cfg.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>(ceil_div(work, 256), 4096)), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = cs;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, w8_prep_kernel, static_cast<const __half *>(x), static_cast<int>(M),
+                           static_cast<int>(K), static_cast<int>(G), static_cast<const __half *>(antiquant_scale),
+                           static_cast<const __half *>(zero_point), static_cast<int>(N), x2, scale2,
+                           zp2) != cudaSuccess)
+        return WQBMM_ERR_CUDA;
+    const Operands op{x2, w_prepacked, scale2, zp2, bias, y};
+    return dispatch(op, s2, plan, workspace, false, -1, nullptr, info, cs);
 }
 
 wqbmm_status wqbmm_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t G, size_t *bytes) {

@@ -155,7 +155,7 @@ WORKLOADS = {
 }
 
 # stream ids
-_S_X, _S_W, _S_SCALE, _S_COLS, _S_WSEL, _S_WPM, _S_ROWS, _S_ZP, _S_BIAS = 1, 2, 3, 4, 5, 6, 7, 8, 9
+_S_X, _S_W, _S_SCALE, _S_COLS, _S_WSEL, _S_WPM, _S_ROWS, _S_ZP, _S_BIAS, _S_W8 = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10
 
 
 def make_x(wl: Workload, M: Optional[int] = None) -> np.ndarray:
@@ -235,6 +235,11 @@ def make_zero_point(wl: Workload, kind: str = "int") -> np.ndarray:
     else:
         raise ValueError(kind)
     return fp16(z).reshape(wl.groups, wl.N)
+
+
+def make_w8(wl: Workload) -> np.ndarray:
+    """Int8 weights [K, N] uniform on [-128, 127] (W8)."""
+    return int_uniform(wl.seed, _S_W8, wl.K * wl.N, -128, 127).astype(np.int8).reshape(wl.K, wl.N)
 
 
 def make_bias(wl: Workload, lo: float = -1.0, hi: float = 1.0) -> np.ndarray:
