@@ -22,6 +22,7 @@ CPU oracle (the plain C implementation of the method used by the tests) on the h
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -53,6 +54,8 @@ def parse():
     ap.add_argument("--zero-point", default="none", choices=["none", "int", "frac"],
                     help="asymmetric weights: seeded zero points [K/G, N] (wqbmm_run_ex)")
     ap.add_argument("--bias", action="store_true", help="add a seeded bias [N] (wqbmm_run_ex)")
+    ap.add_argument("--per-channel", action="store_true", help="per-channel quantization: G = K, scale [1, N]")
+    ap.add_argument("--w8", action="store_true", help="int8 weights [K, N] (wqbmm_run_w8)")
     ap.add_argument("--sustain-s", type=float, default=1.5)
     ap.add_argument("--cpu-baseline-s", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -65,13 +68,16 @@ def metric_for(wl):
     return "A16W4 MSD matmul int8-equivalent TOPS (6*M*N*K)", "TOPS"
 
 
-def units_per_step(wl):
-    """The metric's numerator for one step: weight bytes (M<=16) or int8-equivalent ops."""
-    return wl.weight_bytes() if wl.M <= 16 else wl.int8_equiv_ops()
+def units_per_step(wl, w8=False):
+    """The metric's numerator for one step: weight bytes (M<=16; int8 weights take K N bytes) or int8-equivalent
+    ops."""
+    if wl.M <= 16:
+        return wl.K * wl.N if w8 else wl.weight_bytes()
+    return wl.int8_equiv_ops()
 
 
-def metric_value(wl, seconds_per_step, n=1):
-    return n * units_per_step(wl) / seconds_per_step / (1e9 if wl.M <= 16 else 1e12)
+def metric_value(wl, seconds_per_step, n=1, w8=False):
+    return n * units_per_step(wl, w8) / seconds_per_step / (1e9 if wl.M <= 16 else 1e12)
 
 
 def measured_peaks():
@@ -258,6 +264,8 @@ def run_reference(args, wl):
 def main():
     args = parse()
     wl = I.WORKLOADS[args.workload]
+    if args.per_channel:
+        wl = dataclasses.replace(wl, G=wl.K)
     if args.impl == "reference":
         run_reference(args, wl)
         return
@@ -280,29 +288,41 @@ def main():
 
     # ---- inputs: host copy once, then rotating device copies whose total exceeds 2x L2
     x, wp, sc = I.make_inputs(wl)
-    per_copy = wl.weight_bytes() + x.nbytes + sc.nbytes
+    if args.w8:
+        wp = I.make_w8(wl)
+    per_copy = wp.nbytes + x.nbytes + sc.nbytes
     copies = max(2, min(64, -(-2 * L2_BYTES // per_copy)))
     xd = torch.from_numpy(x).to(dev)
     sd = torch.from_numpy(sc).to(dev)
     wd = torch.from_numpy(wp).to(dev)
-    w_pre0 = wq.prepack_weight(wd, wl.K, wl.N, wl.G)
+    if args.w8:
+        w_pre0 = wq.prepack_weight_w8(wd, wl.K, wl.N, wl.G)
+    else:
+        w_pre0 = wq.prepack_weight(wd, wl.K, wl.N, wl.G)
     del wd
     w_pre = [w_pre0] + [w_pre0.clone() for _ in range(copies - 1)]
     xs = [xd] + [xd.clone() for _ in range(copies - 1)]
     ss = [sd] + [sd.clone() for _ in range(copies - 1)]
     ys = [torch.empty((wl.M, wl.N), dtype=torch.float16, device=dev) for _ in range(copies)]
-    ws = [wq.allocate_workspace(wl.M, wl.K, wl.N, wl.G, dev) for _ in range(copies)]
+    if args.w8:
+        ws = [torch.zeros(wq.wqbmm_workspace_bytes_w8(wl.M, wl.K, wl.N, wl.G), dtype=torch.uint8, device=dev)
+              for _ in range(copies)]
+    else:
+        ws = [wq.allocate_workspace(wl.M, wl.K, wl.N, wl.G, dev) for _ in range(copies)]
     zs = [None] * copies
     if args.zero_point != "none":
         zd = torch.from_numpy(I.make_zero_point(wl, args.zero_point)).to(dev)
         zs = [zd] + [zd.clone() for _ in range(copies - 1)]
     bd = torch.from_numpy(I.make_bias(wl)).to(dev) if args.bias else None
     optionals = args.zero_point != "none" or args.bias
+    variant = optionals or args.per_channel or args.w8           # not the captured kernels' workload
     stream = torch.cuda.Stream(device=dev)
 
     def step(i, s):
         c = i % copies
-        if optionals:
+        if args.w8:
+            wq.wqbmm_run_w8(xs[c], w_pre[c], ss[c], zs[c], bd, ys[c], wl.M, wl.K, wl.N, wl.G, ws[c], None, s)
+        elif optionals:
             wq.wqbmm_run_ex(xs[c], w_pre[c], ss[c], zs[c], bd, ys[c], wl.M, wl.K, wl.N, wl.G, ws[c], None, s)
         else:
             wq.wqbmm_run(xs[c], w_pre[c], ss[c], ys[c], wl.M, wl.K, wl.N, wl.G, ws[c], None, s)
@@ -393,12 +413,12 @@ def main():
     peaks, peak_kind = measured_peaks()
     # the optional inputs add their own bytes: zero points 2 (K/G) N, bias 2 N
     alg_bytes = (wl.algorithmic_bytes() + (2 * wl.groups * wl.N if args.zero_point != "none" else 0) +
-                 (2 * wl.N if args.bias else 0))
+                 (2 * wl.N if args.bias else 0) + (wl.K * wl.N // 2 if args.w8 else 0))
     if wl.M <= 16:
         hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
         achieved = alg_bytes / (ms_step * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                    "frac": achieved / hbm_peak, "traffic": None if optionals else dram_traffic(wl.name),
+                    "frac": achieved / hbm_peak, "traffic": None if variant else dram_traffic(wl.name),
                     "peak_source": f"{peak_kind} hbm_gbs",
                     "algorithmic_bytes_per_launch": alg_bytes}
     else:
@@ -406,12 +426,12 @@ def main():
         bf16 = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
         achieved = wl.int8_equiv_ops() / (ms_step * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": 2 * bf16, "unit": "TFLOP/s",
-                    "frac": achieved / (2 * bf16), "traffic": None if optionals else dram_traffic(wl.name),
+                    "frac": achieved / (2 * bf16), "traffic": None if variant else dram_traffic(wl.name),
                     "peak_source": f"{peak_kind} bf16_tflops x 2 (e4m3)",
                     "algorithmic_flops_per_launch": wl.int8_equiv_ops()}
     line = {
         "metric": metric,
-        "value": metric_value(wl, ms_step * 1e-3, world),
+        "value": metric_value(wl, ms_step * 1e-3, world, args.w8),
         "unit": unit,
         "n_gpus": world,
         "steps": args.steps,
@@ -423,13 +443,14 @@ def main():
         "dtype": "fp16 x / int4 w -> e4m3 tensor-core MMA, f32 accumulate and epilogue",
         "data": "synthetic",
         "config": {"workload": wl.name, "M": wl.M, "K": wl.K, "N": wl.N, "G": wl.G,
-                   "zero_point": args.zero_point, "bias": bool(args.bias),
+                   "zero_point": args.zero_point, "bias": bool(args.bias), "per_channel": bool(args.per_channel),
+                   "weights": "int8" if args.w8 else "int4",
                    "parallelism": f"replicas{world}" if world > 1 else "single GPU",
                    "l2": f"{copies} rotating input copies ({copies * per_copy / 2**20:.0f} MiB > 2x L2)",
                    "launch": f"CUDA graphs of {chunk} steps"},
         "gpu_launches": args.steps * launches_per_step,
         "clocks": sampler.summary(),
-        "e2e": {"value": metric_value(wl, e2e_s, 1), "unit": unit, "h2d_bytes_per_step": int(x.nbytes),
+        "e2e": {"value": metric_value(wl, e2e_s, 1, args.w8), "unit": unit, "h2d_bytes_per_step": int(x.nbytes),
                 "d2h_bytes_per_step": int(wl.M * wl.N * 2),
                 "note": "eager wqbmm_run per step; pinned x in, pinned y out, stream synchronized each step"},
         "roofline": roofline,
