@@ -12,7 +12,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libwqbmm.so")
 SOURCES = [os.path.join(CSRC, "wqbmm.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("msd_kernels.cuh", "ptx.cuh")] + [os.path.join(INCLUDE, "wqbmm.h")]
+DEPS = SOURCES + sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")) + [
+    os.path.join(INCLUDE, "wqbmm.h")]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
