@@ -250,6 +250,8 @@ RUN_CASES = [
     (1, 65536, 256, 128, "normal", "u8", 0.005, 0.02),     # M <= 2, K > 8192: unfold kernel + streaming kernel
     (2, 8320, 264, 64, "t3_clip60", "u8", -1.0, 1.0),
     (2, 1024, 1000, 32, "uniform3", "u7", -3.0, 3.0),      # M <= 2, K <= 8192: one persistent kernel
+    (2, 352, 136, 32, "normal", "u8", 0.005, 0.02),        # M <= 2, ragged last k-block (K = 2.75 x 128)
+    (1, 1280, 39936, 128, "normal", "u8", 0.005, 0.02),    # M <= 2, 2496 column CTAs
     (3, 65536, 256, 128, "normal", "u8", 0.005, 0.02),     # 160-way split-K through the workspace
     (4, 4096, 1024, 128, "t3_clip60", "u8", -0.5, 0.5),    # 8 column tiles x 8 cluster slices
 ]

@@ -144,7 +144,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvPar
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = p.N, K = p.K, G = p.G, kb_total = p.kb_total;
-    const int Gn = K / G, gpk = kKBlock / G;
+    const int gshift = 31 - __clz(G);                  // G is 32, 64 or 128: group index = k >> gshift
+    const int Gn = K >> gshift, gpk = kKBlock >> gshift;
     const int col0 = blockIdx.x * kGemvCols;
     const int nt = col0 / kTileN, r0 = col0 % kTileN;
     const int chunk = lane & 3;
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvPar
         if (!kDebug) {
 #pragma unroll
             for (int j = 0; j < kGemvKbPerPass; ++j) {
-                const int g = ((kw0 + j) * kKBlock + chunk * 32) / G;
+                const int g = ((kw0 + j) * kKBlock + chunk * 32) >> gshift;
                 const bool in = j < nkb && g < Gn;
                 const size_t row_at = static_cast<size_t>(g) * p.group_stride + n_a;
                 sab[j] = in && n_a < N ? __ldg(reinterpret_cast<const __half2 *>(p.scale + row_at)) : __half2(0.0f, 0.0f);
@@ -215,10 +216,10 @@ __global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvPar
         if (ok) {
 #pragma unroll
             for (int j = 0; j < kGemvKbPerPass; ++j) {
-                if (j >= nkb) break;
+                if (j >= nkb) continue;                 // (not break: the loop stays fully unrolled)
                 const int kb = kw0 + j, kbl = kb - pb;
                 const int k0 = kb * kKBlock + chunk * 32;
-                const int g = k0 / G;
+                const int g = k0 >> gshift;
                 const bool live = k0 < K;               // a ragged last k-block: chunks past K hold zeros
 #pragma unroll
                 for (int m = 0; m < MR; ++m) {
