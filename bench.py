@@ -440,7 +440,9 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp16 x / int4 w -> e4m3 tensor-core MMA, f32 accumulate and epilogue",
+        # the arithmetic of the path this workload takes: dp4a on the CUDA cores for M <= 2, tensor cores above
+        "dtype": ("fp16 x / int4 w -> int8 planes, dp4a int32 products, f32 epilogue" if wl.M <= 2 else
+                  "fp16 x / int4 w -> e4m3 tensor-core MMA, f32 accumulate and epilogue"),
         "data": "synthetic",
         "config": {"workload": wl.name, "M": wl.M, "K": wl.K, "N": wl.N, "G": wl.G,
                    "zero_point": args.zero_point, "bias": bool(args.bias), "per_channel": bool(args.per_channel),
