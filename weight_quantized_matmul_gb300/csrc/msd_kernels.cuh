@@ -49,12 +49,15 @@ constexpr int kSmemBudget = 110 * 1024;              // per CTA, so that two CTA
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
-constexpr int kWorkWarp0 = 2;
-constexpr int kNumWorkWarps = 8;
-constexpr int kWorkThreads = kNumWorkWarps * 32;
-constexpr int kWorkBarrierId = 1;
+constexpr int kConvWarp0 = 2;                        // warps 2-5 expand the weights
+constexpr int kNumConvWarps = 4;
+constexpr int kConvThreads = kNumConvWarps * 32;
+constexpr int kEpiWarp0 = 6;                         // warps 6-9: the epilogue, one warp per TMEM lane quarter
+constexpr int kNumEpiWarps = 4;
+constexpr int kEpiThreads = kNumEpiWarps * 32;
+constexpr int kEpiBarrierId = 1;                     // named barrier among the epilogue warps
 constexpr int kOperandBarrier0 = 2;                  // named barriers 2, 3: converted weight slot 0, 1 ready
-constexpr int kOperandThreads = kWorkThreads + 32;   // the workers and the MMA warp
+constexpr int kOperandThreads = kConvThreads + 32;   // the converters and the MMA warp
 constexpr int kConstFloatsPerGroup = 16 * 8;          // 16 rows x {c1 c2 c3 corr, S1 S2 S3 0}
 
 // Method constants (page section 4.1): unfold factors and the combine weights 1/7.49, 1/(7.49*14.98), ...
@@ -80,7 +83,7 @@ template <int NMMA>
 struct Cfg {
     static_assert(NMMA == 16 || NMMA == 32 || NMMA == 48, "MMA N must be 16, 32 or 48");
     static constexpr int kMaxM = NMMA / 3;                         // rows of x per CTA (plane stride in B rows)
-    static constexpr int kRowsPerWarp = (kMaxM + 1) / 2;           // two worker warps share a TMEM lane quarter
+    static constexpr int kRowsPerWarp = kMaxM;                     // one epilogue warp per TMEM lane quarter
     static constexpr int kBufStride = NMMA <= 16 ? 16 : (NMMA <= 32 ? 32 : 64);   // TMEM columns per buffer
     // eight buffers hold two k-blocks of the smallest groups; NMMA = 48 keeps four, so that two CTAs fit in TMEM
     static constexpr int kTmemBufs = NMMA <= 32 ? 8 : 4;
@@ -108,7 +111,7 @@ struct SmallLayout {
         const int fit = (kSmemBudget - fixed - 16 * 8) / stage_bytes;
         p_stages = fit < 3 ? 3 : (fit > 8 ? 8 : fit);
         off_bar = off_stages + p_stages * stage_bytes;
-        off_misc = off_bar + (2 * p_stages + 2 * kMaxTmemBufs) * 8;
+        off_misc = off_bar + (2 * p_stages + 2 * kMaxTmemBufs + kASlots) * 8;
         smem_bytes = off_misc + 64 + 1024;                         // + alignment slack
     }
 };
@@ -524,14 +527,15 @@ __device__ __forceinline__ void debug_rows(const uint32_t (&d)[3][16], const flo
 
 // kZp: the weights carry zero points, w - zp[g, n] being the quantized value the scale multiplies. The plane dots
 // then need (8 + zp) S_i taken off instead of 8 S_i, that is the correction term times 1 + zp / 8.
-// Roles: warp 0 lane 0 issues the loads, warp 1 lane 0 the MMAs; warps 2-9 (the workers) convert each k-block's
-// weight tile together, then run the previous k-block's epilogue: two warps per TMEM lane quarter (32 output
-// columns), each taking half of the rows, reading the constants and scales in place in the load stage. The workers
-// hand a converted tile to the MMA warp through a hardware named barrier. The MMA-issuing thread makes no ordinary
-// shared-memory access between its MMAs (such an access waits for its MMAs in flight to finish reading their
-// operands): it never checks the abort flag, and with enough TMEM buffers it never waits for one to be free. So
-// after a failed wait the workers skip their work but keep every synchronisation (arrivals on the named barrier,
-// waits for the MMAs' commits), and the MMA warp keeps issuing, and nothing can wait forever.
+// Roles: warp 0 lane 0 issues the loads, warp 1 lane 0 the MMAs; warps 2-5 (the converters) expand each k-block's
+// weight tile; warps 6-9 run the epilogue, one warp per TMEM lane quarter (32 output columns) over all rows, reading
+// the constants and scales in place in the load stage, as soon as each K-group's MMAs have committed. So the
+// expansion of a k-block and the epilogue of an earlier one run at the same time on different warps. The converters
+// hand a tile to the MMA warp through a hardware named barrier, once the tile is expanded and the MMAs that read its
+// slot before, and the epilogue reads of the TMEM buffers it will use, are done. The MMA-issuing thread makes no
+// ordinary shared-memory access between its MMAs (such an access waits for its MMAs in flight to finish reading
+// their operands) and never gives up a wait. After a failed wait the other roles skip their work but keep every
+// synchronisation (arrivals on the named barrier, waits for the MMAs' commits), so nothing can wait forever.
 template <int NMMA, bool kZp>
 __global__ void __launch_bounds__(kThreads, 2)
     msd_kernel(const RunParams p, const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_z) {
@@ -545,18 +549,19 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint8_t *a_ring = smem + C::kOffA;
     uint8_t *p_ring = smem + C::kOffStages;
     const uint32_t bar0 = smem_addr(smem + L.off_bar);
-    // barriers: full_p / empty_p  load stage landed / released after the k-block's epilogue
-    //           full_t / empty_t  TMEM accumulator written by the MMAs / read by the workers
-    // and the named barriers kOperandBarrier0 + c: converted weight slot c ready for k-block i (i % 2 == c). When
-    // the workers arrive there for k-block i they have finished the epilogue of k-block i - 2, so the MMAs of the
-    // slot's previous k-block are done and so is every read of the TMEM buffers used two k-blocks back; and the MMA
-    // warp has passed that barrier for k-block i - 2 (the workers waited for its commits), so no arrival can count
-    // towards an earlier phase.
+    // barriers: full_p / empty_p  load stage landed / released (converters done with the weights, epilogue with the
+    //                             constants and scales after the k-block's MMAs, which read the planes)
+    //           full_t / empty_t  TMEM accumulator written by the MMAs / read by the epilogue
+    //           a_free            converted weight slot read by the MMAs (their commit)
+    // and the named barriers kOperandBarrier0 + c: converted weight slot c ready for k-block i (i % 2 == c). Before
+    // the converters arrive there for k-block i they have seen a_free for k-block i - 2, committed after the MMA warp
+    // passed that barrier for k-block i - 2, so no arrival can count towards an earlier phase.
     auto full_p = [&](int s) { return bar0 + 8u * s; };
     auto empty_p = [&](int s) { return bar0 + 8u * (P + s); };
     constexpr int kTmemBufs = C::kTmemBufs;
     auto full_t = [&](int b) { return bar0 + 8u * (2 * P + b); };
     auto empty_t = [&](int b) { return bar0 + 8u * (2 * P + kMaxTmemBufs + b); };
+    auto a_free = [&](int c) { return bar0 + 8u * (2 * P + 2 * kMaxTmemBufs + c); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.off_misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.off_misc + 4);
     int *last_flag = reinterpret_cast<int *>(smem + L.off_misc + 8);
@@ -614,12 +619,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (threadIdx.x == 0) {
         for (int s = 0; s < P; ++s) {
             mbar_init(full_p(s), 1);
-            mbar_init(empty_p(s), kNumWorkWarps);
+            mbar_init(empty_p(s), kNumConvWarps + kNumEpiWarps);
         }
         for (int b = 0; b < kTmemBufs; ++b) {
             mbar_init(full_t(b), 1);
-            mbar_init(empty_t(b), kNumWorkWarps);
+            mbar_init(empty_t(b), kNumEpiWarps);
         }
+        for (int c = 0; c < kASlots; ++c) mbar_init(a_free(c), 1);
         *abort_flag = 0;
         *last_flag = 0;
         mbar_fence_init();
@@ -658,29 +664,19 @@ __global__ void __launch_bounds__(kThreads, 2)
         int j = 0;                           // CTA-local group counter
         int last_j[kTmemBufs];
         for (int b = 0; b < kTmemBufs; ++b) last_j[b] = -1;
-        int prev_first = 0;                  // first group of the previous k-block
         for (int i = 0; i < nkb; ++i) {
             const int c = i % kASlots, s = i % P;
-            // the whole warp: converted tile i is ready (barrier ids stay compile-time constants)
+            // the whole warp: converted tile i is ready, and so are the TMEM buffers of its groups (barrier ids stay
+            // compile-time constants)
             if (c == 0) named_bar_sync(kOperandBarrier0, kOperandThreads);
             else named_bar_sync(kOperandBarrier0 + 1, kOperandThreads);
             const int ng = groups_in(kb0 + i);
-            const int first = j;
             if (lane == 0) {
                 tc_fence_after_sync();
                 const uint32_t a_base = smem_addr(a_ring + c * kATileBytes);
                 const uint32_t b_base = smem_addr(p_ring + s * L.stage_bytes + L.b_off);
                 for (int gg = 0; gg < ng; ++gg) {
-                    const int jj = first + gg, b = jj % kTmemBufs;
-                    // a buffer last used two or more k-blocks back was read before the workers arrived above;
-                    // one used by the previous k-block (four buffers and G = 32 only) may still be read by its
-                    // epilogue. That wait ignores the abort flag: the workers keep releasing buffers regardless.
-                    if (jj - kTmemBufs >= prev_first &&
-                        !mbar_wait_drain(empty_t(b), ((jj / kTmemBufs) & 1) ^ 1)) {
-                        *abort_flag = 1;
-                        record_timeout(kSiteMmaTmemEmpty);
-                    }
-                    tc_fence_after_sync();
+                    const int jj = j + gg, b = jj % kTmemBufs;
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * C::kBufStride);
                     for (int ks = 0; ks < G / 32; ++ks) {
                         const uint32_t kofs = static_cast<uint32_t>(gg * G + ks * 32);
@@ -690,23 +686,56 @@ __global__ void __launch_bounds__(kThreads, 2)
                     umma_commit(full_t(b));
                     last_j[b] = jj;
                 }
+                umma_commit(a_free(c));      // slot c may be overwritten once these MMAs are done
             }
             __syncwarp();
-            prev_first = first;
-            j = first + ng;
+            j += ng;
         }
         // no MMA may still be writing TMEM when it is freed, nor arrive on a barrier after the CTA exits
-        if (lane == 0)
+        if (lane == 0) {
             for (int b = 0; b < kTmemBufs; ++b)
                 if (last_j[b] >= 0) mbar_wait_drain(full_t(b), (last_j[b] / kTmemBufs) & 1);
+            if (nkb > 0) mbar_wait_drain(a_free((nkb - 1) % kASlots), ((nkb - 1) / kASlots) & 1);
+        }
         __syncwarp();
+    } else if (warp < kEpiWarp0) {
+        // ================================================================ converters
+        const int ct = threadIdx.x - kConvWarp0 * 32;    // 0..127
+        bool ok = true;
+        int j = 0;                                       // CTA-local group counter
+        for (int i = 0; i < nkb; ++i) {
+            const int s = i % P, c = i % kASlots;
+            if (ok) ok = mbar_wait_warp(full_p(s), (i / P) & 1, abort_flag, kSiteConvFull);
+            // slot c is free once the MMAs of k-block i - 2 are done. Waited for even after a failure (bounded; the
+            // MMA warp never stops issuing), so that no arrival below counts towards an earlier phase.
+            const uint32_t par = ((i / kASlots) & 1) ^ 1;
+            if (ok) ok = mbar_wait_warp(a_free(c), par, abort_flag, kSiteConvEmpty);
+            if (!ok) {
+                bool drained = true;
+                if (lane == 0) drained = mbar_wait_drain(a_free(c), par);
+                (void)__shfl_sync(0xffffffffu, drained ? 1 : 0, 0);
+            }
+            // the TMEM buffers of this k-block's groups: their previous groups have been read by the epilogue
+            const int ng = groups_in(kb0 + i);
+            for (int gg = 0; gg < ng && ok; ++gg) {
+                const int jj = j + gg;
+                ok = mbar_wait_warp(empty_t(jj % kTmemBufs), ((jj / kTmemBufs) & 1) ^ 1, abort_flag, kSiteMmaTmemEmpty);
+            }
+            j += ng;
+            if (ok) {
+                convert_tile<kConvThreads>(p_ring + s * L.stage_bytes, a_ring + c * kATileBytes, ct);
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (c == 0) named_bar_arrive(kOperandBarrier0, kOperandThreads);
+            else named_bar_arrive(kOperandBarrier0 + 1, kOperandThreads);
+            if (ok && lane == 0) mbar_arrive(empty_p(s));   // the packed weights are read
+        }
     } else {
-        // ================================================================ workers
+        // ================================================================ epilogue
         pdl_wait();                                      // outputs are written after the preceding kernel ended
-        const int w = warp - kWorkWarp0;                 // 0..7
-        const int wt = threadIdx.x - kWorkWarp0 * 32;    // 0..255
+        const int et = threadIdx.x - kEpiWarp0 * 32;     // 0..127
         const int quarter = warp & 3;                    // TMEM lanes this warp may read
-        const int half = w >> 2;                         // rows [half * R, half * R + R)
         const int n_local = quarter * 32 + lane;
         const int n = nt * kTileN + n_local;
         const int rows_valid = min(p.m_sub, M - m0);
@@ -714,30 +743,19 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int r = 0; r < R; ++r) yacc[r] = 0.0f;
 
-        // Iteration i converts k-block i's weight tile, then runs the epilogue of k-block i - 1. After a failed wait
-        // the work is skipped, but every synchronisation with the MMA warp goes on.
+        // After a failed wait the work is skipped, but the MMAs' commits are still waited for (bounded) and the
+        // TMEM buffers released, so that the converters and the MMA warp go on.
         bool ok = true;
         int j = 0;
-        for (int i = 0; i <= nkb; ++i) {
-            if (i < nkb) {
-                const int s = i % P, c = i % kASlots;
-                ok = ok && mbar_wait_warp(full_p(s), (i / P) & 1, abort_flag, kSiteConvFull);
-                if (ok) {
-                    convert_tile256(p_ring + s * L.stage_bytes, a_ring + c * kATileBytes, wt);
-                    fence_proxy_async_smem();
-                }
-                __syncwarp();
-                if (c == 0) named_bar_arrive(kOperandBarrier0, kOperandThreads);
-                else named_bar_arrive(kOperandBarrier0 + 1, kOperandThreads);
-            }
-            const int ie = i - 1;                        // k-block whose epilogue runs now
-            if (ie < 0) continue;
-            const int se = ie % P;
-            const uint8_t *stage = p_ring + se * L.stage_bytes;
+        for (int i = 0; i < nkb; ++i) {
+            const int s = i % P;
+            // the stage landed before its tile was converted; seen here too, for the constants and scales
+            if (ok) ok = mbar_wait_warp(full_p(s), (i / P) & 1, abort_flag, kSiteEpiOperandsEmpty);
+            const uint8_t *stage = p_ring + s * L.stage_bytes;
             const float4 *cs = reinterpret_cast<const float4 *>(stage + L.c_off);
             const __half *ss = reinterpret_cast<const __half *>(stage + L.s_off);
             const __half *zs = reinterpret_cast<const __half *>(stage + L.z_off);
-            const int kb = kb0 + ie;
+            const int kb = kb0 + i;
             const int ng = groups_in(kb);
             for (int gg = 0; gg < ng; ++gg, ++j) {
                 const int b = j % kTmemBufs;
@@ -745,8 +763,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const float s_n = debug || !live ? 0.0f : __half2float(ss[gg * kTileN + n_local]);
                 const float f_n =
                     kZp && !debug && live ? fmaf(__half2float(zs[gg * kTileN + n_local]), 0.125f, 1.0f) : 1.0f;
-                // the MMAs' commit is waited for even after a failure (bounded), so that this warp never gets two
-                // phases ahead of the MMA warp on an operand barrier
                 if (!mbar_wait_warp(full_t(b), (j / kTmemBufs) & 1, abort_flag, kSiteEpiTmemFull)) {
                     ok = false;
                     bool drained = true;
@@ -774,29 +790,26 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (lane == 0) mbar_arrive(empty_t(b));
                 const float4 *cg = cs + gg * (kConstFloatsPerGroup / 4);
                 if (debug) {
-                    if (kb * gpk + gg == p.dbg_group && n < N) {
-                        if (half == 0) debug_rows<kMaxM, R, 0>(d, cg, rows_valid, p.dbg_y123, M, N, m0, n);
-                        else debug_rows<kMaxM, R, 1>(d, cg, rows_valid, p.dbg_y123, M, N, m0, n);
-                    }
+                    if (kb * gpk + gg == p.dbg_group && n < N)
+                        debug_rows<kMaxM, R, 0>(d, cg, rows_valid, p.dbg_y123, M, N, m0, n);
                     continue;
                 }
-                if (half == 0) combine_rows<kMaxM, R, 0, kZp>(d, cg, s_n, f_n, rows_valid, yacc);
-                else combine_rows<kMaxM, R, 1, kZp>(d, cg, s_n, f_n, rows_valid, yacc);
+                combine_rows<kMaxM, R, 0, kZp>(d, cg, s_n, f_n, rows_valid, yacc);
             }
             if (!ok) continue;
             // the k-block's MMAs have completed (its last full_t wait saw them) and its constants are read
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty_p(se));
+            if (lane == 0) mbar_arrive(empty_p(s));
         }
-        // all workers take the same path from here on (named barriers below)
-        ok = !named_bar_or(kWorkBarrierId, kWorkThreads, !ok);
+        // all epilogue warps take the same path from here on (named barriers below)
+        ok = !named_bar_or(kEpiBarrierId, kEpiThreads, !ok);
 
         if (ok && !debug) {
             const float bias_n = p.bias != nullptr && n < N ? __half2float(p.bias[n]) : 0.0f;
             if (p.reduce == kReduceNone) {
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    const int m = half * R + r;
+                    const int m = r;
                     if (m < rows_valid && n < N)
                         p.y[static_cast<size_t>(m0 + m) * N + n] =
                             __float2half_rn(p.bias != nullptr ? yacc[r] + bias_n : yacc[r]);
@@ -807,27 +820,26 @@ __global__ void __launch_bounds__(kThreads, 2)
                 float *red = reinterpret_cast<float *>(a_ring);
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    const int m = half * R + r;
+                    const int m = r;
                     if (m < kMaxM) red[m * kTileN + n_local] = yacc[r];
                 }
             } else {
                 float *part = p.ws_part + static_cast<size_t>(sp) * M * N;
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    const int m = half * R + r;
+                    const int m = r;
                     if (m < rows_valid && n < N) part[static_cast<size_t>(m0 + m) * N + n] = yacc[r];
                 }
                 __threadfence();
-                named_bar_sync(kWorkBarrierId, kWorkThreads);
-                if (wt == 0) {
+                named_bar_sync(kEpiBarrierId, kEpiThreads);
+                if (et == 0) {
                     const uint32_t prev = atomicAdd(p.ws_count + static_cast<size_t>(mt) * p.n_tiles + nt, 1u);
                     *last_flag = (prev == static_cast<uint32_t>(p.splits - 1));
                 }
-                named_bar_sync(kWorkBarrierId, kWorkThreads);
+                named_bar_sync(kEpiBarrierId, kEpiThreads);
                 if (*last_flag) {
                     __threadfence();
-                    // the two warps of a lane quarter take alternate rows
-                    for (int m = half; m < rows_valid && n < N; m += 2) {
+                    for (int m = 0; m < rows_valid && n < N; ++m) {
                         const float *src = p.ws_part + static_cast<size_t>(m0 + m) * N + n;
                         const size_t slice = static_cast<size_t>(M) * N;
                         float acc = 0.0f;
@@ -841,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         if (p.bias != nullptr) acc += bias_n;
                         p.y[static_cast<size_t>(m0 + m) * N + n] = __float2half_rn(acc);
                     }
-                    if (wt == 0) p.ws_count[static_cast<size_t>(mt) * p.n_tiles + nt] = 0u;
+                    if (et == 0) p.ws_count[static_cast<size_t>(mt) * p.n_tiles + nt] = 0u;
                 }
             }
         }
@@ -851,16 +863,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         // every thread of every CTA of the cluster takes part in both barriers (warps reconverged first)
         __syncwarp();
         cluster_sync_all();                                      // all partial sums are in shared memory
-        if (warp >= kWorkWarp0) {
-            const int half = (warp - kWorkWarp0) >> 2;
+        if (warp >= kEpiWarp0) {
             const int n_local = (warp & 3) * 32 + lane;
             const int n = nt * kTileN + n_local;
             const int rows_valid = min(p.m_sub, M - m0);
             const uint32_t red = smem_addr(a_ring);
-            // CTA r of the cluster finishes rows r, r + S, ... (alternating between the two warps of a lane
-            // quarter); every row sums the slices in slice order
-            for (int m = static_cast<int>(cluster_ctarank()) + half * p.splits; m < rows_valid && n < N;
-                 m += 2 * p.splits) {
+            // CTA r of the cluster finishes rows r, r + S, ...; every row sums the slices in slice order
+            for (int m = static_cast<int>(cluster_ctarank()); m < rows_valid && n < N; m += p.splits) {
                 float v[kMaxClusterSplits];
                 const uint32_t off = static_cast<uint32_t>((m * kTileN + n_local) * 4);
 #pragma unroll
