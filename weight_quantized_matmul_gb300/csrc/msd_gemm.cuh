@@ -7,11 +7,18 @@
 //                         per-(row, group) constants {c1 A_max, c2 A_max, c3 A_max, 8 sum_i c_i A_max S_i}
 //   msd_gemm_kernel       steps 9-11 for one 128-row x 128-column output tile per CTA: the planes are the MMA's A
 //                         operand (M = 128 rows of x), the int4 weights converted to E4M3 the B operand (N = 128
-//                         columns); each plane of each K-group accumulates in its own 128-column TMEM slot (four
-//                         slots rotate, so the next group's first plane overlaps the epilogue of this group)
+//                         columns); each plane of each K-group accumulates in its own 128-column TMEM slot, four
+//                         slots rotating
 // Roles in msd_gemm_kernel (384 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA issuer, warps 2-3 int4 ->
 // E4M3 converters (and fp16 -> fp32 scales), warps 4-11 epilogue (two warps per TMEM lane quarter, 64 columns each,
-// packed FP32x2 math).
+// packed FP32x2 math). The epilogue folds the planes of a group in one at a time (T = c1 D1 - corr, T += c2 D2,
+// T += c3 D3, y += scale T) and hands each plane's slot back as soon as it has read it, so the MMAs can run up to
+// three planes ahead of the epilogue.
+// Every wait of the MMA-issuing thread leaves the tensor pipe idle for hundreds of cycles (measured: ~700 per wait
+// when it waited once per plane, against ~75 per 128 x 128 x 32 MMA), so the MMA warp waits once per K-group, on a
+// hardware named barrier, for everything the group's three planes need: the converters arrive there once the weights
+// are converted and the epilogue has released the group's three TMEM slots. The MMA warp never gives up a wait;
+// after a failed wait the other roles skip their work but keep every arrival, in order, so nothing waits forever.
 #pragma once
 
 #include "msd_kernels.cuh"
@@ -27,6 +34,15 @@ constexpr int kGemmEpiWarp0 = 4;
 constexpr int kGemmNumEpiWarps = 8;
 constexpr int kGemmBStages = 2;
 constexpr int kGemmSlots = 4;                                  // TMEM accumulator slots of 128 columns
+constexpr int kGemmGroupBar0 = 2;                              // named barriers 2, 3: even / odd K-group ready
+constexpr int kGemmGroupBarThreads = kGemmNumConvWarps * 32 + 32;
+// Registers: launched with 168 per thread (384 x 168 = 64512); warps 0-3 (producer, MMA, converters) then give up
+// to 96 and the two epilogue warpgroups take 200: 128 x 96 + 256 x 200 = 63488.
+constexpr int kGemmLaunchRegs = 168;
+constexpr uint32_t kGemmRolesRegs = 96;
+constexpr uint32_t kGemmEpiRegs = 200;
+static_assert(128 * kGemmRolesRegs + (kGemmThreads - 128) * kGemmEpiRegs <= kGemmThreads * kGemmLaunchRegs,
+              "register split above the launch allocation");
 constexpr int kPlaneImageBytes = kGemmTileM * kKBlock;         // 16384: one plane of one k-block
 constexpr int kGemmConstRowBytes = 16;                         // float4 per (row, group)
 constexpr int kGemmSmemLimit = 232448;                         // opt-in shared memory per CTA on sm_103
@@ -55,7 +71,7 @@ struct GemmLayout {
         p_stages = (kGemmSmemLimit - fixed) / stage_bytes;
         if (p_stages > 3) p_stages = 3;
         off_bar = off_p + p_stages * stage_bytes;
-        off_misc = off_bar + 8 * (3 * 3 + 2 * kGemmBStages + 2 * kGemmSlots);
+        off_misc = off_bar + 8 * (3 * 3 + kGemmBStages + 2 * kGemmSlots);
         smem_bytes = off_misc + 64 + 1024;
     }
 };
@@ -143,15 +159,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // barriers: full_p / empty_p  load stage landed / released (MMAs done with the planes, converters with the
     //                             weights, epilogue with constants and scales)
     //           sready            scales of the stage converted to fp32 (the epilogue's view of the stage)
-    //           bfull / bfree     converted weight tile ready / consumed by the MMAs
-    //           tfull / tfree     TMEM slot written by the MMAs / read by the epilogue
+    //           bfree             converted weight stage consumed by the MMAs (their commit)
+    //           tfull / trel      TMEM slot written by the MMAs (their commit) / read by the epilogue
+    // and the named barriers kGemmGroupBar0 + (j & 1): everything K-group j of the CTA needs is ready (the converters
+    // arrive, the MMA warp waits).
     auto full_p = [&](int s) { return bar0 + 8u * s; };
     auto empty_p = [&](int s) { return bar0 + 8u * (3 + s); };
     auto sready = [&](int s) { return bar0 + 8u * (6 + s); };
-    auto bfull = [&](int c) { return bar0 + 8u * (9 + c); };
-    auto bfree = [&](int c) { return bar0 + 8u * (9 + kGemmBStages + c); };
-    auto tfull = [&](int t) { return bar0 + 8u * (9 + 2 * kGemmBStages + t); };
-    auto tfree = [&](int t) { return bar0 + 8u * (9 + 2 * kGemmBStages + kGemmSlots + t); };
+    auto bfree = [&](int c) { return bar0 + 8u * (9 + c); };
+    auto tfull = [&](int t) { return bar0 + 8u * (9 + kGemmBStages + t); };
+    auto trel = [&](int t) { return bar0 + 8u * (9 + kGemmBStages + kGemmSlots + t); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.off_misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.off_misc + 4);
 
@@ -163,7 +180,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int kb0 = kDebug ? p.dbg_group * G / kKBlock : 0;
     const int nkb = kDebug ? 1 : p.kb_total;
 
-    auto groups_in = [&](int kb) { return (min(K, (kb + 1) * kKBlock) - kb * kKBlock) / G; };
+    const int gshift = 31 - __clz(G);                  // G is 32, 64 or 128
+    auto groups_in = [&](int kb) { return (min(K, (kb + 1) * kKBlock) - kb * kKBlock) >> gshift; };
+    // plane-accumulation units of this CTA: three per group, unit u in TMEM slot u % kGemmSlots
+    const int total_units = 3 * (kDebug ? groups_in(kb0) : Gn);
     auto stage_tx = [&](int kb) {
         return static_cast<uint32_t>(3 * kPlaneImageBytes + kPackedTileBytes + groups_in(kb) * kGemmTileM * 16 +
                                      (kDebug ? 0 : (kZp ? 2 : 1) * gpk * kGemmTileN * 2));
@@ -186,6 +206,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         bulk_g2s(dst + L.off_const, p.consts + (static_cast<size_t>(mt) * Gn + kb * gpk) * kGemmTileM,
                  groups_in(kb) * kGemmTileM * 16, full_p(s), pol_keep);
     };
+    // named barrier of K-group j, with compile-time ids
+    auto group_bar = [&](int j, bool wait) {
+        if (wait) {
+            if ((j & 1) == 0) named_bar_sync(kGemmGroupBar0, kGemmGroupBarThreads);
+            else named_bar_sync(kGemmGroupBar0 + 1, kGemmGroupBarThreads);
+        } else {
+            if ((j & 1) == 0) named_bar_arrive(kGemmGroupBar0, kGemmGroupBarThreads);
+            else named_bar_arrive(kGemmGroupBar0 + 1, kGemmGroupBarThreads);
+        }
+    };
 
     const int first = nkb < P ? nkb : P;
     uint64_t pol_stream = 0, pol_keep = 0;
@@ -195,13 +225,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(empty_p(s), 1 + kGemmNumConvWarps + kGemmNumEpiWarps);
             mbar_init(sready(s), kGemmNumConvWarps);
         }
-        for (int c = 0; c < kGemmBStages; ++c) {
-            mbar_init(bfull(c), kGemmNumConvWarps);
-            mbar_init(bfree(c), 1);
-        }
+        for (int c = 0; c < kGemmBStages; ++c) mbar_init(bfree(c), 1);
         for (int t = 0; t < kGemmSlots; ++t) {
             mbar_init(tfull(t), 1);
-            mbar_init(tfree(t), kGemmNumEpiWarps);
+            mbar_init(trel(t), kGemmNumEpiWarps);
         }
         *abort_flag = 0;
         mbar_fence_init();
@@ -223,7 +250,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 0) {
+    if (warp < kGemmEpiWarp0) {
+      regs_release<kGemmRolesRegs>();
+      if (warp == 0) {
         // ================================================================ TMA producer
         if (lane == 0) {
             int issued = first;
@@ -235,30 +264,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             for (int j = issued > P ? issued - P : 0; j < issued; ++j) mbar_wait_drain(full_p(j % P), (j / P) & 1);
         }
-    } else if (warp == 1) {
-        // ================================================================ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = (1u << 4) | (static_cast<uint32_t>(kGemmTileN >> 3) << 17) |
-                                       (static_cast<uint32_t>(kGemmTileM >> 4) << 24);
-            int u = 0;                                   // plane-accumulation unit counter (3 per group)
-            int last_u[kGemmSlots] = {-1, -1, -1, -1};
-            bool stop = false;
-            for (int i = 0; i < nkb && !stop; ++i) {
-                const int s = i % P, cb = i % kGemmBStages;
-                if (!mbar_wait(full_p(s), (i / P) & 1, abort_flag, kSiteMmaOperands)) break;
-                if (!mbar_wait(bfull(cb), (i / kGemmBStages) & 1, abort_flag, kSiteMmaOperands)) break;
-                tc_fence_after_sync();
-                const uint32_t plane_base = smem_addr(p_ring + s * L.stage_bytes);
-                const uint32_t w_base = smem_addr(b_ring + cb * (kGemmTileN * kKBlock));
-                const int ng = groups_in(kb0 + i);
-                for (int gg = 0; gg < ng && !stop; ++gg) {
-                    for (int pl = 0; pl < 3; ++pl, ++u) {
-                        const int t = u % kGemmSlots;
-                        if (!mbar_wait(tfree(t), ((u / kGemmSlots) & 1) ^ 1, abort_flag, kSiteMmaTmemEmpty)) {
-                            stop = true;
-                            break;
-                        }
-                        tc_fence_after_sync();
+      } else if (warp == 1) {
+        // ================================================================ MMA issuer (the whole warp takes the
+        // named barriers, lane 0 issues)
+        constexpr uint32_t idesc = (1u << 4) | (static_cast<uint32_t>(kGemmTileN >> 3) << 17) |
+                                   (static_cast<uint32_t>(kGemmTileM >> 4) << 24);
+        int j = 0;                                       // K-group counter of the CTA
+        for (int i = 0; i < nkb; ++i) {
+            const int s = i % P, cb = i % kGemmBStages;
+            const uint32_t plane_base = smem_addr(p_ring + s * L.stage_bytes);
+            const uint32_t w_base = smem_addr(b_ring + cb * (kGemmTileN * kKBlock));
+            const int ng = groups_in(kb0 + i);
+            for (int gg = 0; gg < ng; ++gg, ++j) {
+                // the weights of k-block i are converted (so its stage has landed) and the three TMEM slots of
+                // group j have been read
+                group_bar(j, true);
+                if (lane == 0) {
+                    tc_fence_after_sync();
+                    for (int pl = 0; pl < 3; ++pl) {
+                        const int t = (3 * j + pl) % kGemmSlots;
                         const uint32_t d = tmem_base + static_cast<uint32_t>(t * kGemmTileN);
                         for (int ks = 0; ks < G / 32; ++ks) {
                             const uint32_t kofs = static_cast<uint32_t>(gg * G + ks * 32);
@@ -266,51 +290,83 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                         sdesc_kmajor_sw128(w_base + kofs), idesc, ks > 0 ? 1u : 0u);
                         }
                         umma_commit(tfull(t));
-                        last_u[t] = u;
                     }
                 }
-                if (stop) break;
+                __syncwarp();
+            }
+            if (lane == 0) {
                 umma_commit(bfree(cb));
                 umma_commit(empty_p(s));
             }
-            for (int t = 0; t < kGemmSlots; ++t)
-                if (last_u[t] >= 0) mbar_wait_drain(tfull(t), (last_u[t] / kGemmSlots) & 1);
+            __syncwarp();
         }
+        // no MMA may still be writing TMEM when it is freed, nor arrive on a barrier after the CTA exits
+        if (lane == 0)
+            for (int v = total_units > kGemmSlots ? total_units - kGemmSlots : 0; v < total_units; ++v)
+                mbar_wait_drain(tfull(v % kGemmSlots), (v / kGemmSlots) & 1);
         __syncwarp();
-    } else if (warp < kGemmEpiWarp0) {
+      } else {
         // ================================================================ int4 -> E4M3 converters, scales to fp32
         const int ct = threadIdx.x - kGemmConvWarp0 * 32;
         constexpr int kConvThreads = kGemmNumConvWarps * 32;
+        bool ok = true;
+        int j = 0;                                       // K-group counter of the CTA
         for (int i = 0; i < nkb; ++i) {
             const int s = i % P, cb = i % kGemmBStages;
-            if (!mbar_wait_warp(full_p(s), (i / P) & 1, abort_flag, kSiteConvFull)) break;
+            if (ok) ok = mbar_wait_warp(full_p(s), (i / P) & 1, abort_flag, kSiteConvFull);
             uint8_t *stage = p_ring + s * L.stage_bytes;
-            if (!kDebug) {
+            if (ok && !kDebug) {
                 const __half2 *s16 = reinterpret_cast<const __half2 *>(stage + L.off_scale);
                 float2 *s32 = reinterpret_cast<float2 *>(stage + L.off_scale32);
-                for (int j = ct; j < gpk * kGemmTileN / 2; j += kConvThreads) s32[j] = __half22float2(s16[j]);
+                for (int e = ct; e < gpk * kGemmTileN / 2; e += kConvThreads) s32[e] = __half22float2(s16[e]);
                 if constexpr (kZp) {
                     const __half2 *z16 = reinterpret_cast<const __half2 *>(stage + L.off_zp);
                     float2 *z32 = reinterpret_cast<float2 *>(stage + L.off_zp32);
-                    for (int j = ct; j < gpk * kGemmTileN / 2; j += kConvThreads) {
-                        const float2 z = __half22float2(z16[j]);
-                        z32[j] = make_float2(fmaf(z.x, 0.125f, 1.0f), fmaf(z.y, 0.125f, 1.0f));
+                    for (int e = ct; e < gpk * kGemmTileN / 2; e += kConvThreads) {
+                        const float2 z = __half22float2(z16[e]);
+                        z32[e] = make_float2(fmaf(z.x, 0.125f, 1.0f), fmaf(z.y, 0.125f, 1.0f));
                     }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sready(s));
             }
-            if (!mbar_wait_warp(bfree(cb), ((i / kGemmBStages) & 1) ^ 1, abort_flag, kSiteConvEmpty)) break;
-            convert_tile<kConvThreads>(stage + 3 * kPlaneImageBytes, b_ring + cb * (kGemmTileN * kKBlock), ct);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(bfull(cb));
-                mbar_arrive(empty_p(s));
+            // the weight stage is free once the MMAs of k-block i - 2 are done. Waited for even after a failure
+            // (bounded; the MMA warp never stops issuing), so that this warp never arrives on a group barrier
+            // twice before the MMA warp has waited there once.
+            const uint32_t par = ((i / kGemmBStages) & 1) ^ 1;
+            if (ok) ok = mbar_wait_warp(bfree(cb), par, abort_flag, kSiteConvEmpty);
+            if (!ok) {
+                bool drained = true;
+                if (lane == 0) drained = mbar_wait_drain(bfree(cb), par);
+                (void)__shfl_sync(0xffffffffu, drained ? 1 : 0, 0);
             }
+            if (ok) {
+                convert_tile<kConvThreads>(stage + 3 * kPlaneImageBytes, b_ring + cb * (kGemmTileN * kKBlock), ct);
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            // per K-group: its three planes go to slots last used by units 3j - 4 .. 3j - 2, which the epilogue
+            // releases in order. Waited for even after a failure, for the same reason as above.
+            const int ng = groups_in(kb0 + i);
+            for (int gg = 0; gg < ng; ++gg, ++j) {
+                const int v = 3 * j - 2;
+                if (v >= 0) {
+                    const uint32_t vpar = (v / kGemmSlots) & 1;
+                    if (ok) ok = mbar_wait_warp(trel(v % kGemmSlots), vpar, abort_flag, kSiteConvEmpty);
+                    if (!ok) {
+                        bool drained = true;
+                        if (lane == 0) drained = mbar_wait_drain(trel(v % kGemmSlots), vpar);
+                        (void)__shfl_sync(0xffffffffu, drained ? 1 : 0, 0);
+                    }
+                }
+                group_bar(j, false);
+            }
+            if (ok && lane == 0) mbar_arrive(empty_p(s));
         }
+      }
     } else {
         // ================================================================ epilogue
+        regs_claim<kGemmEpiRegs>();
         pdl_wait();
         const int ew = warp - kGemmEpiWarp0;             // 0..7
         const int quarter = warp & 3;                    // TMEM lanes (rows) this warp may read
@@ -322,97 +378,174 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
         for (int q = 0; q < 32; ++q) yacc[q] = make_float2(0.0f, 0.0f);
         bool ok = true;
+        // waits for the MMAs of unit uu; after a failure it still waits (bounded, the MMA warp never stops issuing)
+        // so that no release runs ahead of the MMAs it frees the slot from
+        auto wait_unit = [&](int uu) {
+            const int t = uu % kGemmSlots;
+            const uint32_t par = (uu / kGemmSlots) & 1;
+            if (ok) ok = mbar_wait_warp(tfull(t), par, abort_flag, kSiteEpiTmemFull);
+            if (!ok) {
+                bool drained = true;
+                if (lane == 0) drained = mbar_wait_drain(tfull(t), par);
+                (void)__shfl_sync(0xffffffffu, drained ? 1 : 0, 0);
+            }
+        };
+        // 32 columns of the warp's lane quarter: two loads in flight per wait
+        auto ld32 = [&](uint32_t taddr, uint32_t(&dd)[2][16]) {
+            tmem_ld16(taddr, dd[0]);
+            tmem_ld16(taddr + 16, dd[1]);
+            tmem_wait_ld();
+            reg_fence16(dd[0]);
+            reg_fence16(dd[1]);
+        };
+        auto release_unit = [&](int uu) {
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(trel(uu % kGemmSlots));
+        };
         int u = 0;
-        for (int i = 0; i < nkb && ok; ++i) {
+        for (int i = 0; i < nkb; ++i) {
             const int s = i % P, kb = kb0 + i;
             // the epilogue reads constants (landed with the stage) and fp32 scales (written by the converters)
-            ok = kDebug ? mbar_wait_warp(full_p(s), (i / P) & 1, abort_flag, kSiteEpiOperandsEmpty)
-                        : mbar_wait_warp(sready(s), (i / P) & 1, abort_flag, kSiteEpiOperandsEmpty);
-            if (!ok) break;
+            if (ok)
+                ok = kDebug ? mbar_wait_warp(full_p(s), (i / P) & 1, abort_flag, kSiteEpiOperandsEmpty)
+                            : mbar_wait_warp(sready(s), (i / P) & 1, abort_flag, kSiteEpiOperandsEmpty);
             const uint8_t *stage = p_ring + s * L.stage_bytes;
             const int ng = groups_in(kb);
             for (int gg = 0; gg < ng; ++gg, u += 3) {
-                const float4 cr = reinterpret_cast<const float4 *>(stage + L.off_const)[gg * kGemmTileM + r];
-                const int t0 = u % kGemmSlots, t1 = (u + 1) % kGemmSlots, t2 = (u + 2) % kGemmSlots;
-                // the three planes were committed in order: the last one's completion covers all three
-                ok = mbar_wait_warp(tfull(t2), ((u + 2) / kGemmSlots) & 1, abort_flag, kSiteEpiTmemFull);
-                if (!ok) break;
-                tc_fence_after_sync();
-                const uint32_t a0 = tmem_base + lane_off + static_cast<uint32_t>(t0 * kGemmTileN + half * 64);
-                const uint32_t a1p = tmem_base + lane_off + static_cast<uint32_t>(t1 * kGemmTileN + half * 64);
-                const uint32_t a2p = tmem_base + lane_off + static_cast<uint32_t>(t2 * kGemmTileN + half * 64);
+                const float4 cr = ok ? reinterpret_cast<const float4 *>(stage + L.off_const)[gg * kGemmTileM + r]
+                                     : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                 if (kDebug) {
-                    if (kb * gpk + gg == p.dbg_group) {
+                    // warp-uniform: tcgen05.ld is executed by the whole warp; rows past M only skip the stores
+                    const bool here = kb * gpk + gg == p.dbg_group;
+                    const float splane[3] = {cr.x, cr.y, cr.z};   // debug records hold the plane sums
 #pragma unroll 1
-                        for (int ch = 0; ch < 4; ++ch) {
-                            uint32_t d1[16], d2[16], d3[16];
-                            tmem_ld16(a0 + ch * 16, d1);
-                            tmem_ld16(a1p + ch * 16, d2);
-                            tmem_ld16(a2p + ch * 16, d3);
-                            tmem_wait_ld();
-                            if (m < M) {
+                    for (int pl = 0; pl < 3; ++pl) {
+                        const int t = (u + pl) % kGemmSlots;
+                        wait_unit(u + pl);
+                        if (ok && here) {
+                            tc_fence_after_sync();
+                            const uint32_t a = tmem_base + lane_off + static_cast<uint32_t>(t * kGemmTileN + half * 64);
+#pragma unroll 1
+                            for (int ch = 0; ch < 4; ++ch) {
+                                uint32_t d[16];
+                                tmem_ld16(a + ch * 16, d);
+                                tmem_wait_ld();
+                                reg_fence16(d);
                                 for (int q = 0; q < 16; ++q) {
                                     const int n = nt * kGemmTileN + half * 64 + ch * 16 + q;
-                                    if (n < N) {
-                                        // in debug runs the constant record holds the plane sums
-                                        p.dbg_y123[(static_cast<size_t>(0) * M + m) * N + n] =
-                                            __float2int_rn(kMmaUnit * __uint_as_float(d1[q]) - 8.0f * cr.x);
-                                        p.dbg_y123[(static_cast<size_t>(1) * M + m) * N + n] =
-                                            __float2int_rn(kMmaUnit * __uint_as_float(d2[q]) - 8.0f * cr.y);
-                                        p.dbg_y123[(static_cast<size_t>(2) * M + m) * N + n] =
-                                            __float2int_rn(kMmaUnit * __uint_as_float(d3[q]) - 8.0f * cr.z);
-                                    }
+                                    if (m < M && n < N)
+                                        p.dbg_y123[(static_cast<size_t>(pl) * M + m) * N + n] =
+                                            __float2int_rn(kMmaUnit * __uint_as_float(d[q]) - 8.0f * splane[pl]);
                                 }
                             }
                         }
+                        release_unit(u + pl);
                     }
-                } else {
-                    const float2 c1 = make_float2(cr.x, cr.x), c2 = make_float2(cr.y, cr.y);
-                    const float2 c3 = make_float2(cr.z, cr.z), nc = make_float2(-cr.w, -cr.w);
-                    const float4 *srow =
-                        reinterpret_cast<const float4 *>(stage + L.off_scale32) + (gg * kGemmTileN + half * 64) / 4;
-                    const float4 *zrow =
-                        reinterpret_cast<const float4 *>(stage + L.off_zp32) + (gg * kGemmTileN + half * 64) / 4;
+                    continue;
+                }
+                const float4 *srow =
+                    reinterpret_cast<const float4 *>(stage + L.off_scale32) + (gg * kGemmTileN + half * 64) / 4;
+                const float4 *zrow =
+                    reinterpret_cast<const float4 *>(stage + L.off_zp32) + (gg * kGemmTileN + half * 64) / 4;
+                float2 T[32];
+                // plane 1: T = c1 D1 - corr (times 1 + zp / 8 per column with zero points)
+                {
+                    const int t = u % kGemmSlots;
+                    wait_unit(u);
+                    if (ok) {
+                        tc_fence_after_sync();
+                        const uint32_t a = tmem_base + lane_off + static_cast<uint32_t>(t * kGemmTileN + half * 64);
+                        const float2 c1 = make_float2(cr.x, cr.x), nc = make_float2(-cr.w, -cr.w);
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        uint32_t d1[16], d2[16], d3[16];
-                        tmem_ld16(a0 + ch * 16, d1);
-                        tmem_ld16(a1p + ch * 16, d2);
-                        tmem_ld16(a2p + ch * 16, d3);
-                        tmem_wait_ld();
+                        for (int ch2 = 0; ch2 < 2; ++ch2) {
+                          uint32_t dd[2][16];
+                          ld32(a + ch2 * 32, dd);
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const float4 sc = srow[ch * 4 + q4];           // same address in every lane: broadcast
-                            float4 zf = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
-                            if constexpr (kZp) zf = zrow[ch * 4 + q4];
+                          for (int sub = 0; sub < 2; ++sub) {
+                            const int ch = ch2 * 2 + sub;
+                            const uint32_t(&d)[16] = dd[sub];
 #pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                const int q = q4 * 2 + h;
-                                const float2 scv = h == 0 ? make_float2(sc.x, sc.y) : make_float2(sc.z, sc.w);
-                                const float2 v1 = make_float2(__uint_as_float(d1[2 * q]), __uint_as_float(d1[2 * q + 1]));
-                                const float2 v2 = make_float2(__uint_as_float(d2[2 * q]), __uint_as_float(d2[2 * q + 1]));
-                                const float2 v3 = make_float2(__uint_as_float(d3[2 * q]), __uint_as_float(d3[2 * q + 1]));
-                                float2 ncz = nc;
-                                if constexpr (kZp)
-                                    ncz = __fmul2_rn(nc, h == 0 ? make_float2(zf.x, zf.y) : make_float2(zf.z, zf.w));
-                                float2 acc = __ffma2_rn(c1, v1, ncz);
-                                acc = __ffma2_rn(c2, v2, acc);
-                                acc = __ffma2_rn(c3, v3, acc);
-                                yacc[ch * 8 + q] = __ffma2_rn(scv, acc, yacc[ch * 8 + q]);
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                float4 zf = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+                                if constexpr (kZp) zf = zrow[ch * 4 + q4];
+#pragma unroll
+                                for (int h = 0; h < 2; ++h) {
+                                    const int q = q4 * 2 + h;
+                                    const float2 v = make_float2(__uint_as_float(d[2 * q]), __uint_as_float(d[2 * q + 1]));
+                                    float2 ncz = nc;
+                                    if constexpr (kZp)
+                                        ncz = __fmul2_rn(nc, h == 0 ? make_float2(zf.x, zf.y) : make_float2(zf.z, zf.w));
+                                    T[ch * 8 + q] = __ffma2_rn(c1, v, ncz);
+                                }
                             }
+                          }
                         }
                     }
+                    release_unit(u);
                 }
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(tfree(t0));
-                    mbar_arrive(tfree(t1));
-                    mbar_arrive(tfree(t2));
+                // plane 2: T += c2 D2
+                {
+                    const int t = (u + 1) % kGemmSlots;
+                    wait_unit(u + 1);
+                    if (ok) {
+                        tc_fence_after_sync();
+                        const uint32_t a = tmem_base + lane_off + static_cast<uint32_t>(t * kGemmTileN + half * 64);
+                        const float2 c2 = make_float2(cr.y, cr.y);
+#pragma unroll
+                        for (int ch2 = 0; ch2 < 2; ++ch2) {
+                          uint32_t dd[2][16];
+                          ld32(a + ch2 * 32, dd);
+#pragma unroll
+                          for (int sub = 0; sub < 2; ++sub) {
+                            const int ch = ch2 * 2 + sub;
+                            const uint32_t(&d)[16] = dd[sub];
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                T[ch * 8 + q] = __ffma2_rn(
+                                    c2, make_float2(__uint_as_float(d[2 * q]), __uint_as_float(d[2 * q + 1])),
+                                    T[ch * 8 + q]);
+                          }
+                        }
+                    }
+                    release_unit(u + 1);
+                }
+                // plane 3: T += c3 D3, then y += scale T
+                {
+                    const int t = (u + 2) % kGemmSlots;
+                    wait_unit(u + 2);
+                    if (ok) {
+                        tc_fence_after_sync();
+                        const uint32_t a = tmem_base + lane_off + static_cast<uint32_t>(t * kGemmTileN + half * 64);
+                        const float2 c3 = make_float2(cr.z, cr.z);
+#pragma unroll
+                        for (int ch2 = 0; ch2 < 2; ++ch2) {
+                          uint32_t dd[2][16];
+                          ld32(a + ch2 * 32, dd);
+#pragma unroll
+                          for (int sub = 0; sub < 2; ++sub) {
+                            const int ch = ch2 * 2 + sub;
+                            const uint32_t(&d)[16] = dd[sub];
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                const float4 sc = srow[ch * 4 + q4];           // same address in every lane: broadcast
+#pragma unroll
+                                for (int h = 0; h < 2; ++h) {
+                                    const int q = q4 * 2 + h;
+                                    const float2 v = make_float2(__uint_as_float(d[2 * q]), __uint_as_float(d[2 * q + 1]));
+                                    const float2 tq = __ffma2_rn(c3, v, T[ch * 8 + q]);
+                                    const float2 scv = h == 0 ? make_float2(sc.x, sc.y) : make_float2(sc.z, sc.w);
+                                    yacc[ch * 8 + q] = __ffma2_rn(scv, tq, yacc[ch * 8 + q]);
+                                }
+                            }
+                          }
+                        }
+                    }
+                    release_unit(u + 2);
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty_p(s));
+            if (ok && lane == 0) mbar_arrive(empty_p(s));
         }
         if (!kDebug && ok && m < M) {
             __half *yrow = p.y + static_cast<size_t>(m) * N;

@@ -586,7 +586,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     // One load stage: the k-block's packed weight tile, planes image, constants, scale tile and zero-point tile, all
     // counted on full_p(s).
     const uint8_t *w_src = p.w + (static_cast<size_t>(nt) * p.kb_total + kb0) * kPackedTileBytes;
-    auto groups_in = [&](int kb) { return (min(K, (kb + 1) * kKBlock) - kb * kKBlock) / G; };
+    const int gshift = 31 - __clz(G);                  // G is 32, 64 or 128
+    auto groups_in = [&](int kb) { return (min(K, (kb + 1) * kKBlock) - kb * kKBlock) >> gshift; };
     auto stage_tx = [&](int kb) {
         return static_cast<uint32_t>(kPackedTileBytes + C::kBTileBytes + groups_in(kb) * kConstFloatsPerGroup * 4 +
                                      (debug ? 0 : (kZp ? 2 : 1) * gpk * kTileN * 2));

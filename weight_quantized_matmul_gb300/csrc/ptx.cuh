@@ -112,6 +112,19 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
     return true;
 }
 
+// ------------------------------------------------------------------------------------------------ register split
+
+// Warpgroup-wide change of the per-thread register allocation. The increases of a CTA are granted from what the
+// decreases release, within the registers the CTA was launched with: the caller keeps the sum within that.
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_release() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_claim() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // ------------------------------------------------------------------------------------------------ named barriers
 
 // Arrival on a named barrier without waiting (the warp must be converged); completes when `nthreads` threads,

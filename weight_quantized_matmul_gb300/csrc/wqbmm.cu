@@ -322,6 +322,15 @@ wqbmm_status launch_large(const Shape &s, const Plan &plan, const Operands &op, 
                 cudaFuncSetAttribute(msd_gemm_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kGemmSmemLimit) != cudaSuccess)
                 return WQBMM_ERR_CUDA;
+            // the kernel's register split assumes the launch allocation it was written for: with any other, a
+            // warpgroup's claim could wait forever, so the kernel is not launched at all
+            for (const void *fn : {reinterpret_cast<const void *>(msd_gemm_kernel<false, false>),
+                                   reinterpret_cast<const void *>(msd_gemm_kernel<false, true>),
+                                   reinterpret_cast<const void *>(msd_gemm_kernel<true, false>)}) {
+                cudaFuncAttributes fa{};
+                if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess || fa.numRegs != kGemmLaunchRegs)
+                    return WQBMM_ERR_CUDA;
+            }
             info->gemm_smem_set = true;
         }
     }
