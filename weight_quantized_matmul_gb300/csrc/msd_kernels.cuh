@@ -67,15 +67,14 @@ constexpr float kC1 = static_cast<float>(1.0 / 7.49);
 constexpr float kC2 = static_cast<float>(1.0 / (7.49 * 14.98));
 constexpr float kC3 = static_cast<float>(1.0 / (7.49 * 14.98 * 14.98));
 
-// Wait-site ids recorded with a timeout
+// Wait-site ids recorded with a timeout (4 is no longer used: the MMA warps wait only on named barriers)
 enum WaitSite : int {
-    kSiteProducerEmpty = 1,
-    kSiteConvFull = 2,
-    kSiteConvEmpty = 3,
-    kSiteMmaOperands = 4,
-    kSiteMmaTmemEmpty = 5,
-    kSiteEpiOperandsEmpty = 6,
-    kSiteEpiTmemFull = 7,
+    kSiteProducerEmpty = 1,     // a load stage to be released
+    kSiteConvFull = 2,          // a load stage to land
+    kSiteConvEmpty = 3,         // a converted-weight slot (or TMEM slot, large M) to be free
+    kSiteTmemEmpty = 5,         // a TMEM accumulator to be read by the epilogue
+    kSiteEpiOperandsEmpty = 6,  // the epilogue's constants and scales
+    kSiteEpiTmemFull = 7,       // a TMEM accumulator to be written
     kSiteDebugWait = 9,
 };
 
@@ -720,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int ng = groups_in(kb0 + i);
             for (int gg = 0; gg < ng && ok; ++gg) {
                 const int jj = j + gg;
-                ok = mbar_wait_warp(empty_t(jj % kTmemBufs), ((jj / kTmemBufs) & 1) ^ 1, abort_flag, kSiteMmaTmemEmpty);
+                ok = mbar_wait_warp(empty_t(jj % kTmemBufs), ((jj / kTmemBufs) & 1) ^ 1, abort_flag, kSiteTmemEmpty);
             }
             j += ng;
             if (ok) {
