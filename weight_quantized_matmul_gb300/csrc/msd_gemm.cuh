@@ -472,10 +472,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                                 for (int h = 0; h < 2; ++h) {
                                     const int q = q4 * 2 + h;
-                                    const float2 v = make_float2(__uint_as_float(d[2 * q]), __uint_as_float(d[2 * q + 1]));
+                                    const float2 v =
+                                        make_float2(__uint_as_float(d[2 * q]), __uint_as_float(d[2 * q + 1]));
                                     float2 ncz = nc;
                                     if constexpr (kZp)
-                                        ncz = __fmul2_rn(nc, h == 0 ? make_float2(zf.x, zf.y) : make_float2(zf.z, zf.w));
+                                        ncz = __fmul2_rn(nc, h == 0 ? make_float2(zf.x, zf.y)
+                                                                    : make_float2(zf.z, zf.w));
                                     T[ch * 8 + q] = __ffma2_rn(c1, v, ncz);
                                 }
                             }
@@ -532,7 +534,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                                 for (int h = 0; h < 2; ++h) {
                                     const int q = q4 * 2 + h;
-                                    const float2 v = make_float2(__uint_as_float(d[2 * q]), __uint_as_float(d[2 * q + 1]));
+                                    const float2 v =
+                                        make_float2(__uint_as_float(d[2 * q]), __uint_as_float(d[2 * q + 1]));
                                     const float2 tq = __ffma2_rn(c3, v, T[ch * 8 + q]);
                                     const float2 scv = h == 0 ? make_float2(sc.x, sc.y) : make_float2(sc.z, sc.w);
                                     yacc[ch * 8 + q] = __ffma2_rn(scv, tq, yacc[ch * 8 + q]);

@@ -204,7 +204,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvPar
                 const int g = ((kw0 + j) * kKBlock + chunk * 32) >> gshift;
                 const bool in = j < nkb && g < Gn;
                 const size_t row_at = static_cast<size_t>(g) * p.group_stride + n_a;
-                sab[j] = in && n_a < N ? __ldg(reinterpret_cast<const __half2 *>(p.scale + row_at)) : __half2(0.0f, 0.0f);
+                sab[j] = in && n_a < N ? __ldg(reinterpret_cast<const __half2 *>(p.scale + row_at))
+                                       : __half2(0.0f, 0.0f);
                 if constexpr (kZp) {
                     const bool first = in && n_a < N && (chunk & (lpg_chunks - 1)) == 0;
                     zab[j] = first ? __ldg(reinterpret_cast<const __half2 *>(p.zp + row_at)) : __half2(0.0f, 0.0f);
@@ -250,8 +251,9 @@ __global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvPar
 #pragma unroll
                             for (int q = 0; q < 3; ++q) {
                                 const int sq = __float2int_rn(sv[q]);
-                                if (n_a < N) p.dbg_y123[(static_cast<size_t>(q) * p.M + m) * N + n_a] = da[q] / 16 - 8 * sq;
-                                if (n_b < N) p.dbg_y123[(static_cast<size_t>(q) * p.M + m) * N + n_b] = db[q] / 16 - 8 * sq;
+                                int32_t *dst = p.dbg_y123 + (static_cast<size_t>(q) * p.M + m) * N;
+                                if (n_a < N) dst[n_a] = da[q] / 16 - 8 * sq;
+                                if (n_b < N) dst[n_b] = db[q] / 16 - 8 * sq;
                             }
                         }
                         continue;

@@ -537,7 +537,8 @@ __device__ __forceinline__ void debug_rows(const uint32_t (&d)[3][16], const flo
 // synchronisation (arrivals on the named barrier, waits for the MMAs' commits), so nothing can wait forever.
 template <int NMMA, bool kZp>
 __global__ void __launch_bounds__(kThreads, 2)
-    msd_kernel(const RunParams p, const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_z) {
+    msd_kernel(const RunParams p, const __grid_constant__ CUtensorMap tmap_s,
+               const __grid_constant__ CUtensorMap tmap_z) {
     using C = Cfg<NMMA>;
     constexpr int kMaxM = C::kMaxM;
     constexpr int R = C::kRowsPerWarp;
@@ -846,7 +847,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                         for (int s0 = 0; s0 < p.splits; s0 += 8) {     // eight loads in flight, summed in order
                             float v[8];
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) v[q] = s0 + q < p.splits ? __ldcg(src + (s0 + q) * slice) : 0.0f;
+                            for (int q = 0; q < 8; ++q)
+                                v[q] = s0 + q < p.splits ? __ldcg(src + (s0 + q) * slice) : 0.0f;
 #pragma unroll
                             for (int q = 0; q < 8; ++q) acc += v[q];
                         }

@@ -466,7 +466,8 @@ wqbmm_status per_channel_prep(const Shape &s, const Plan &plan, Operands *op, vo
                                                                    scale_rep_bytes(s));
     }
     const int reps = static_cast<int>(s.K / s.G);
-    const int copy_blocks = plan.gemv ? 0 : static_cast<int>(std::min<int64_t>(ceil_div(int64_t(reps) * s.N, 256), 1024));
+    const int copy_blocks =
+        plan.gemv ? 0 : static_cast<int>(std::min<int64_t>(ceil_div(int64_t(reps) * s.N, 256), 1024));
     if (s.M + copy_blocks > INT_MAX) return WQBMM_ERR_INVALID;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
