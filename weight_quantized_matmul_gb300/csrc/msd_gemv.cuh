@@ -34,10 +34,13 @@ __global__ void __launch_bounds__(128) gemv_unfold_kernel(const __half *__restri
                                                           float4 *__restrict__ consts, int debug,
                                                           const float *__restrict__ row_amax) {
     pdl_launch_dependents();
-    pdl_wait();                                        // x may be the preceding kernel's output
     const int lane = threadIdx.x & 31;
     const int kb = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int row = blockIdx.y;
+    // the warp's 256 bytes of x (two lines) on their way to L2 while the preceding kernel finishes
+    if (kb < kb_total && (lane & 15) == 0 && kb * kKBlock + lane * 4 < K)
+        prefetch_l2(x + static_cast<size_t>(row) * K + kb * kKBlock + lane * 4);
+    pdl_wait();                                        // x may be the preceding kernel's output
     if (kb >= kb_total) return;                        // whole warps only
     const int lpg = G / 4;
     float v[4];

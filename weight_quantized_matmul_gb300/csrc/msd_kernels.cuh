@@ -440,12 +440,15 @@ __global__ void __launch_bounds__(512) unfold_small_kernel(const __half *__restr
                                                            uint8_t *__restrict__ planes, float *__restrict__ consts,
                                                            const float *__restrict__ row_amax) {
     pdl_launch_dependents();
-    pdl_wait();                  // x may be the preceding kernel's output, which may also still read the planes
     const int lane = threadIdx.x & 31, r = threadIdx.x >> 5;
     const int kb = blockIdx.x, mt = blockIdx.y;
     const int max_m = nmma / 3, lpg = G / 4, Gn = K / G;
     const int m = mt * m_sub + r;
     const bool live = r < m_sub && m < M;
+    // the warp's 256 bytes of x (two lines) on their way to L2 while the preceding kernel finishes
+    if (live && (lane & 15) == 0 && kb * kKBlock + lane * 4 < K)
+        prefetch_l2(x + static_cast<size_t>(m) * K + kb * kKBlock + lane * 4);
+    pdl_wait();                  // x may be the preceding kernel's output, which may also still read the planes
     float v[4];
     load_x4(x, live ? M : 0, K, m, kb * kKBlock + lane * 4, v);     // a dead row slot reads zeros
     float am = group_absmax(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))), lpg);

@@ -230,6 +230,12 @@ __device__ __forceinline__ uint4 ldg_stream16(const void *p, uint64_t policy) {
     return v;
 }
 
+// Brings the line holding `p` into L2 only. Safe before griddepcontrol.wait on data the preceding kernel may still
+// write: L2 is where global memory is kept coherent, and no L1 copy is made that could go stale.
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
