@@ -719,17 +719,22 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (lane == 0) drained = mbar_wait_drain(a_free(c), par);
                 (void)__shfl_sync(0xffffffffu, drained ? 1 : 0, 0);
             }
-            // the TMEM buffers of this k-block's groups: their previous groups have been read by the epilogue
-            const int ng = groups_in(kb0 + i);
-            for (int gg = 0; gg < ng && ok; ++gg) {
-                const int jj = j + gg;
-                ok = mbar_wait_warp(empty_t(jj % kTmemBufs), ((jj / kTmemBufs) & 1) ^ 1, abort_flag, kSiteTmemEmpty);
-            }
-            j += ng;
             if (ok) {
                 convert_tile<kConvThreads>(p_ring + s * L.stage_bytes, a_ring + c * kATileBytes, ct);
                 fence_proxy_async_smem();
             }
+            // the TMEM buffers of this k-block's groups must have been read by the epilogue (their previous groups)
+            // before the MMA warp issues into them; that gates the MMAs, not the expansion, so one converter warp
+            // checks it after its expansion, while the others finish theirs
+            const int ng = groups_in(kb0 + i);
+            if (warp == kConvWarp0) {
+                for (int gg = 0; gg < ng && ok; ++gg) {
+                    const int jj = j + gg;
+                    ok = mbar_wait_warp(empty_t(jj % kTmemBufs), ((jj / kTmemBufs) & 1) ^ 1, abort_flag,
+                                        kSiteTmemEmpty);
+                }
+            }
+            j += ng;
             __syncwarp();
             if (c == 0) named_bar_arrive(kOperandBarrier0, kOperandThreads);
             else named_bar_arrive(kOperandBarrier0 + 1, kOperandThreads);
