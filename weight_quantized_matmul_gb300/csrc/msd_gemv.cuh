@@ -7,10 +7,11 @@
 //   msd_gemv_kernel     steps 9-11 for 16 output columns over all of K per CTA: no split over K, so no reduction
 //                       between CTAs. Each warp takes an eighth of the k-blocks; a lane streams 16-byte pieces of two
 //                       weight rows straight into registers (issued before waiting for the unfold, so the weight
-//                       stream overlaps it), widens the nibbles to bytes u = w + 8 and takes dp4a against the planes:
-//                       dot_i = sum A_i u = Y_i + 8 S_i. Lanes that share a group add their dots, every lane applies
-//                       the combine and the scale, and the partial sums of the lanes and warps are added in a fixed
-//                       order, so the result does not depend on timing.
+//                       stream overlaps it) and takes two dp4a per 32-bit weight word and plane, of its low nibbles
+//                       and of the whole word (u = w + 8 per nibble): dot_i = 16 sum A_i u = 16 (Y_i + 8 S_i).
+//                       Lanes that share a group add their dots, every lane applies the combine and the scale, and
+//                       the partial sums of the lanes and warps are added in a fixed order, so the result does not
+//                       depend on timing.
 // Both kernels run under programmatic launch: the unfold waits for the preceding kernel before reading x, the GEMV
 // kernel fetches weights and scales at once and waits for the unfold before reading the planes.
 #pragma once
@@ -27,8 +28,8 @@ constexpr int kGemvKbPerPass = 8;                   // k-blocks per warp held in
 constexpr int kGemvPlaneBytes = 3 * kKBlock;        // one row, one k-block: [chunk 4][plane 3][32 bytes]
 constexpr float kDotUnitInv = 1.0f / 16.0f;          // the dot products come out as 16 sum_k A_i u
 
-// Steps 1-8 for one row and one 128-k block per warp (lane: 4 k). Planes to [row][kb][chunk][plane][32 B] as int8,
-// constants to [row][group] (float4).
+// Steps 1-8 for one row and one 128-k block per warp (lane: 4 k). Planes to [row][kb][chunk][plane][32 B] as int8
+// (low-nibble positions as 16 A_lo - A_hi, below), constants to [row][group] (float4).
 __global__ void __launch_bounds__(128) gemv_unfold_kernel(const __half *__restrict__ x, int M, int K, int G,
                                                           int kb_total, int8_t *__restrict__ planes,
                                                           float4 *__restrict__ consts, int debug,
@@ -53,14 +54,20 @@ __global__ void __launch_bounds__(128) gemv_unfold_kernel(const __half *__restri
     const int s1 = group_isum(__float2int_rn((a1[0] + a1[1]) + (a1[2] + a1[3])), lpg);
     const int s2 = group_isum(__float2int_rn((a2[0] + a2[1]) + (a2[2] + a2[3])), lpg);
     const int s3 = group_isum(__float2int_rn((a3[0] + a3[1]) + (a3[2] + a3[3])), lpg);
-    // k = 8q .. 8q + 3 meet the low nibbles of a weight word, k = 8q + 4 .. 8q + 7 the high nibbles (16 u as a
-    // byte): the former planes are stored x16 (|16 A| <= 112 fits int8), so every product is 16 A u
-    const int mul = (lane & 1) ? 1 : 16;
-    auto pack4 = [mul](const float (&a)[4]) {
-        return (static_cast<uint32_t>(mul * static_cast<int>(a[0])) & 0xFFu) |
-               ((static_cast<uint32_t>(mul * static_cast<int>(a[1])) & 0xFFu) << 8) |
-               ((static_cast<uint32_t>(mul * static_cast<int>(a[2])) & 0xFFu) << 16) |
-               (static_cast<uint32_t>(mul * static_cast<int>(a[3])) << 24);
+    // k = 8q .. 8q + 3 (even lanes) meet the low nibbles lo of a weight word w, k = 8q + 4 .. 8q + 7 (odd lanes) the
+    // high nibbles hi, byte for byte. The GEMV takes two dp4a per word, of lo = w & 0x0F0F0F0F against D and of w
+    // itself (lo + 16 hi per byte) against H: with D = 16 A_lo - A_hi (|D| <= 119 fits int8) and H = A_hi that is
+    // sum lo (16 A_lo - A_hi) + sum (lo + 16 hi) A_hi = 16 (sum lo A_lo + sum hi A_hi), exact in int32
+    auto pack4 = [lane](const float (&a)[4]) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int mine = static_cast<int>(a[j]);
+            const int hi = __shfl_down_sync(0xffffffffu, mine, 1);      // the same byte of the high positions
+            const int v = (lane & 1) ? mine : 16 * mine - hi;
+            word |= (static_cast<uint32_t>(v) & 0xFFu) << (8 * j);
+        }
+        return word;
     };
     int8_t *dst = planes + (static_cast<size_t>(row) * kb_total + kb) * kGemvPlaneBytes + (lane >> 3) * 96 +
                   (lane & 7) * 4;
@@ -103,17 +110,17 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
     return d;
 }
 
-// 16 sum_k A[k] u[k] over a 16-byte weight piece (32 k) and its 32 plane bytes: the low nibbles meet the x16 plane
-// bytes, the high nibbles (masked in place, worth 16 u) the plain ones.
+// 16 sum_k A[k] u[k] over a 16-byte weight piece (32 k) and its 32 plane bytes: per weight word the low nibbles
+// against D = 16 A_lo - A_hi and the whole word (lo + 16 hi per byte) against A_hi (see gemv_unfold_kernel).
 __device__ __forceinline__ int dot32(const uint4 w, const int4 pa, const int4 pb, int acc) {
     acc = dp4a_us(w.x & 0x0F0F0F0Fu, pa.x, acc);
-    acc = dp4a_us(w.x & 0xF0F0F0F0u, pa.y, acc);
+    acc = dp4a_us(w.x, pa.y, acc);
     acc = dp4a_us(w.y & 0x0F0F0F0Fu, pa.z, acc);
-    acc = dp4a_us(w.y & 0xF0F0F0F0u, pa.w, acc);
+    acc = dp4a_us(w.y, pa.w, acc);
     acc = dp4a_us(w.z & 0x0F0F0F0Fu, pb.x, acc);
-    acc = dp4a_us(w.z & 0xF0F0F0F0u, pb.y, acc);
+    acc = dp4a_us(w.z, pb.y, acc);
     acc = dp4a_us(w.w & 0x0F0F0F0Fu, pb.z, acc);
-    acc = dp4a_us(w.w & 0xF0F0F0F0u, pb.w, acc);
+    acc = dp4a_us(w.w, pb.w, acc);
     return acc;
 }
 
