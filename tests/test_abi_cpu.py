@@ -229,3 +229,20 @@ def test_no_device_is_a_cuda_error(lib):
     assert lib.wqbmm_prepack_weight_w8(A, A, 4096, 4096, 128, None) == wq.ERR_CUDA
     assert lib.wqbmm_run_batched(A, A, A, None, None, A, 4, 2, 4096, 4096, 128, 9216, 8192, A, 1 << 30,
                                  None) == wq.ERR_CUDA
+
+
+def test_empty_batch_returns_an_empty_product(lib):
+    # no rows: nothing to compute, y keeps the batch dimensions; the library still validates K, N and G
+    import torch
+    K, N, G = 512, 264, 128
+    w = torch.empty(0, dtype=torch.uint8)
+    s = torch.empty((K // G, N), dtype=torch.float16)
+    for shape in [(0, K), (3, 0, K)]:
+        y = wq.msd_matmul(torch.empty(shape, dtype=torch.float16), w, s, G)
+        assert tuple(y.shape) == shape[:-1] + (N,) and y.dtype == torch.float16
+    y8 = wq.msd_matmul_w8(torch.empty((0, K), dtype=torch.float16), w, s, G)
+    assert tuple(y8.shape) == (0, N)
+    with pytest.raises(Exception):
+        wq.msd_matmul(torch.empty((0, K), dtype=torch.float16), w, torch.empty((K // 48, N)), 48)   # G not allowed
+    with pytest.raises(Exception):
+        wq.msd_matmul(torch.empty((0, K), dtype=torch.float16), w, torch.empty((K // G, 260)), G)   # N % 8 != 0

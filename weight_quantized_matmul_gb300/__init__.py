@@ -256,6 +256,9 @@ def msd_matmul_w8(x, w_prepacked, antiquant_scale, G: int, y=None, workspace=Non
     N = antiquant_scale.shape[1]
     if y is None:
         y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    if M == 0:
+        wqbmm_workspace_bytes_w8(1, K, N, G)        # the library still checks K, N and G; no rows, nothing to run
+        return y
     if workspace is None:
         workspace = torch.zeros(wqbmm_workspace_bytes_w8(M, K, N, G), dtype=torch.uint8, device=x.device)
     wqbmm_run_w8(x, w_prepacked, antiquant_scale, zero_point, bias, y, M, K, N, G, workspace, None, stream)
@@ -287,6 +290,9 @@ def msd_matmul(x, w_prepacked, antiquant_scale, G: int, y=None, workspace=None, 
         raise ValueError("x must be contiguous")
     if y is None:
         y = torch.empty(lead + (N,), dtype=torch.float16, device=x.device)
+    if M == 0:
+        wqbmm_workspace_bytes(1, K, N, G)           # the library still checks K, N and G; no rows, nothing to run
+        return y
     if workspace is None:
         workspace = allocate_workspace(M, K, N, G, x.device)
     if zero_point is None and bias is None:
