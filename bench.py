@@ -1,17 +1,21 @@
 """Benchmark of the A16W4 per-group MSD matmul on GB300.
 
 One step = one wqbmm_run over one batch of the workload: all steps of the method (A_max, unfold, the three integer
-matmuls, the per-group combine, the accumulation and the fp16 store). Depending on M that is one fused kernel
-(3 <= M < 64) or an unfold kernel followed by the main kernel (M <= 2: dp4a matrix-vector kernel; M >= 64:
-tensor-core tile kernel).
+matmuls, the per-group combine, the accumulation and the fp16 store). Every path is an unfold pre-pass followed by
+the main kernel (M <= 2: dp4a matrix-vector kernel; 3 <= M < 64: small-M tensor-core kernel; M >= 64: tensor-core
+tile kernel).
 
 Default workload: decode GEMV M=1, K=4096, N=4096, G=128 (x ~ N(0,1) fp16, int4 weights uniform on [-8, 7],
-antiquant_scale uniform on [0.005, 0.02], seed 1). Metric: effective weight GB/s (K*N/2 bytes per step / step time).
+antiquant_scale uniform on [0.005, 0.02], seed 1). Metric: effective weight GB/s (K*N/2 bytes per step / step time)
+for M <= 16, int8-equivalent TOPS (6 M N K per step / step time) above.
 
 Timing: W warm-up steps, then a short sustained phase (not timed, keeps the clocks representative and gives the
 clock sampler something to see), then exactly K timed steps between CUDA events on the launching stream, replayed
-from CUDA graphs. Each step uses a different copy of the weights, scales and input (rotating copies whose total is
-more than twice the 126 MB L2), so every step streams its weights from HBM.
+from CUDA graphs; then K launches of the main kernel alone (wqbmm_run_part, part 2), the same way, for the roofline
+of the dominant kernel. Each step uses a different copy of the weights, scales and input (rotating copies whose total
+is more than twice the 126 MB L2), so every step streams its weights from HBM. The other workload shapes are timed
+the same way into a `workloads` record of the same line. The dense tensor-core peaks (E4M3, int8, bf16) are measured
+in the same run; the E4M3 one is the denominator of the tensor-bound fractions.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -59,6 +63,7 @@ def parse():
     ap.add_argument("--sustain-s", type=float, default=1.5)
     ap.add_argument("--cpu-baseline-s", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="time only the selected workload")
     return ap.parse_args()
 
 
@@ -187,10 +192,14 @@ class ClockSampler:
         if self.thread is not None:
             self.thread.join(timeout=5)
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Median SM clock, maximum and throttle reasons seen over the samples taken between t0 and t1 (all when
+        not given)."""
         sm, smax, reasons = [], 0.0, set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for _, ln in self.lines:
+        for t, ln in self.lines:
+            if (t0 is not None and t < t0) or (t1 is not None and t > t1):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -208,57 +217,286 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def cpu_oracle_baseline(wl, budget_s):
-    """The oracle as it stands (binary64 MSD, single thread) on whole problems of the workload, or on seeded rows
-    when one problem alone would exceed the budget. Returns the metric value and a description."""
+def _oracle_blocks(wl, x, wp, sc, rows, threads):
+    """The oracle's work split into `threads` independent calls: blocks of output columns (their weight columns and
+    scales copied out once), all rows (or the seeded rows) each."""
+    n_blocks = max(1, min(threads, wl.N // 8))
+    edges = [wl.N * i // n_blocks // 8 * 8 for i in range(n_blocks)] + [wl.N]
+    blocks = []
+    for a, b in zip(edges[:-1], edges[1:]):
+        if b > a:
+            blocks.append((np.ascontiguousarray(wp[:, a:b]), np.ascontiguousarray(sc[:, a:b])))
+    return blocks
+
+
+def cpu_oracle_baseline(wl, budget_s, threads=1):
+    """The oracle as it stands (binary64 MSD, plain C) on the workload: whole problems, or seeded rows when one
+    problem would be too long for the budget. With threads > 1 the calls run on that many host threads at once,
+    each on its own block of output columns (the oracle releases the interpreter lock while it computes). Returns
+    the metric value, the threads used, a description of the sample and the seconds per problem sample."""
     import oracle
+    from concurrent.futures import ThreadPoolExecutor
     x, wp, sc = I.make_inputs(wl)
-    rows = None
+    rows = I.sample_rows(wl, 8) if wl.M > 16 else None
+    nrows = len(rows) if rows is not None else wl.M
     per_row_units = units_per_step(wl) / wl.M
-    if wl.M > 16:
-        rows = I.sample_rows(wl, 8)
+    blocks = _oracle_blocks(wl, x, wp, sc, rows, threads)
+
+    def one_block(b):
+        oracle.msd_matmul(x, b[0], b[1], wl.G, mode=oracle.MODE_D, rows=rows)
+
+    pool = ThreadPoolExecutor(max_workers=len(blocks)) if len(blocks) > 1 else None
     t0 = time.perf_counter()
     calls = 0
     while True:
-        oracle.msd_matmul(x, wp, sc, wl.G, mode=oracle.MODE_D, rows=rows)
+        if pool is None:
+            one_block(blocks[0])
+        else:
+            list(pool.map(one_block, blocks))
         calls += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = (time.perf_counter() - t0) / calls
-    units = per_row_units * (len(rows) if rows is not None else wl.M)
-    value = units / dt / (1e9 if wl.M <= 16 else 1e12)
-    sample = (f"{calls} calls of the whole {wl.name} problem" if rows is None else
-              f"{calls} calls on {len(rows)} seeded rows of {wl.name}")
-    return value, 1, sample, dt
+    if pool is not None:
+        pool.shutdown()
+    value = per_row_units * nrows / dt / (1e9 if wl.M <= 16 else 1e12)
+    what = f"the whole {wl.name} problem" if rows is None else f"{nrows} seeded rows of {wl.name}"
+    sample = f"{calls} passes over {what}, {len(blocks)} column block(s) on {len(blocks)} thread(s)"
+    return value, len(blocks), sample, dt
 
 
 def run_reference(args, wl):
+    """The reference arm: the oracle, as it stands, on all host cores (column blocks on threads), timed per step."""
     world, rank, _ = dist_env()
     if world > 1 and rank != 0:
         return
     import oracle
+    from concurrent.futures import ThreadPoolExecutor
     metric, unit = metric_for(wl)
     x, wp, sc = I.make_inputs(wl)
     rows = I.sample_rows(wl, 8) if wl.M > 16 else None
     nrows = len(rows) if rows is not None else wl.M
     units = units_per_step(wl) / wl.M * nrows
+    blocks = _oracle_blocks(wl, x, wp, sc, rows, os.cpu_count() or 1)
+    pool = ThreadPoolExecutor(max_workers=len(blocks))
+
+    def step():
+        list(pool.map(lambda b: oracle.msd_matmul(x, b[0], b[1], wl.G, mode=oracle.MODE_D, rows=rows), blocks))
+
     for _ in range(args.warmup):
-        oracle.msd_matmul(x, wp, sc, wl.G, mode=oracle.MODE_D, rows=rows)
+        step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.msd_matmul(x, wp, sc, wl.G, mode=oracle.MODE_D, rows=rows)
+        step()
     dt = (time.perf_counter() - t0) / args.steps
+    pool.shutdown()
     value = units / dt / (1e9 if wl.M <= 16 else 1e12)
-    sample = "whole problem per step" if rows is None else f"{nrows} seeded rows per step"
+    sample = ("whole problem per step" if rows is None else f"{nrows} seeded rows per step") + \
+        f", {len(blocks)} column blocks on {len(blocks)} threads"
     print(json.dumps({
         "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "M": wl.M, "K": wl.K, "N": wl.N, "G": wl.G,
-                   "parallelism": "host cores, single thread"},
-        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle", "sample": sample},
+                   "parallelism": f"host cores, {len(blocks)} threads"},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": len(blocks), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
+
+
+def tensor_peaks(torch, dev, n=8192, reps=10):
+    """Dense tensor-core peaks measured here, best of `reps` n^3 products (CUDA events): E4M3 through
+    torch._scaled_mm (the format this path's MMAs use), int8 through torch._int_mm, bf16 through torch.matmul."""
+    out = {"shape": f"{n}^3, best of {reps}"}
+
+    def best(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        t = float("inf")
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            t = min(t, a.elapsed_time(b))
+        return 2.0 * n ** 3 / (t * 1e-3) / 1e12
+
+    try:
+        a8 = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b8 = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()
+        one = torch.tensor(1.0, device=dev)
+        out["e4m3_tflops"] = best(lambda: torch._scaled_mm(a8, b8, scale_a=one, scale_b=one, out_dtype=torch.bfloat16))
+        del a8, b8
+    except Exception as e:                      # noqa: BLE001 - report, fall back to the bf16 ratio
+        out["e4m3_error"] = repr(e)[:160]
+    try:
+        ai = torch.randint(-8, 8, (n, n), device=dev, dtype=torch.int8)
+        bi = torch.randint(-8, 8, (n, n), device=dev, dtype=torch.int8)
+        out["int8_tops"] = best(lambda: torch._int_mm(ai, bi))
+        del ai, bi
+    except Exception as e:                      # noqa: BLE001
+        out["int8_error"] = repr(e)[:160]
+    ah = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    out["bf16_tflops"] = best(lambda: ah @ ah)
+    del ah
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure(torch, wq, wl, args, dev, sampler, steps, sustain_s, variant, with_e2e):
+    """Times `steps` calls of the workload replayed from CUDA graphs (the whole call, and the main kernel alone),
+    with rotating input copies larger than twice L2, after warm-up and a sustained phase. Returns a record."""
+    zero_point, bias, w8 = variant
+    x, wp, sc = I.make_inputs(wl)
+    if w8:
+        wp = I.make_w8(wl)
+    per_copy = wp.nbytes + x.nbytes + sc.nbytes
+    copies = max(2, min(64, -(-2 * L2_BYTES // per_copy)))
+    xd = torch.from_numpy(x).to(dev)
+    sd = torch.from_numpy(sc).to(dev)
+    wd = torch.from_numpy(wp).to(dev)
+    w_pre0 = wq.prepack_weight_w8(wd, wl.K, wl.N, wl.G) if w8 else wq.prepack_weight(wd, wl.K, wl.N, wl.G)
+    del wd
+    w_pre = [w_pre0] + [w_pre0.clone() for _ in range(copies - 1)]
+    xs = [xd] + [xd.clone() for _ in range(copies - 1)]
+    ss = [sd] + [sd.clone() for _ in range(copies - 1)]
+    ys = [torch.empty((wl.M, wl.N), dtype=torch.float16, device=dev) for _ in range(copies)]
+    if w8:
+        ws = [torch.zeros(wq.wqbmm_workspace_bytes_w8(wl.M, wl.K, wl.N, wl.G), dtype=torch.uint8, device=dev)
+              for _ in range(copies)]
+    else:
+        ws = [wq.allocate_workspace(wl.M, wl.K, wl.N, wl.G, dev) for _ in range(copies)]
+    zs = [None] * copies
+    if zero_point != "none":
+        zd = torch.from_numpy(I.make_zero_point(wl, zero_point)).to(dev)
+        zs = [zd] + [zd.clone() for _ in range(copies - 1)]
+    bd = torch.from_numpy(I.make_bias(wl)).to(dev) if bias else None
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i, s, part=0):
+        c = i % copies
+        if w8:
+            wq.wqbmm_run_w8(xs[c], w_pre[c], ss[c], zs[c], bd, ys[c], wl.M, wl.K, wl.N, wl.G, ws[c], None, s)
+        else:
+            wq.wqbmm_run_part(xs[c], w_pre[c], ss[c], zs[c], bd, ys[c], wl.M, wl.K, wl.N, wl.G, ws[c], None, part,
+                              s)
+
+    # warm-up (eager; also sets kernel attributes before any capture), then one call per copy so that every
+    # workspace holds its copy's unfolded x for the main-kernel-only graph
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i, stream)
+        for c in range(copies):
+            step(c, stream)
+    torch.cuda.synchronize()
+    if wq.wqbmm_read_device_status(stream=stream) != 0:
+        raise SystemExit("device status error during warm-up")
+
+    chunk = min(steps, 4 * copies)
+
+    def graphs_for(part):
+        made = {}
+
+        def graph(n):
+            if n not in made:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(n):
+                        step(i, torch.cuda.current_stream(), part)
+                made[n] = g
+            return made[n]
+        full, rem = divmod(steps, chunk)
+        return graph(chunk), (graph(rem) if rem else None), full
+
+    def timed(gfull, grem, full):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(full):
+                gfull.replay()
+            if grem is not None:
+                grem.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    g_call = graphs_for(0)
+    g_main = None if w8 else graphs_for(2)
+    torch.cuda.synchronize()
+    t_start = time.time()
+    t_end = t_start + sustain_s
+    with torch.cuda.stream(stream):                 # sustained phase: steady clocks, clock samples around the timing
+        while time.time() < t_end:
+            g_call[0].replay()
+            stream.synchronize()
+    world = dist_env()[0]
+    if world > 1:
+        torch.distributed.barrier()
+    ms_total = timed(*g_call)
+    if world > 1:
+        torch.distributed.barrier()
+    main_ms = timed(*g_main) if g_main is not None else None
+    t_stop = time.time()
+    status = wq.wqbmm_read_device_status(stream=stream)
+    if status != 0:
+        raise SystemExit(f"device status error {status:#x}")
+    rec = {"ms_total": ms_total, "ms_step": ms_total / steps, "steps": steps, "copies": copies,
+           "per_copy": per_copy, "chunk": chunk,
+           "kernel_us": None if main_ms is None else main_ms / steps * 1e3,
+           "clocks": sampler.summary(t_start, t_stop), "x_bytes": int(x.nbytes)}
+    if with_e2e:
+        # end to end through the C ABI with host buffers: pinned x in, pinned y out, every step
+        x_host = torch.from_numpy(x).pin_memory()
+        y_host = torch.empty((wl.M, wl.N), dtype=torch.float16).pin_memory()
+        e2e_steps = max(20, min(steps, 500))
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                xs[0].copy_(x_host, non_blocking=True)
+                step(0, stream)
+                y_host.copy_(ys[0], non_blocking=True)
+                stream.synchronize()
+            t0 = time.perf_counter()
+            for i in range(e2e_steps):
+                c = i % copies
+                xs[c].copy_(x_host, non_blocking=True)
+                step(c, stream)
+                y_host.copy_(ys[c], non_blocking=True)
+                stream.synchronize()
+            rec["e2e_s"] = (time.perf_counter() - t0) / e2e_steps
+    del w_pre, xs, ss, ys, ws, zs
+    torch.cuda.empty_cache()
+    return rec
+
+
+def roofline_for(wl, rec, peaks, peak_kind, alg_bytes, variant_name):
+    """Roofline of the dominant (main) kernel: algorithmic bytes (M <= 16) or int8-equivalent ops per call over the
+    main kernel's own time per launch (timed alone, CUDA events over a graph of main-kernel launches); the same
+    figure over the whole call (pre-passes included) as call_frac."""
+    call_s = rec["ms_step"] * 1e-3
+    kern_s = rec["kernel_us"] * 1e-6 if rec["kernel_us"] else None
+    if wl.M <= 16:
+        peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+        work, unit, bound, div = alg_bytes, "GB/s", "hbm", 1e9
+        source = f"{peak_kind} hbm_gbs"
+    else:
+        e4m3 = peaks.get("e4m3_tflops")
+        if e4m3:
+            peak, source = e4m3, "e4m3 dense, torch._scaled_mm measured in this run"
+        else:
+            peak = 2 * float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+            source = f"{peak_kind} bf16_tflops x 2 (nominal e4m3 : bf16 ratio)"
+        work, unit, bound, div = wl.int8_equiv_ops(), "TFLOP/s", "tensor", 1e12
+    achieved = work / (kern_s if kern_s else call_s) / div
+    call_achieved = work / call_s / div
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "traffic": None if variant_name else dram_traffic(wl.name),
+            "kernel_us": rec["kernel_us"], "call_us": rec["ms_step"] * 1e3,
+            "call_achieved": call_achieved, "call_frac": call_achieved / peak,
+            "peak_source": source,
+            ("algorithmic_bytes_per_launch" if bound == "hbm" else "algorithmic_flops_per_launch"): work}
 
 
 def main():
@@ -286,149 +524,40 @@ def main():
     wqbuild.build()
     metric, unit = metric_for(wl)
 
-    # ---- inputs: host copy once, then rotating device copies whose total exceeds 2x L2
-    x, wp, sc = I.make_inputs(wl)
-    if args.w8:
-        wp = I.make_w8(wl)
-    per_copy = wp.nbytes + x.nbytes + sc.nbytes
-    copies = max(2, min(64, -(-2 * L2_BYTES // per_copy)))
-    xd = torch.from_numpy(x).to(dev)
-    sd = torch.from_numpy(sc).to(dev)
-    wd = torch.from_numpy(wp).to(dev)
-    if args.w8:
-        w_pre0 = wq.prepack_weight_w8(wd, wl.K, wl.N, wl.G)
-    else:
-        w_pre0 = wq.prepack_weight(wd, wl.K, wl.N, wl.G)
-    del wd
-    w_pre = [w_pre0] + [w_pre0.clone() for _ in range(copies - 1)]
-    xs = [xd] + [xd.clone() for _ in range(copies - 1)]
-    ss = [sd] + [sd.clone() for _ in range(copies - 1)]
-    ys = [torch.empty((wl.M, wl.N), dtype=torch.float16, device=dev) for _ in range(copies)]
-    if args.w8:
-        ws = [torch.zeros(wq.wqbmm_workspace_bytes_w8(wl.M, wl.K, wl.N, wl.G), dtype=torch.uint8, device=dev)
-              for _ in range(copies)]
-    else:
-        ws = [wq.allocate_workspace(wl.M, wl.K, wl.N, wl.G, dev) for _ in range(copies)]
-    zs = [None] * copies
-    if args.zero_point != "none":
-        zd = torch.from_numpy(I.make_zero_point(wl, args.zero_point)).to(dev)
-        zs = [zd] + [zd.clone() for _ in range(copies - 1)]
-    bd = torch.from_numpy(I.make_bias(wl)).to(dev) if args.bias else None
-    optionals = args.zero_point != "none" or args.bias
-    variant = optionals or args.per_channel or args.w8           # not the captured kernels' workload
-    stream = torch.cuda.Stream(device=dev)
-
-    def step(i, s):
-        c = i % copies
-        if args.w8:
-            wq.wqbmm_run_w8(xs[c], w_pre[c], ss[c], zs[c], bd, ys[c], wl.M, wl.K, wl.N, wl.G, ws[c], None, s)
-        elif optionals:
-            wq.wqbmm_run_ex(xs[c], w_pre[c], ss[c], zs[c], bd, ys[c], wl.M, wl.K, wl.N, wl.G, ws[c], None, s)
-        else:
-            wq.wqbmm_run(xs[c], w_pre[c], ss[c], ys[c], wl.M, wl.K, wl.N, wl.G, ws[c], None, s)
-
-    # ---- warm-up (eager, also sets kernel attributes before any capture)
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            step(i, stream)
-    torch.cuda.synchronize()
-    if wq.wqbmm_read_device_status(stream=stream) != 0:
-        raise SystemExit("device status error during warm-up")
-
-    # ---- graphs: a chunk of steps, replayed; the remainder in a second graph
-    chunk = min(args.steps, 4 * copies)
-    graphs = {}
-
-    def graph_for(n):
-        if n not in graphs:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(n):
-                    step(i, torch.cuda.current_stream())
-            graphs[n] = g
-        return graphs[n]
-
-    full, rem = divmod(args.steps, chunk)
-    g_full = graph_for(chunk)
-    g_rem = graph_for(rem) if rem else None
-    torch.cuda.synchronize()
-
     sampler = ClockSampler(nvsmi_id(torch, dev, local))
     sampler.start()
-    # sustained phase: steady clocks and at least a second of clock samples around the timed region
-    t_end = time.time() + args.sustain_s
-    with torch.cuda.stream(stream):
-        while time.time() < t_end:
-            g_full.replay()
-            stream.synchronize()
+    variant = (args.zero_point, bool(args.bias), bool(args.w8))
+    variant_name = ",".join(n for n, on in (("zero_point", args.zero_point != "none"), ("bias", args.bias),
+                                             ("per_channel", args.per_channel), ("w8", args.w8)) if on)
+    rec = measure(torch, wq, wl, args, dev, sampler, args.steps, args.sustain_s, variant, True)
+    ms_step = slowest_rank_ms(rec["ms_total"], world, dev) / args.steps
 
-    start_ev, stop_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        start_ev.record(stream)
-        for _ in range(full):
-            g_full.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        stop_ev.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    others = {}
+    if not variant_name and not args.no_workloads:
+        # every other workload shape of the metric, shorter sustained phase, same steps (at least 10)
+        for name, other in I.WORKLOADS.items():
+            if name == wl.name:
+                continue
+            r = measure(torch, wq, other, args, dev, sampler, max(10, args.steps), 0.5, variant, False)
+            others[name] = r
+    peaks_here = tensor_peaks(torch, dev) if rank == 0 else {}
     time.sleep(0.25)
     sampler.stop()
-    ms_total = slowest_rank_ms(start_ev.elapsed_time(stop_ev), world, dev)
-    ms_step = ms_total / args.steps
-    status = wq.wqbmm_read_device_status(stream=stream)
-    if status != 0:
-        raise SystemExit(f"device status error {status:#x}")
-
-    # ---- end to end through the C ABI with host buffers: pinned x in, pinned y out, every step
-    x_host = torch.from_numpy(x).pin_memory()
-    y_host = torch.empty((wl.M, wl.N), dtype=torch.float16).pin_memory()
-    e2e_steps = max(20, min(args.steps, 500))
-    with torch.cuda.stream(stream):
-        for i in range(3):
-            xs[0].copy_(x_host, non_blocking=True)
-            step(0, stream)
-            y_host.copy_(ys[0], non_blocking=True)
-            stream.synchronize()
-        t0 = time.perf_counter()
-        for i in range(e2e_steps):
-            c = i % copies
-            xs[c].copy_(x_host, non_blocking=True)
-            step(c, stream)
-            y_host.copy_(ys[c], non_blocking=True)
-            stream.synchronize()
-        e2e_s = (time.perf_counter() - t0) / e2e_steps
-
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return
 
-    # every path runs an unfold pre-pass and then the main kernel
-    launches_per_step = 2
     peaks, peak_kind = measured_peaks()
+    peaks = dict(peaks)
+    if "e4m3_tflops" in peaks_here:
+        peaks["e4m3_tflops"] = peaks_here["e4m3_tflops"]
     # the optional inputs add their own bytes: zero points 2 (K/G) N, bias 2 N
     alg_bytes = (wl.algorithmic_bytes() + (2 * wl.groups * wl.N if args.zero_point != "none" else 0) +
                  (2 * wl.N if args.bias else 0) + (wl.K * wl.N // 2 if args.w8 else 0))
-    if wl.M <= 16:
-        hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-        achieved = alg_bytes / (ms_step * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                    "frac": achieved / hbm_peak, "traffic": None if variant else dram_traffic(wl.name),
-                    "peak_source": f"{peak_kind} hbm_gbs",
-                    "algorithmic_bytes_per_launch": alg_bytes}
-    else:
-        # E4M3 dense tensor peak = the measured bf16 peak x 2 (the nominal fp8 : bf16 ratio 4.5 : 2.25)
-        bf16 = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
-        achieved = wl.int8_equiv_ops() / (ms_step * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "achieved": achieved, "peak": 2 * bf16, "unit": "TFLOP/s",
-                    "frac": achieved / (2 * bf16), "traffic": None if variant else dram_traffic(wl.name),
-                    "peak_source": f"{peak_kind} bf16_tflops x 2 (e4m3)",
-                    "algorithmic_flops_per_launch": wl.int8_equiv_ops()}
+    rec["ms_step"] = ms_step
+    roofline = roofline_for(wl, rec, peaks, peak_kind, alg_bytes, variant_name)
+    launches_per_step = 2 + (1 if args.per_channel or args.w8 else 0)
     line = {
         "metric": metric,
         "value": metric_value(wl, ms_step * 1e-3, world, args.w8),
@@ -448,19 +577,34 @@ def main():
                    "zero_point": args.zero_point, "bias": bool(args.bias), "per_channel": bool(args.per_channel),
                    "weights": "int8" if args.w8 else "int4",
                    "parallelism": f"replicas{world}" if world > 1 else "single GPU",
-                   "l2": f"{copies} rotating input copies ({copies * per_copy / 2**20:.0f} MiB > 2x L2)",
-                   "launch": f"CUDA graphs of {chunk} steps"},
+                   "l2": f"{rec['copies']} rotating input copies ({rec['copies'] * rec['per_copy'] / 2**20:.0f} MiB "
+                         f"> 2x L2)",
+                   "launch": f"CUDA graphs of {rec['chunk']} steps"},
         "gpu_launches": args.steps * launches_per_step,
-        "clocks": sampler.summary(),
-        "e2e": {"value": metric_value(wl, e2e_s, 1, args.w8), "unit": unit, "h2d_bytes_per_step": int(x.nbytes),
-                "d2h_bytes_per_step": int(wl.M * wl.N * 2),
+        "clocks": rec["clocks"],
+        "e2e": {"value": metric_value(wl, rec["e2e_s"], 1, args.w8), "unit": unit,
+                "h2d_bytes_per_step": rec["x_bytes"], "d2h_bytes_per_step": int(wl.M * wl.N * 2),
                 "note": "eager wqbmm_run per step; pinned x in, pinned y out, stream synchronized each step"},
         "roofline": roofline,
+        "tensor_peaks": peaks_here,
     }
+    if others:
+        recs = {}
+        for name, r in others.items():
+            owl = I.WORKLOADS[name]
+            om, ou = metric_for(owl)
+            rf = roofline_for(owl, r, peaks, peak_kind, owl.algorithmic_bytes(), "")
+            recs[name] = {"metric": om, "value": metric_value(owl, r["ms_step"] * 1e-3), "unit": ou,
+                          "ms": r["ms_step"], "kernel_us": r["kernel_us"], "steps": r["steps"],
+                          "frac": rf["frac"], "call_frac": rf["call_frac"], "bound": rf["bound"],
+                          "peak": rf["peak"], "traffic": rf["traffic"], "clocks": r["clocks"]}
+        line["workloads"] = recs
     if not args.no_cpu_baseline:
-        v, cores, sample, dt = cpu_oracle_baseline(wl, args.cpu_baseline_s)
-        line["cpu_baseline"] = {"value": v, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample,
-                                "s_per_call": dt}
+        v1, c1, sample1, dt1 = cpu_oracle_baseline(wl, args.cpu_baseline_s / 2, threads=1)
+        vn, cn, samplen, dtn = cpu_oracle_baseline(wl, args.cpu_baseline_s / 2, threads=os.cpu_count() or 1)
+        line["cpu_baseline"] = {"value": vn, "unit": unit, "cores": cn, "kind": "oracle", "sample": samplen,
+                                "s_per_call": dtn, "single_thread": {"value": v1, "cores": c1, "sample": sample1,
+                                                                     "s_per_call": dt1}}
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

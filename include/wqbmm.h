@@ -25,7 +25,8 @@
  *
  * Conventions for every entry point:
  *   - All pointers are caller-owned. Pointers marked "device" must be device memory of the current CUDA device;
- *     the library allocates nothing and keeps no state beyond cached device attributes and the device status word.
+ *     the library allocates nothing and keeps no state beyond cached device attributes and one device status word
+ *     per device (see wqbmm_read_device_status).
  *   - Work is enqueued asynchronously on `stream` (0 = the legacy default stream); the library never synchronizes,
  *     except wqbmm_read_device_status, which waits for `stream`.
  *   - Arguments are validated before anything is enqueued. On any error nothing is launched and outputs are
@@ -106,9 +107,10 @@ WQBMM_API wqbmm_status wqbmm_prepack_weight_nk(const uint8_t *w_packed_nk, void 
  * the planes (3 bytes per element of x, rows padded to a multiple of 128) and the constants. Per channel it also
  * holds each row's A_max and, for M >= 3, the scale and zero-point rows repeated once per 128 k (or 64 or 32 when K
  * is not a multiple of 128).
- * It must be zero-filled once before its first use; every successful run leaves the counters at zero again, so the
- * same workspace can be reused by later runs on the same stream without clearing. Runs that execute concurrently must
- * use different workspaces.
+ * It needs no initialisation: every run writes what it later reads (the unfold pre-pass also clears the split-K
+ * arrival counters before the main kernel uses them), so a workspace can be reused by later runs on the same stream
+ * in whatever state an earlier run left it, including a run that ended with WQBMM_ERR_DEVICE_TIMEOUT. Runs that
+ * execute concurrently must use different workspaces.
  * Errors: NULLPTR if bytes is null; INVALID if the shape rules fail.
  */
 WQBMM_API wqbmm_status wqbmm_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t G, size_t *bytes);
@@ -148,6 +150,19 @@ WQBMM_API wqbmm_status wqbmm_run_ex(const void *x, const void *w_prepacked, cons
                                     const void *zero_point, const void *bias, void *y, int64_t M, int64_t K,
                                     int64_t N, int64_t G, void *workspace, size_t workspace_bytes,
                                     wqbmm_stream_t stream);
+
+/*
+ * Measurement aid: one part of wqbmm_run_ex on its own, so that the main kernel can be timed without the pre-passes
+ * that precede it. part 0 launches everything (the same as wqbmm_run_ex); part 1 only the pre-passes (the unfold of
+ * x into the workspace, and for per-channel shapes the row maxima and repeated scale rows); part 2 only the main
+ * kernel, which reads what part 1 (or an earlier run of the same shape and inputs on this workspace) left in the
+ * workspace. A part-2 launch on a workspace that holds no such result gives an undefined y (but stays within the
+ * buffers). Arguments, launch and errors as for wqbmm_run_ex; also INVALID for a part outside 0..2.
+ */
+WQBMM_API wqbmm_status wqbmm_run_part(const void *x, const void *w_prepacked, const void *antiquant_scale,
+                                      const void *zero_point, const void *bias, void *y, int64_t M, int64_t K,
+                                      int64_t N, int64_t G, void *workspace, size_t workspace_bytes, int part,
+                                      wqbmm_stream_t stream);
 
 /*
  * Int8 weights (W8; the weight dtype INT8 of the page "aclnnCalculateMatmulWeightSizeV2 接口详解"): the same eleven
@@ -217,6 +232,10 @@ WQBMM_API wqbmm_status wqbmm_debug_group_partials(const void *x, const void *w_p
  * Reads (and, if clear != 0, resets) the current device's status word after waiting for `stream`.
  * *code is 0 when no kernel of this library has recorded an error; otherwise it is WQBMM_ERR_DEVICE_TIMEOUT in the
  * low 8 bits and the site of the wait that gave up in bits 8-15.
+ * There is one status word per device for the whole library (the first error recorded wins), not one per workspace
+ * or stream: an error recorded by a run on another stream, or by another caller in the same process, is reported
+ * here too, and clearing it clears it for every caller. Callers that share a device should agree on who reads and
+ * clears it.
  * Errors: NULLPTR, CUDA.
  */
 WQBMM_API wqbmm_status wqbmm_read_device_status(int32_t *code, int clear, wqbmm_stream_t stream);
@@ -234,14 +253,20 @@ WQBMM_API wqbmm_status wqbmm_debug_wait_timeout(int64_t limit_ns, wqbmm_stream_t
  * buffers) and that therefore has no way to provide wqbmm_run's workspace. (The paper has no counterpart: this is
  * an interface convenience, not part of the method.)
  *   x, w_prepacked, antiquant_scale, y   as for wqbmm_run (caller-owned device memory)
- * Scratch: the split-K partial sums and arrival counters live in one statically sized device array of 2 MiB
- * (2097152 bytes) inside this library; every GPU that loads the library holds it until the process exits. A shape
- * whose workspace (as reported by wqbmm_workspace_bytes) exceeds that size is rejected with
- * WQBMM_ERR_SCRATCH_LIMIT before anything is launched.
- * Set-up: the first call on each device looks up the array's device address (with that device current) and keeps
- * it; make that first call before any stream capture. Nothing is allocated by any call: no cudaMalloc, no
- * cudaFree, no allocating library routine. Each call clears the counters it uses (one cudaMemsetAsync on
- * `stream`) and then launches the same kernel as wqbmm_run.
+ * Scratch: everything wqbmm_run keeps in its workspace (the unfolded planes of x and the per-row combine constants,
+ * the split-K partial sums and arrival counters, the per-channel rows) lives in one statically sized device array of
+ * 2 MiB (2097152 bytes) inside this library; every GPU that loads the library holds it until the process exits. A
+ * shape whose workspace (as reported by wqbmm_workspace_bytes) exceeds that size is rejected with
+ * WQBMM_ERR_SCRATCH_LIMIT before anything is launched. The planes take about 3 bytes per element of x (rows padded
+ * to 16 below 64 rows and to 128 from 64 rows on); shapes of 3 to 63 rows with few column tiles also need split-K
+ * partial sums, 4 bytes per output element and K-slice. wqbmm_workspace_bytes gives the exact figure. Shapes that
+ * fit include M = 1 or 2 with K up to 65536 at any N, M = 8 with K = 4096 and N = 11008, and M = 128 with K = 5120
+ * and N = 13824; prefill-sized products (thousands of rows) do not fit and must use wqbmm_run.
+ * Set-up: the first call in each CUDA context of a device looks up the array's device address (with that device
+ * current) and keeps it with the context, so a device reset, which makes a new context, leads to a new look-up; make
+ * the first call on a device before any stream capture. Nothing is allocated by any call: no cudaMalloc, no cudaFree,
+ * no allocating library routine. Each call launches the same kernels as wqbmm_run, which write everything they later
+ * read, so the array's contents from earlier calls (of any shape) do not matter.
  * All calls share the one array: calls whose executions overlap on the GPU (different streams, or one device
  * used from several host threads without ordering) race on it and give wrong results. Order them on one stream.
  * Errors: NULLPTR, INVALID, UNSUPPORTED_ARCH, CUDA, SCRATCH_LIMIT.

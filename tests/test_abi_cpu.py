@@ -198,6 +198,10 @@ CASES = [
     ("static_scratch_misaligned_x", lambda L: L.wqbmm_run_static_scratch(MIS, A, A, A, 1, 128, 128, 128, None),
      INVALID),
     ("static_scratch_bad_group", lambda L: L.wqbmm_run_static_scratch(A, A, A, A, 1, 128, 128, 96, None), INVALID),
+    ("run_part_bad_part",
+     lambda L: L.wqbmm_run_part(A, A, A, None, None, A, 1, 128, 128, 128, A, 1 << 20, 3, None), INVALID),
+    ("run_part_null_y",
+     lambda L: L.wqbmm_run_part(A, A, A, None, None, None, 1, 128, 128, 128, A, 1 << 20, 2, None), NULLPTR),
     ("status_null", lambda L: L.wqbmm_read_device_status(None, 0, None), NULLPTR),
     ("timeout_limit_too_small", lambda L: L.wqbmm_debug_wait_timeout(10, None), INVALID),
     ("timeout_limit_too_large", lambda L: L.wqbmm_debug_wait_timeout(10 ** 10, None), INVALID),

@@ -5,12 +5,15 @@ Bars (method: WeightQuantBatchMatmulExperiment page, section 4.1):
   - steps 1-8 (A_max and the three planes, wqbmm_debug_unfold): bit-exact against the oracle's binary32 unfold;
   - step 9 (per-group integer Y1..Y3 from the tensor-core path, wqbmm_debug_group_partials): bit-exact;
   - steps 1-11 (wqbmm_run, fp16 y): |y - y_ref| <= 2e-3 * max|y_ref| + 1 fp16 ulp(y_ref) against the oracle in
-    binary64 (and in binary32 unfold), element by element; at full workload sizes on seeded sampled rows.
+    binary64 (and in binary32 unfold), element by element; at full workload sizes on seeded sampled rows; and the
+    tight bar of tests/tolerance.py (the binary32-unfold oracle rounded to fp16, within 0.6 ulp, on every output
+    that is not small), which sees an error in any one combine constant.
 """
 import numpy as np
 import pytest
 
 import oracle
+import tolerance as T
 import weight_quantized_matmul_gb300 as wq
 from weight_quantized_matmul_gb300 import build as wqbuild
 from weight_quantized_matmul_gb300 import inputs as I
@@ -18,21 +21,6 @@ from weight_quantized_matmul_gb300 import inputs as I
 pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
-
-
-def fp16_ulp(v):
-    a = np.abs(np.asarray(v, dtype=np.float64))
-    e = np.floor(np.log2(np.maximum(a, 2.0 ** -14)))
-    return 2.0 ** (e - 10)
-
-
-def assert_within_tolerance(got, ref, what=""):
-    got = np.asarray(got, dtype=np.float64)
-    tol = 2e-3 * np.abs(ref).max() + fp16_ulp(ref)
-    err = np.abs(got - ref)
-    bad = err > tol
-    assert not bad.any(), (f"{what}: {int(bad.sum())}/{bad.size} outside tolerance, max err {err.max():.4g}, "
-                           f"max |ref| {np.abs(ref).max():.4g}, first bad {np.argwhere(bad)[:3].tolist()}")
 
 
 @pytest.fixture(scope="module")
@@ -101,6 +89,68 @@ def test_prepack_of_transposed_weights_matches(dev, K, N, G):
     a = wq.prepack_weight(to_dev(wp, dev), K, N, G).cpu().numpy()
     b = wq.prepack_weight_nk(to_dev(nk, dev), K, N, G).cpu().numpy()
     np.testing.assert_array_equal(a, b)
+
+
+NK_CASES = [
+    # M, K, N, G: every kernel path, ragged N, K past 8192
+    (1, 4096, 520, 128),            # decode kernel
+    (2, 8320, 264, 64),             # decode kernel, K > 8192, ragged last CTA
+    (3, 512, 1000, 32),             # small-M tensor-core kernel
+    (16, 1024, 392, 64),            # small-M, cluster-reduced split-K
+    (3, 16384, 136, 128),           # small-M, split-K through the workspace
+    (64, 640, 264, 128),            # large-M
+    (200, 1280, 136, 32),
+]
+
+
+@pytest.mark.parametrize("M,K,N,G", NK_CASES)
+def test_transposed_weights_match_oracle(dev, M, K, N, G):
+    """Weights given as [N, K/2] (the operator's transpose option for the weight, page 2 section 5.4), prepacked by
+    wqbmm_prepack_weight_nk, then wqbmm_run and wqbmm_run_ex (fractional zero points and a bias): against the oracle,
+    which reads the same weights in their [K/2, N] packing."""
+    wl = I.small_case(M, K, N, G, seed=13 * M + K + N, x_dist="t3_clip60" if M % 2 else "normal")
+    x, wp, sc = I.make_inputs(wl)
+    zp, bias = I.make_zero_point(wl, "frac"), I.make_bias(wl)
+    w_pre = wq.prepack_weight_nk(to_dev(pack_int4_nk(wp, K, N), dev), K, N, G)
+    xd, sd = to_dev(x, dev), to_dev(sc, dev)
+    ws = wq.allocate_workspace(M, K, N, G, dev)
+    y = torch.empty((M, N), dtype=torch.float16, device=dev)
+    wq.wqbmm_run(xd, w_pre, sd, y, M, K, N, G, ws)
+    T.assert_matches(y.cpu().numpy(), oracle.msd_matmul(x, wp, sc, G, mode=oracle.MODE_D),
+                     oracle.msd_matmul(x, wp, sc, G, mode=oracle.MODE_F), "transposed weights")
+    y_ex = torch.empty((M, N), dtype=torch.float16, device=dev)
+    wq.wqbmm_run_ex(xd, w_pre, sd, to_dev(zp, dev), to_dev(bias, dev), y_ex, M, K, N, G, ws)
+    T.assert_matches(y_ex.cpu().numpy(),
+                     oracle.msd_matmul_ex(x, wp, sc, G, zero_point=zp, bias=bias, mode=oracle.MODE_D),
+                     oracle.msd_matmul_ex(x, wp, sc, G, zero_point=zp, bias=bias, mode=oracle.MODE_F),
+                     "transposed weights, zero points and bias")
+
+
+def test_binding_rejects_mismatched_tensors(dev):
+    """The binding checks what the C ABI cannot see behind its raw pointers (shapes, dtypes, contiguity, devices,
+    sizes) before anything is launched; the output is left untouched."""
+    M, K, N, G = 4, 512, 264, 128
+    x, wp, sc = I.make_inputs(I.small_case(M, K, N, G, seed=6))
+    xd, sd = to_dev(x, dev), to_dev(sc, dev)
+    w_pre = wq.prepack_weight(to_dev(wp, dev), K, N, G)
+    y = torch.full((M, N), 5.0, dtype=torch.float16, device=dev)
+    bad = [
+        dict(y=torch.empty((M, N - 8), dtype=torch.float16, device=dev)),          # y too narrow
+        dict(y=torch.empty((M, N), dtype=torch.float32, device=dev)),              # y of another dtype
+        dict(antiquant_scale=sd[:2]),                                              # too few scale rows
+        dict(antiquant_scale=torch.empty((N, K // G), dtype=torch.float16, device=dev).t()),   # not contiguous
+        dict(x=xd.float()),                                                        # x of another dtype
+        dict(w_prepacked=w_pre[:-16]),                                             # prepacked weights too short
+        dict(zero_point=torch.zeros((K // G, N - 8), dtype=torch.float16, device=dev)),
+        dict(bias=torch.zeros(N, dtype=torch.float16)),                            # bias on the host
+    ]
+    for kw in bad:
+        args = dict(x=xd, w_prepacked=w_pre, antiquant_scale=sd, y=y)
+        args.update(kw)
+        with pytest.raises((ValueError, TypeError)):
+            wq.msd_matmul(args.pop("x"), args.pop("w_prepacked"), args.pop("antiquant_scale"), G, **args)
+    torch.cuda.synchronize()
+    assert (y == 5.0).all()
 
 
 # ------------------------------------------------------------------------------------------- steps 1-8
@@ -262,8 +312,8 @@ def test_run_matches_oracle(dev, M, K, N, G, xd, wd, lo, hi):
     x, wp, sc = I.make_inputs(I.small_case(M, K, N, G, seed=M + K + N, x_dist=xd, w_dist=wd, scale_lo=lo,
                                            scale_hi=hi))
     y = gpu_run(x, wp, sc, G, dev)
-    assert_within_tolerance(y, oracle.msd_matmul(x, wp, sc, G, mode=oracle.MODE_D), "binary64 oracle")
-    assert_within_tolerance(y, oracle.msd_matmul(x, wp, sc, G, mode=oracle.MODE_F), "binary32-unfold oracle")
+    T.assert_matches(y, oracle.msd_matmul(x, wp, sc, G, mode=oracle.MODE_D),
+                     oracle.msd_matmul(x, wp, sc, G, mode=oracle.MODE_F), "run")
 
 
 def test_run_zero_and_constant_rows(dev):
@@ -275,7 +325,8 @@ def test_run_zero_and_constant_rows(dev):
     x[3, :128] = np.float16(-60.0)
     y = gpu_run(x, wp, sc, G, dev)
     assert not y[0].any()
-    assert_within_tolerance(y, oracle.msd_matmul(x, wp, sc, G), "special rows")
+    T.assert_matches(y, oracle.msd_matmul(x, wp, sc, G), oracle.msd_matmul(x, wp, sc, G, mode=oracle.MODE_F),
+                     "special rows")
 
 
 @pytest.mark.parametrize("wl", [I.WORKLOADS["decode_m1_k4096_n4096"],                  # cluster-reduced split-K
@@ -292,11 +343,48 @@ def test_run_deterministic_and_workspace_left_clean(dev, wl):
         wq.wqbmm_run(xd, w_pre, sd, y, wl.M, wl.K, wl.N, wl.G, ws)
         outs.append(y.cpu().numpy().view(np.uint16))
     assert all(np.array_equal(outs[0], o) for o in outs[1:])
-    assert_within_tolerance(outs[0].view(np.float16), oracle.msd_matmul(x, wp, sc, wl.G), wl.name)
+    T.assert_matches(outs[0].view(np.float16), oracle.msd_matmul(x, wp, sc, wl.G),
+                     oracle.msd_matmul(x, wp, sc, wl.G, mode=oracle.MODE_F), wl.name)
     if ws is not None and 2 < wl.M < 64:
         # the arrival counters sit after the partial sums; all must be back at zero
         counters = ws.cpu().numpy()[-256:].view(np.uint32)
         assert not counters.any()
+
+
+@pytest.mark.parametrize("wl", [I.small_case(1, 4096, 520, 128, seed=31),                   # decode
+                                I.small_case(3, 16384, 520, 64, seed=32),                   # split-K, workspace
+                                I.small_case(4, 4096, 1024, 128, seed=33),                  # split-K, cluster
+                                I.small_case(130, 512, 256, 64, seed=34)])                  # large M
+def test_run_needs_no_cleared_workspace(dev, wl):
+    """A workspace full of leftover bytes (as an earlier run that gave up a wait could leave it) gives the same
+    result: every kernel writes what it later reads, the split-K arrival counters included."""
+    x, wp, sc = I.make_inputs(wl)
+    w_pre = wq.prepack_weight(to_dev(wp, dev), wl.K, wl.N, wl.G)
+    nbytes = wq.wqbmm_workspace_bytes(wl.M, wl.K, wl.N, wl.G)
+    ws = torch.full((nbytes,), 0xA5, dtype=torch.uint8, device=dev)
+    y = torch.empty((wl.M, wl.N), dtype=torch.float16, device=dev)
+    wq.wqbmm_run(to_dev(x, dev), w_pre, to_dev(sc, dev), y, wl.M, wl.K, wl.N, wl.G, ws)
+    T.assert_matches(y.cpu().numpy(), oracle.msd_matmul(x, wp, sc, wl.G),
+                     oracle.msd_matmul(x, wp, sc, wl.G, mode=oracle.MODE_F), "leftover workspace")
+
+
+@pytest.mark.parametrize("M,K,N,G", [(1, 4096, 520, 128), (2, 1024, 264, 32), (5, 2048, 1000, 64),
+                                     (3, 16384, 136, 128), (130, 512, 392, 64), (8, 1024, 264, 1024),
+                                     (200, 256, 136, 256)])
+def test_run_parts_compose_to_run(dev, M, K, N, G):
+    """wqbmm_run_part: the pre-passes (part 1) and then the main kernel alone (part 2) give wqbmm_run's y bit for
+    bit, on every path (per channel included); the main kernel alone again on the same workspace gives it too."""
+    x, wp, sc = I.make_inputs(I.small_case(M, K, N, G, seed=M + 2 * K + N))
+    xd, sd = to_dev(x, dev), to_dev(sc, dev)
+    w_pre = wq.prepack_weight(to_dev(wp, dev), K, N, G)
+    a = torch.empty((M, N), dtype=torch.float16, device=dev)
+    wq.wqbmm_run(xd, w_pre, sd, a, M, K, N, G, wq.allocate_workspace(M, K, N, G, dev))
+    ws = wq.allocate_workspace(M, K, N, G, dev)
+    for parts in ((1, 2), (2,)):
+        b = torch.full((M, N), 9.0, dtype=torch.float16, device=dev)
+        for part in parts:
+            wq.wqbmm_run_part(xd, w_pre, sd, None, None, b, M, K, N, G, ws, None, part)
+        np.testing.assert_array_equal(a.cpu().numpy().view(np.uint16), b.cpu().numpy().view(np.uint16))
 
 
 def test_run_errors_leave_output_untouched(dev):
@@ -324,7 +412,7 @@ def test_bounded_wait_reports_timeout(dev):
     assert wq.wqbmm_read_device_status() == 0
     # the context is still usable
     x, wp, sc = I.make_inputs(I.small_case(2, 256, 128, 128, seed=1))
-    assert_within_tolerance(gpu_run(x, wp, sc, 128, dev), oracle.msd_matmul(x, wp, sc, 128), "after timeout")
+    T.assert_within_tolerance(gpu_run(x, wp, sc, 128, dev), oracle.msd_matmul(x, wp, sc, 128), "after timeout")
 
 
 # ------------------------------------------------------------------------------------------- full workloads
@@ -335,7 +423,8 @@ def test_workload_full_output(dev, name):
     wl = I.WORKLOADS[name]
     x, wp, sc = I.make_inputs(wl)
     y = gpu_run(x, wp, sc, wl.G, dev)
-    assert_within_tolerance(y, oracle.msd_matmul(x, wp, sc, wl.G, mode=oracle.MODE_D), name)
+    T.assert_matches(y, oracle.msd_matmul(x, wp, sc, wl.G, mode=oracle.MODE_D),
+                     oracle.msd_matmul(x, wp, sc, wl.G, mode=oracle.MODE_F), name)
 
 
 @pytest.mark.parametrize("name,nrows", [("mid_m128_k5120_n13824", 16), ("prefill_m2048_k8192_n28672", 64)])
@@ -344,8 +433,8 @@ def test_workload_sampled_rows(dev, name, nrows):
     x, wp, sc = I.make_inputs(wl)
     y = gpu_run(x, wp, sc, wl.G, dev)
     rows = I.sample_rows(wl, nrows)
-    ref = oracle.msd_matmul(x, wp, sc, wl.G, mode=oracle.MODE_D, rows=rows)
-    assert_within_tolerance(y[rows], ref, name)
+    T.assert_matches(y[rows], oracle.msd_matmul(x, wp, sc, wl.G, mode=oracle.MODE_D, rows=rows),
+                     oracle.msd_matmul(x, wp, sc, wl.G, mode=oracle.MODE_F, rows=rows), name)
     # one group's integer partials on the same rows, bit-exact (the tensor-core step at full size)
     g = wl.groups // 2
     y123 = torch.empty((3, wl.M, wl.N), dtype=torch.int32, device=dev)
@@ -394,9 +483,8 @@ def test_run_ex_matches_oracle(dev, M, K, N, G, zkind, with_bias):
     zp = None if zkind is None else I.make_zero_point(wl, zkind)
     bias = I.make_bias(wl) if with_bias else None
     y = gpu_run_ex(x, wp, sc, zp, bias, G, dev)
-    for mode, what in ((oracle.MODE_D, "binary64 oracle"), (oracle.MODE_F, "binary32-unfold oracle")):
-        ref = oracle.msd_matmul_ex(x, wp, sc, G, zero_point=zp, bias=bias, mode=mode)
-        assert_within_tolerance(y, ref, what)
+    T.assert_matches(y, oracle.msd_matmul_ex(x, wp, sc, G, zero_point=zp, bias=bias, mode=oracle.MODE_D),
+                     oracle.msd_matmul_ex(x, wp, sc, G, zero_point=zp, bias=bias, mode=oracle.MODE_F), "run_ex")
 
 
 @pytest.mark.parametrize("M,K,N,G", [(1, 1024, 264, 64), (9, 1024, 264, 64), (130, 512, 256, 64)])
@@ -453,8 +541,10 @@ def test_run_ex_mid_workload_sampled_rows(dev):
     zp, bias = I.make_zero_point(wl, "frac"), I.make_bias(wl)
     y = gpu_run_ex(x, wp, sc, zp, bias, wl.G, dev)
     rows = I.sample_rows(wl, 8)
-    ref = oracle.msd_matmul_ex(x, wp, sc, wl.G, zero_point=zp, bias=bias, mode=oracle.MODE_D, rows=rows)
-    assert_within_tolerance(y[rows], ref, wl.name)
+    T.assert_matches(y[rows], oracle.msd_matmul_ex(x, wp, sc, wl.G, zero_point=zp, bias=bias, mode=oracle.MODE_D,
+                                                   rows=rows),
+                     oracle.msd_matmul_ex(x, wp, sc, wl.G, zero_point=zp, bias=bias, mode=oracle.MODE_F, rows=rows),
+                     wl.name)
 
 
 # ------------------------------------------------------------------------------------------- per channel (G = K)
@@ -483,9 +573,8 @@ def test_per_channel_matches_oracle(dev, M, K, N, zkind, with_bias):
     zp = None if zkind is None else I.make_zero_point(wl, zkind)
     bias = I.make_bias(wl) if with_bias else None
     y = gpu_run_ex(x, wp, sc, zp, bias, K, dev)
-    for mode, what in ((oracle.MODE_D, "binary64 oracle"), (oracle.MODE_F, "binary32-unfold oracle")):
-        ref = oracle.msd_matmul_ex(x, wp, sc, K, zero_point=zp, bias=bias, mode=mode)
-        assert_within_tolerance(y, ref, what)
+    T.assert_matches(y, oracle.msd_matmul_ex(x, wp, sc, K, zero_point=zp, bias=bias, mode=oracle.MODE_D),
+                     oracle.msd_matmul_ex(x, wp, sc, K, zero_point=zp, bias=bias, mode=oracle.MODE_F), "per channel")
 
 
 @pytest.mark.parametrize("M,K", [(9, 1024), (3, 352), (2, 4096)])
@@ -509,8 +598,8 @@ def test_batched_x_matches_oracle(dev, B, M, K, N, G):
     w_pre = wq.prepack_weight(to_dev(wp, dev), K, N, G)
     y = wq.msd_matmul(to_dev(x.reshape(B, M, K), dev), w_pre, to_dev(sc, dev), G)
     assert tuple(y.shape) == (B, M, N)
-    ref = oracle.msd_matmul(x, wp, sc, G, mode=oracle.MODE_D).reshape(B, M, N)
-    assert_within_tolerance(y.cpu().numpy(), ref, "batched")
+    T.assert_matches(y.cpu().numpy(), oracle.msd_matmul(x, wp, sc, G, mode=oracle.MODE_D).reshape(B, M, N),
+                     oracle.msd_matmul(x, wp, sc, G, mode=oracle.MODE_F).reshape(B, M, N), "batched")
 
 
 @pytest.mark.parametrize("B,M,K,N,G", [(3, 5, 1024, 264, 64), (2, 70, 256, 128, 128)])
@@ -531,8 +620,10 @@ def test_batched_strided_matches_oracle(dev, B, M, K, N, G):
     got = y.cpu().numpy()
     assert (got[:, M] == 3.0).all()
     for b in range(B):
-        ref = oracle.msd_matmul_ex(x[b * M:(b + 1) * M], wp, sc, G, zero_point=zp, bias=bias, mode=oracle.MODE_D)
-        assert_within_tolerance(got[b, :M], ref, f"item {b}")
+        xb = x[b * M:(b + 1) * M]
+        T.assert_matches(got[b, :M], oracle.msd_matmul_ex(xb, wp, sc, G, zero_point=zp, bias=bias, mode=oracle.MODE_D),
+                         oracle.msd_matmul_ex(xb, wp, sc, G, zero_point=zp, bias=bias, mode=oracle.MODE_F),
+                         f"item {b}")
     # contiguous: one product of B * M rows
     xc = to_dev(x, dev)
     yc = torch.empty((B * M, N), dtype=torch.float16, device=dev)
@@ -587,6 +678,5 @@ def test_w8_matches_oracle(dev, M, K, N, G, zkind, with_bias):
     y = wq.msd_matmul_w8(to_dev(x, dev), w_pre, to_dev(sc, dev), G,
                          zero_point=None if zp is None else to_dev(zp, dev),
                          bias=None if bias is None else to_dev(bias, dev)).cpu().numpy()
-    for mode, what in ((oracle.MODE_D, "binary64 oracle"), (oracle.MODE_F, "binary32-unfold oracle")):
-        ref = oracle.msd_matmul_w8(x, w8, sc, G, zero_point=zp, bias=bias, mode=mode)
-        assert_within_tolerance(y, ref, what)
+    T.assert_matches(y, oracle.msd_matmul_w8(x, w8, sc, G, zero_point=zp, bias=bias, mode=oracle.MODE_D),
+                     oracle.msd_matmul_w8(x, w8, sc, G, zero_point=zp, bias=bias, mode=oracle.MODE_F), "int8 weights")

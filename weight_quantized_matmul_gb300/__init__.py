@@ -18,6 +18,7 @@ __all__ = [
     "allocate_workspace", "msd_matmul", "SYMBOLS", "wqbmm_run_static_scratch", "wqbmm_prepack_weight_nk",
     "prepack_weight_nk", "wqbmm_run_ex", "wqbmm_run_batched", "wqbmm_prepacked_weight_bytes_w8",
     "wqbmm_prepack_weight_w8", "wqbmm_workspace_bytes_w8", "wqbmm_run_w8", "prepack_weight_w8", "msd_matmul_w8",
+    "wqbmm_run_part",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -33,7 +34,7 @@ SYMBOLS = (
     "wqbmm_debug_unfold", "wqbmm_debug_group_partials", "wqbmm_read_device_status", "wqbmm_debug_wait_timeout",
     "wqbmm_status_string", "wqbmm_run_static_scratch", "wqbmm_prepack_weight_nk", "wqbmm_run_ex",
     "wqbmm_run_batched", "wqbmm_prepacked_weight_bytes_w8", "wqbmm_prepack_weight_w8", "wqbmm_workspace_bytes_w8",
-    "wqbmm_run_w8",
+    "wqbmm_run_w8", "wqbmm_run_part",
 )
 
 
@@ -64,6 +65,7 @@ def load_library():
                 "wqbmm_workspace_bytes": [i64, i64, i64, i64, ctypes.POINTER(sz)],
                 "wqbmm_run": [p, p, p, p, i64, i64, i64, i64, p, sz, p],
                 "wqbmm_run_ex": [p, p, p, p, p, p, i64, i64, i64, i64, p, sz, p],
+                "wqbmm_run_part": [p, p, p, p, p, p, i64, i64, i64, i64, p, sz, ctypes.c_int, p],
                 "wqbmm_run_batched": [p, p, p, p, p, p, i64, i64, i64, i64, i64, i64, i64, p, sz, p],
                 "wqbmm_prepacked_weight_bytes_w8": [i64, i64, i64, ctypes.POINTER(sz)],
                 "wqbmm_prepack_weight_w8": [p, p, i64, i64, i64, p],
@@ -149,6 +151,15 @@ def wqbmm_run_ex(x, w_prepacked, antiquant_scale, zero_point, bias, y, M: int, K
     _check(load_library().wqbmm_run_ex(_ptr(x), _ptr(w_prepacked), _ptr(antiquant_scale), _ptr(zero_point),
                                         _ptr(bias), _ptr(y), M, K, N, G, _ptr(workspace), workspace_bytes,
                                         _stream(stream)), "wqbmm_run_ex")
+
+
+def wqbmm_run_part(x, w_prepacked, antiquant_scale, zero_point, bias, y, M: int, K: int, N: int, G: int,
+                   workspace=None, workspace_bytes: int | None = None, part: int = 0, stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().wqbmm_run_part(_ptr(x), _ptr(w_prepacked), _ptr(antiquant_scale), _ptr(zero_point),
+                                          _ptr(bias), _ptr(y), M, K, N, G, _ptr(workspace), workspace_bytes, int(part),
+                                          _stream(stream)), "wqbmm_run_part")
 
 
 def wqbmm_run_batched(x, w_prepacked, antiquant_scale, zero_point, bias, y, batch: int, M: int, K: int, N: int,
@@ -259,10 +270,43 @@ def msd_matmul_w8(x, w_prepacked, antiquant_scale, G: int, y=None, workspace=Non
     if M == 0:
         wqbmm_workspace_bytes_w8(1, K, N, G)        # the library still checks K, N and G; no rows, nothing to run
         return y
+    _check_operands(x, w_prepacked, antiquant_scale, zero_point, bias, y, (M, N), K, N, G, M,
+                    wqbmm_prepacked_weight_bytes_w8(K, N, G))
     if workspace is None:
         workspace = torch.zeros(wqbmm_workspace_bytes_w8(M, K, N, G), dtype=torch.uint8, device=x.device)
     wqbmm_run_w8(x, w_prepacked, antiquant_scale, zero_point, bias, y, M, K, N, G, workspace, None, stream)
     return y
+
+
+def _check_operands(x, w_prepacked, scale, zero_point, bias, y, y_shape, K: int, N: int, G: int, M: int,
+                    w_bytes: int) -> None:
+    """Shapes, dtypes, contiguity and devices of the tensors handed to the C ABI, which sees only raw pointers: a
+    buffer that is too small or on another device would be read or written out of bounds by the kernels."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device())
+    groups = K // G if G != K else 1
+    named = [("x", x, torch.float16, None), ("y", y, torch.float16, tuple(y_shape)),
+             ("antiquant_scale", scale, torch.float16, (groups, N)), ("w_prepacked", w_prepacked, None, None)]
+    if zero_point is not None:
+        named.append(("zero_point", zero_point, torch.float16, (groups, N)))
+    if bias is not None:
+        named.append(("bias", bias, torch.float16, (N,)))
+    for name, t, dtype, shape in named:
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch tensor")
+        if t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, the current CUDA device is {dev}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if dtype is not None and t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+        if shape is not None and tuple(t.shape) != shape:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shape}")
+    if tuple(x.shape)[-1] != K:
+        raise ValueError(f"x has {tuple(x.shape)[-1]} columns, expected K = {K}")
+    if w_prepacked.numel() * w_prepacked.element_size() < w_bytes:
+        raise ValueError(f"w_prepacked holds {w_prepacked.numel() * w_prepacked.element_size()} bytes, the "
+                         f"prepacked layout of K = {K}, N = {N} needs {w_bytes}")
 
 
 def allocate_workspace(M: int, K: int, N: int, G: int, device):
@@ -286,13 +330,13 @@ def msd_matmul(x, w_prepacked, antiquant_scale, G: int, y=None, workspace=None, 
     for d in lead:
         M *= d
     N = antiquant_scale.shape[1]
-    if not x.is_contiguous():
-        raise ValueError("x must be contiguous")
     if y is None:
         y = torch.empty(lead + (N,), dtype=torch.float16, device=x.device)
     if M == 0:
         wqbmm_workspace_bytes(1, K, N, G)           # the library still checks K, N and G; no rows, nothing to run
         return y
+    _check_operands(x, w_prepacked, antiquant_scale, zero_point, bias, y, lead + (N,), K, N, G, M,
+                    wqbmm_prepacked_weight_bytes(K, N, G))
     if workspace is None:
         workspace = allocate_workspace(M, K, N, G, x.device)
     if zero_point is None and bias is None:

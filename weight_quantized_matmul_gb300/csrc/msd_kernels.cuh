@@ -435,10 +435,13 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns) {
 // swizzle, K-major); row slots past the tile's rows or past M, and the padding rows 3 max_m .. nmma - 1, hold zeros.
 // Per (row, group) the constant record holds 512 c_i A_max (i = 1..3, the MMA unit folded in), the offset-binary
 // correction 8 sum_i c_i A_max S_i, then the plane sums S_i (read by debug runs) and a zero: [row][8] per group.
+// counters (null when the main kernel reduces without them): the split-K arrival counters of the main kernel that
+// follows, cleared here by block (0, 0), so that a run needs no cleared workspace even after an earlier run gave up.
 __global__ void __launch_bounds__(512) unfold_small_kernel(const __half *__restrict__ x, int M, int K, int G,
                                                            int kb_total, int m_sub, int nmma,
                                                            uint8_t *__restrict__ planes, float *__restrict__ consts,
-                                                           const float *__restrict__ row_amax) {
+                                                           const float *__restrict__ row_amax,
+                                                           uint32_t *__restrict__ counters, int n_counters) {
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31, r = threadIdx.x >> 5;
     const int kb = blockIdx.x, mt = blockIdx.y;
@@ -449,6 +452,9 @@ __global__ void __launch_bounds__(512) unfold_small_kernel(const __half *__restr
     if (live && (lane & 15) == 0 && kb * kKBlock + lane * 4 < K)
         prefetch_l2(x + static_cast<size_t>(m) * K + kb * kKBlock + lane * 4);
     pdl_wait();                  // x may be the preceding kernel's output, which may also still read the planes
+    // the preceding run's main kernel has ended; this run's reads its counters only after this kernel has ended
+    if (counters != nullptr && kb == 0 && mt == 0)
+        for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0u;
     float v[4];
     load_x4(x, live ? M : 0, K, m, kb * kKBlock + lane * 4, v);     // a dead row slot reads zeros
     float am = group_absmax(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))), lpg);

@@ -21,6 +21,9 @@ constexpr int kMaxDevices = 64;
 constexpr int kPlanSms = 160;       // workspace sizing assumes at most this many SMs, so it needs no device
 constexpr int kCtasPerSm = 2;       // shared memory (at most 110 KB) and TMEM allow two run CTAs per SM
 
+// Which kernels of a product to launch (wqbmm_run_part): all of them, only the pre-passes, or only the main kernel.
+constexpr int kPartAll = 0, kPartPre = 1, kPartMain = 2;
+
 struct DeviceInfo {
     bool probed = false;
     bool supported = false;
@@ -287,7 +290,7 @@ wqbmm_status launch_small_zp(const RunParams &rp, const Plan &plan, DeviceInfo *
 // Small-M path: the unfold pre-pass writes the planes images and constants into the workspace, then the tensor-core
 // kernel runs under programmatic launch.
 wqbmm_status launch_small(const void *x, const float *row_amax, const RunParams &rp, const Plan &plan,
-                          DeviceInfo *info, cudaStream_t stream) {
+                          DeviceInfo *info, cudaStream_t stream, int part) {
     if (plan.m_tiles > 65535 || plan.splits > 65535) return WQBMM_ERR_INVALID;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -298,10 +301,13 @@ wqbmm_status launch_small(const void *x, const float *row_amax, const RunParams 
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, unfold_small_kernel, static_cast<const __half *>(x), rp.M, rp.K, rp.G, plan.kb_total,
+    const int n_counters = rp.ws_count != nullptr ? plan.m_tiles * plan.n_tiles : 0;
+    if (part != kPartMain &&
+        cudaLaunchKernelEx(&cfg, unfold_small_kernel, static_cast<const __half *>(x), rp.M, rp.K, rp.G, plan.kb_total,
                            plan.m_sub, plan.nmma, const_cast<uint8_t *>(rp.planes), const_cast<float *>(rp.consts),
-                           row_amax) != cudaSuccess)
+                           row_amax, rp.ws_count, n_counters) != cudaSuccess)
         return WQBMM_ERR_CUDA;
+    if (part == kPartPre) return WQBMM_OK;
     // debug runs read no zero points (they expose the integer partials of the plain weights)
     return rp.zp != nullptr && rp.dbg_group < 0 ? launch_small_zp<true>(rp, plan, info, stream)
                                                 : launch_small_zp<false>(rp, plan, info, stream);
@@ -310,7 +316,7 @@ wqbmm_status launch_small(const void *x, const float *row_amax, const RunParams 
 // Large-M path: the unfold pre-pass writes plane tiles and constants into the workspace, then the GEMM kernel runs
 // under programmatic launch (it fetches weights and scales while the pre-pass finishes).
 wqbmm_status launch_large(const Shape &s, const Plan &plan, const Operands &op, void *workspace, int dbg_group,
-                          int32_t *dbg_y123, DeviceInfo *info, cudaStream_t stream) {
+                          int32_t *dbg_y123, DeviceInfo *info, cudaStream_t stream, int part) {
     if (plan.n_tiles > 65535) return WQBMM_ERR_INVALID;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
@@ -339,10 +345,13 @@ wqbmm_status launch_large(const Shape &s, const Plan &plan, const Operands &op, 
     uint8_t *planes = static_cast<uint8_t *>(workspace);
     float4 *consts = reinterpret_cast<float4 *>(planes + align256(planes_bytes(plan)));
     const dim3 ugrid(static_cast<unsigned>(plan.m_tiles * kGemmTileM / 8), static_cast<unsigned>(plan.kb_total));
-    unfold_planes_kernel<<<ugrid, 256, 0, stream>>>(static_cast<const __half *>(op.x), static_cast<int>(s.M),
-                                                    static_cast<int>(s.K), static_cast<int>(s.G), plan.kb_total,
-                                                    planes, consts, dbg_group >= 0 ? 1 : 0, op.row_amax);
-    if (cudaPeekAtLastError() != cudaSuccess) return WQBMM_ERR_CUDA;
+    if (part != kPartMain) {
+        unfold_planes_kernel<<<ugrid, 256, 0, stream>>>(static_cast<const __half *>(op.x), static_cast<int>(s.M),
+                                                        static_cast<int>(s.K), static_cast<int>(s.G), plan.kb_total,
+                                                        planes, consts, dbg_group >= 0 ? 1 : 0, op.row_amax);
+        if (cudaPeekAtLastError() != cudaSuccess) return WQBMM_ERR_CUDA;
+    }
+    if (part == kPartPre) return WQBMM_OK;
     CUtensorMap tmap_s{}, tmap_z{};
     if (!dbg && !fp16_tensor_map(&tmap_s, op.scale, s.K / s.G, s.N, static_cast<int>(kKBlock / s.G), kGemmTileN))
         return WQBMM_ERR_CUDA;
@@ -389,7 +398,7 @@ bool gemv_smem_attr() {
 }
 
 wqbmm_status launch_gemv(const Shape &s, const Plan &plan, const Operands &op, void *workspace, int dbg_group,
-                         int32_t *dbg_y123, DeviceInfo *info, cudaStream_t stream) {
+                         int32_t *dbg_y123, DeviceInfo *info, cudaStream_t stream, int part) {
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         if (!info->gemv_smem_set) {
@@ -412,10 +421,12 @@ wqbmm_status launch_gemv(const Shape &s, const Plan &plan, const Operands &op, v
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, gemv_unfold_kernel, static_cast<const __half *>(op.x), static_cast<int>(s.M),
+    if (part != kPartMain &&
+        cudaLaunchKernelEx(&cfg, gemv_unfold_kernel, static_cast<const __half *>(op.x), static_cast<int>(s.M),
                            static_cast<int>(s.K), static_cast<int>(s.G), plan.kb_total, planes, consts,
                            dbg_group >= 0 ? 1 : 0, op.row_amax) != cudaSuccess)
         return WQBMM_ERR_CUDA;
+    if (part == kPartPre) return WQBMM_OK;
     GemvParams gp{};
     gp.w = static_cast<const uint8_t *>(op.w);
     gp.scale = static_cast<const __half *>(op.scale);
@@ -453,10 +464,11 @@ wqbmm_status launch_gemv(const Shape &s, const Plan &plan, const Operands &op, v
 }
 
 // Launches one product (or, with dbg_group >= 0, the integer partials of one group) planned by `plan` on the current
-// device. `workspace` holds workspace_for(shape, plan) bytes; `clear_counters` clears the split-K counters first.
+// device. `workspace` holds workspace_for(shape, plan) bytes, in any state: every kernel writes what it later reads.
 // Per channel: each row's A_max and (for the paths that load scale tiles) the repeated scale and zero-point rows,
 // into the workspace after the path's own part, by one kernel under programmatic launch.
-wqbmm_status per_channel_prep(const Shape &s, const Plan &plan, Operands *op, void *workspace, cudaStream_t stream) {
+wqbmm_status per_channel_prep(const Shape &s, const Plan &plan, Operands *op, void *workspace, cudaStream_t stream,
+                              bool launch) {
     uint8_t *base = static_cast<uint8_t *>(workspace) + path_workspace(s, plan);
     float *row_amax = reinterpret_cast<float *>(base);
     __half *scale_rep = nullptr, *zp_rep = nullptr;
@@ -478,7 +490,8 @@ wqbmm_status per_channel_prep(const Shape &s, const Plan &plan, Operands *op, vo
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, per_channel_prep_kernel, static_cast<const __half *>(op->x), static_cast<int>(s.M),
+    if (launch &&
+        cudaLaunchKernelEx(&cfg, per_channel_prep_kernel, static_cast<const __half *>(op->x), static_cast<int>(s.M),
                            static_cast<int>(s.K), row_amax, static_cast<const __half *>(op->scale),
                            static_cast<const __half *>(op->zp), static_cast<int>(s.N), reps, scale_rep,
                            zp_rep) != cudaSuccess)
@@ -492,16 +505,16 @@ wqbmm_status per_channel_prep(const Shape &s, const Plan &plan, Operands *op, vo
     return WQBMM_OK;
 }
 
-wqbmm_status dispatch(const Operands &op_in, const Shape &s, const Plan &plan, void *workspace, bool clear_counters,
-                      int dbg_group, int32_t *dbg_y123, DeviceInfo *info, cudaStream_t stream) {
+wqbmm_status dispatch(const Operands &op_in, const Shape &s, const Plan &plan, void *workspace, int dbg_group,
+                      int32_t *dbg_y123, DeviceInfo *info, cudaStream_t stream, int part = kPartAll) {
     Operands op = op_in;
     op.group_stride = static_cast<int>(s.N);
     if (s.pc) {
-        const wqbmm_status st = per_channel_prep(s, plan, &op, workspace, stream);
+        const wqbmm_status st = per_channel_prep(s, plan, &op, workspace, stream, part != kPartMain);
         if (st != WQBMM_OK) return st;
     }
-    if (plan.gemv) return launch_gemv(s, plan, op, workspace, dbg_group, dbg_y123, info, stream);
-    if (plan.large) return launch_large(s, plan, op, workspace, dbg_group, dbg_y123, info, stream);
+    if (plan.gemv) return launch_gemv(s, plan, op, workspace, dbg_group, dbg_y123, info, stream, part);
+    if (plan.large) return launch_large(s, plan, op, workspace, dbg_group, dbg_y123, info, stream, part);
     RunParams rp{};
     rp.planes = static_cast<const uint8_t *>(workspace);
     rp.consts = reinterpret_cast<const float *>(static_cast<uint8_t *>(workspace) + align256(small_planes_bytes(plan)));
@@ -516,11 +529,7 @@ wqbmm_status dispatch(const Operands &op_in, const Shape &s, const Plan &plan, v
                         align256(small_consts_bytes(s, plan));
         const size_t counters_at = align256(static_cast<size_t>(plan.splits) * s.M * s.N * sizeof(float));
         rp.ws_part = reinterpret_cast<float *>(part);
-        rp.ws_count = reinterpret_cast<uint32_t *>(part + counters_at);
-        if (clear_counters &&
-            cudaMemsetAsync(rp.ws_count, 0, static_cast<size_t>(plan.m_tiles) * plan.n_tiles * sizeof(uint32_t),
-                            stream) != cudaSuccess)
-            return WQBMM_ERR_CUDA;
+        rp.ws_count = reinterpret_cast<uint32_t *>(part + counters_at);     // cleared by the unfold pre-pass
     }
     rp.M = static_cast<int>(s.M);
     rp.K = static_cast<int>(s.K);
@@ -533,25 +542,56 @@ wqbmm_status dispatch(const Operands &op_in, const Shape &s, const Plan &plan, v
     rp.kb_total = plan.kb_total;
     rp.reduce = plan.reduce;
     rp.dbg_group = dbg_group;
-    return launch_small(op.x, op.row_amax, rp, plan, info, stream);
+    return launch_small(op.x, op.row_amax, rp, plan, info, stream, part);
 }
 
 // Scratch for wqbmm_run_static_scratch: a fixed device array instead of a caller workspace. Host code must not
-// pass the symbol itself to a kernel (on the host it only names a stand-in); the device address of this array on
-// each device is looked up once with cudaGetSymbolAddress and kept in g_scratch_addr.
+// pass the symbol itself to a kernel (on the host it only names a stand-in); the device address of this array is
+// looked up with cudaGetSymbolAddress, with the device current, on the first call in each CUDA context of a device,
+// and kept with that context: after a device reset the runtime makes a new context (and loads the module again), so
+// the next call sees another context and looks the address up again.
 constexpr size_t kStaticScratchBytes = size_t(2) << 20;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
-void *g_scratch_addr[kMaxDevices] = {};
 
-// Device address of g_static_scratch on `dev` (the current device), found on the first call for that device.
-wqbmm_status static_scratch_address(int dev, void **addr) {
+struct ScratchAddress {
+    CUcontext ctx = nullptr;
+    void *addr = nullptr;
+};
+ScratchAddress g_scratch_addr[kMaxDevices];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+    static CtxGetCurrentFn fn = nullptr;
+    static bool probed = false;
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_scratch_addr[dev]) {
+    if (!probed) {
+        probed = true;
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(f);
+    }
+    return fn;
+}
+
+// Device address of g_static_scratch on `dev` (the current device) in the current context.
+wqbmm_status static_scratch_address(int dev, void **addr) {
+    const CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+    if (!get_ctx) return WQBMM_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    if (get_ctx(&ctx) != CUDA_SUCCESS) return WQBMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    ScratchAddress &c = g_scratch_addr[dev];
+    if (ctx == nullptr || ctx != c.ctx || c.addr == nullptr) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return WQBMM_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+        if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return WQBMM_ERR_CUDA;   // the lookup made it current
+        c.ctx = ctx;
+        c.addr = p;
     }
-    *addr = g_scratch_addr[dev];
+    *addr = c.addr;
     return WQBMM_OK;
 }
 
@@ -707,7 +747,7 @@ wqbmm_status wqbmm_run_w8(const void *x, const void *w_prepacked, const void *an
                            zp2) != cudaSuccess)
         return WQBMM_ERR_CUDA;
     const Operands op{x2, w_prepacked, scale2, zp2, bias, y};
-    return dispatch(op, s2, plan, workspace, false, -1, nullptr, info, cs);
+    return dispatch(op, s2, plan, workspace, -1, nullptr, info, cs);
 }
 
 wqbmm_status wqbmm_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t G, size_t *bytes) {
@@ -729,7 +769,15 @@ wqbmm_status wqbmm_run(const void *x, const void *w_prepacked, const void *antiq
 wqbmm_status wqbmm_run_ex(const void *x, const void *w_prepacked, const void *antiquant_scale,
                           const void *zero_point, const void *bias, void *y, int64_t M, int64_t K, int64_t N,
                           int64_t G, void *workspace, size_t workspace_bytes, wqbmm_stream_t stream) {
+    return wqbmm_run_part(x, w_prepacked, antiquant_scale, zero_point, bias, y, M, K, N, G, workspace,
+                          workspace_bytes, kPartAll, stream);
+}
+
+wqbmm_status wqbmm_run_part(const void *x, const void *w_prepacked, const void *antiquant_scale,
+                            const void *zero_point, const void *bias, void *y, int64_t M, int64_t K, int64_t N,
+                            int64_t G, void *workspace, size_t workspace_bytes, int part, wqbmm_stream_t stream) {
     if (!x || !w_prepacked || !antiquant_scale || !y) return WQBMM_ERR_NULLPTR;
+    if (part != kPartAll && part != kPartPre && part != kPartMain) return WQBMM_ERR_INVALID;
     wqbmm_status st = check_shape(Shape{M, K, N, G});
     if (st != WQBMM_OK) return st;
     const Shape s = kernel_shape(M, K, N, G);
@@ -745,7 +793,7 @@ wqbmm_status wqbmm_run_ex(const void *x, const void *w_prepacked, const void *an
     const Plan plan = make_plan(s, info->sms < kPlanSms ? info->sms : kPlanSms);
     if (workspace_bytes < workspace_for(s, plan)) return WQBMM_ERR_INVALID;
     const Operands op{x, w_prepacked, antiquant_scale, zero_point, bias, y};
-    return dispatch(op, s, plan, workspace, false, -1, nullptr, info, reinterpret_cast<cudaStream_t>(stream));
+    return dispatch(op, s, plan, workspace, -1, nullptr, info, reinterpret_cast<cudaStream_t>(stream), part);
 }
 
 wqbmm_status wqbmm_run_batched(const void *x, const void *w_prepacked, const void *antiquant_scale,
@@ -792,9 +840,10 @@ wqbmm_status wqbmm_run_static_scratch(const void *x, const void *w_prepacked, co
     if (need > kStaticScratchBytes) return WQBMM_ERR_SCRATCH_LIMIT;
     void *base = nullptr;
     if (need > 0 && (st = static_scratch_address(dev, &base)) != WQBMM_OK) return st;
-    // the array keeps whatever the previous call (of any shape) left there: split-K counters are cleared first
+    // the array keeps whatever the previous call (of any shape) left there; as with a caller's workspace, every
+    // kernel writes what it later reads (the unfold pre-pass also clears the split-K counters)
     const Operands op{x, w_prepacked, antiquant_scale, nullptr, nullptr, y};
-    return dispatch(op, s, plan, base, true, -1, nullptr, info, reinterpret_cast<cudaStream_t>(stream));
+    return dispatch(op, s, plan, base, -1, nullptr, info, reinterpret_cast<cudaStream_t>(stream));
 }
 
 wqbmm_status wqbmm_debug_unfold(const void *x, int64_t M, int64_t K, int64_t G, int8_t *planes, float *amax,
@@ -849,8 +898,7 @@ wqbmm_status wqbmm_debug_group_partials(const void *x, const void *w_prepacked, 
     }
     if (workspace_bytes < workspace_for(s, plan)) return WQBMM_ERR_INVALID;
     const Operands op{x, w_prepacked, nullptr, nullptr, nullptr, nullptr};
-    return dispatch(op, s, plan, workspace, false, static_cast<int>(g), y123, info,
-                    reinterpret_cast<cudaStream_t>(stream));
+    return dispatch(op, s, plan, workspace, static_cast<int>(g), y123, info, reinterpret_cast<cudaStream_t>(stream));
 }
 
 wqbmm_status wqbmm_read_device_status(int32_t *code, int clear, wqbmm_stream_t stream) {
