@@ -413,7 +413,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint8_t *stage = p_ring + s * L.stage_bytes;
             const int ng = groups_in(kb);
             for (int gg = 0; gg < ng; ++gg, u += 3) {
-                const float4 cr = ok ? reinterpret_cast<const float4 *>(stage + L.off_const)[gg * kGemmTileM + r]
+                const float4 cr = ok ? lds_f128(smem_addr(stage + L.off_const) + 16 * (gg * kGemmTileM + r))
                                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                 if (kDebug) {
                     // warp-uniform: tcgen05.ld is executed by the whole warp; rows past M only skip the stores
@@ -444,10 +444,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     continue;
                 }
-                const float4 *srow =
-                    reinterpret_cast<const float4 *>(stage + L.off_scale32) + (gg * kGemmTileN + half * 64) / 4;
-                const float4 *zrow =
-                    reinterpret_cast<const float4 *>(stage + L.off_zp32) + (gg * kGemmTileN + half * 64) / 4;
+                // scales (and 1 + zp / 8) of the warp's 64 columns, as 32-bit shared-window addresses
+                const uint32_t srow = smem_addr(stage + L.off_scale32) + 4 * (gg * kGemmTileN + half * 64);
+                const uint32_t zrow = smem_addr(stage + L.off_zp32) + 4 * (gg * kGemmTileN + half * 64);
                 float2 T[32];
                 // plane 1: T = c1 D1 - corr (times 1 + zp / 8 per column with zero points)
                 {
@@ -468,7 +467,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                             for (int q4 = 0; q4 < 4; ++q4) {
                                 float4 zf = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
-                                if constexpr (kZp) zf = zrow[ch * 4 + q4];
+                                if constexpr (kZp) zf = lds_f128(zrow + 16 * (ch * 4 + q4));
 #pragma unroll
                                 for (int h = 0; h < 2; ++h) {
                                     const int q = q4 * 2 + h;
@@ -530,7 +529,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             const uint32_t(&d)[16] = dd[sub];
 #pragma unroll
                             for (int q4 = 0; q4 < 4; ++q4) {
-                                const float4 sc = srow[ch * 4 + q4];           // same address in every lane: broadcast
+                                const float4 sc = lds_f128(srow + 16 * (ch * 4 + q4));   // one address: broadcast
 #pragma unroll
                                 for (int h = 0; h < 2; ++h) {
                                     const int q = q4 * 2 + h;

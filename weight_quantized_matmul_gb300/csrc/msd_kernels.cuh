@@ -495,13 +495,13 @@ __global__ void __launch_bounds__(512) unfold_small_kernel(const __half *__restr
 // statically) from one K-group's TMEM columns d (column i * kMaxM + m holds 2^-9 sum_k A_i[m, k] u[k, n]):
 // y[m] += s_n (sum_i (512 c_i A_max) d_i - corr f_n), with corr = 8 sum_i c_i A_max S_i and f_n = 1 + zp / 8.
 template <int kMaxM, int R, int H, bool kZp>
-__device__ __forceinline__ void combine_rows(const uint32_t (&d)[3][16], const float4 *cg, float s_n, float f_n,
+__device__ __forceinline__ void combine_rows(const uint32_t (&d)[3][16], uint32_t cg, float s_n, float f_n,
                                              int rows_valid, float (&yacc)[R]) {
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) {
         const int m = H * R + rr;
         if (m < kMaxM && m < rows_valid) {
-            const float4 c = cg[2 * m];
+            const float4 c = lds_f128(cg + 32 * m);       // the row's record: one address for the warp
             const float d1 = __uint_as_float(d[m >> 4][m & 15]);
             const float d2 = __uint_as_float(d[(kMaxM + m) >> 4][(kMaxM + m) & 15]);
             const float d3 = __uint_as_float(d[(2 * kMaxM + m) >> 4][(2 * kMaxM + m) & 15]);
@@ -515,13 +515,13 @@ __device__ __forceinline__ void combine_rows(const uint32_t (&d)[3][16], const f
 
 // Debug: the integer partials Y_i = 512 d_i - 8 S_i of the same rows for group dbg_group.
 template <int kMaxM, int R, int H>
-__device__ __forceinline__ void debug_rows(const uint32_t (&d)[3][16], const float4 *cg, int rows_valid, int32_t *dbg,
+__device__ __forceinline__ void debug_rows(const uint32_t (&d)[3][16], uint32_t cg, int rows_valid, int32_t *dbg,
                                            int M, int N, int m0, int n) {
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) {
         const int m = H * R + rr;
         if (m < kMaxM && m < rows_valid) {
-            const float4 sv = cg[2 * m + 1];
+            const float4 sv = lds_f128(cg + 32 * m + 16);
             const float sp[3] = {sv.x, sv.y, sv.z};
 #pragma unroll
             for (int pl = 0; pl < 3; ++pl) {
@@ -767,17 +767,19 @@ __global__ void __launch_bounds__(kThreads, 2)
             // the stage landed before its tile was converted; seen here too, for the constants and scales
             if (ok) ok = mbar_wait_warp(full_p(s), (i / P) & 1, abort_flag, kSiteEpiOperandsEmpty);
             const uint8_t *stage = p_ring + s * L.stage_bytes;
-            const float4 *cs = reinterpret_cast<const float4 *>(stage + L.c_off);
-            const __half *ss = reinterpret_cast<const __half *>(stage + L.s_off);
-            const __half *zs = reinterpret_cast<const __half *>(stage + L.z_off);
+            const uint32_t cs = smem_addr(stage + L.c_off);
+            const uint32_t ss = smem_addr(stage + L.s_off), zs = smem_addr(stage + L.z_off);
             const int kb = kb0 + i;
             const int ng = groups_in(kb);
             for (int gg = 0; gg < ng; ++gg, ++j) {
                 const int b = j % kTmemBufs;
                 const bool live = ok;
-                const float s_n = debug || !live ? 0.0f : __half2float(ss[gg * kTileN + n_local]);
+                const float s_n =
+                    debug || !live ? 0.0f : __half2float(__ushort_as_half(lds_u16(ss + 2 * (gg * kTileN + n_local))));
                 const float f_n =
-                    kZp && !debug && live ? fmaf(__half2float(zs[gg * kTileN + n_local]), 0.125f, 1.0f) : 1.0f;
+                    kZp && !debug && live
+                        ? fmaf(__half2float(__ushort_as_half(lds_u16(zs + 2 * (gg * kTileN + n_local)))), 0.125f, 1.0f)
+                        : 1.0f;
                 if (!mbar_wait_warp(full_t(b), (j / kTmemBufs) & 1, abort_flag, kSiteEpiTmemFull)) {
                     ok = false;
                     bool drained = true;
@@ -803,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_t(b));
-                const float4 *cg = cs + gg * (kConstFloatsPerGroup / 4);
+                const uint32_t cg = cs + 4 * gg * kConstFloatsPerGroup;
                 if (debug) {
                     if (kb * gpk + gg == p.dbg_group && n < N)
                         debug_rows<kMaxM, R, 0>(d, cg, rows_valid, p.dbg_y123, M, N, m0, n);

@@ -191,6 +191,22 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
     return v;
 }
 
+// ------------------------------------------------------------------------------------------------ shared loads
+
+// Loads from shared memory by a 32-bit shared-window address. Dynamic shared memory reached through an aligned
+// generic pointer would otherwise be read with generic loads, which take the slower generic path.
+__device__ __forceinline__ float4 lds_f128(uint32_t saddr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(saddr));
+    return v;
+}
+
+__device__ __forceinline__ uint16_t lds_u16(uint32_t saddr) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(saddr));
+    return v;
+}
+
 // ------------------------------------------------------------------------------------------------ bulk copies
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
