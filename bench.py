@@ -11,7 +11,8 @@ for M <= 16, int8-equivalent TOPS (6 M N K per step / step time) above.
 
 Timing: W warm-up steps, then a short sustained phase (not timed, keeps the clocks representative and gives the
 clock sampler something to see), then exactly K timed steps between CUDA events on the launching stream, replayed
-from CUDA graphs; then K launches of the main kernel alone (wqbmm_run_part, part 2), the same way, for the roofline
+from CUDA graphs (a short device-side spin before the start event keeps the host's graph-launch latency out of the
+timed region); then K launches of the main kernel alone (wqbmm_run_part, part 2), the same way, for the roofline
 of the dominant kernel. Each step uses a different copy of the weights, scales and input (rotating copies whose total
 is more than twice the 126 MB L2), so every step streams its weights from HBM. The other workload shapes are timed
 the same way into a `workloads` record of the same line. The dense tensor-core peaks (E4M3, int8, bf16) are measured
@@ -44,6 +45,7 @@ from weight_quantized_matmul_gb300 import inputs as I  # noqa: E402
 
 DEFAULT_WORKLOAD = "decode_m1_k4096_n4096"
 L2_BYTES = 126 * 1024 * 1024
+HOLD_CYCLES = 200_000            # ~0.1 ms of device spin before each timed region
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -414,6 +416,9 @@ def measure(torch, wq, wl, args, dev, sampler, steps, sustain_s, variant, with_e
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
+            # a short spin on the device holds the stream while the host queues the graph replays, so that the start
+            # event is followed at once by the first step rather than by the host's launch latency
+            torch.cuda._sleep(HOLD_CYCLES)
             a.record(stream)
             for _ in range(full):
                 gfull.replay()
