@@ -24,7 +24,7 @@ constexpr int kGemvMaxRows = 2;
 constexpr int kGemvCols = 16;                       // output columns per CTA
 constexpr int kGemvWarps = 8;
 constexpr int kGemvThreads = kGemvWarps * 32;
-constexpr int kGemvKbPerPass = 8;                   // k-blocks per warp held in registers at a time
+constexpr int kGemvKbPerPass = 8;                   // k-blocks per warp held in registers at a time (at most)
 constexpr int kGemvPlaneBytes = 3 * kKBlock;        // one row, one k-block: [chunk 4][plane 3][32 bytes]
 constexpr float kDotUnitInv = 1.0f / 16.0f;          // the dot products come out as 16 sum_k A_i u
 
@@ -147,8 +147,13 @@ struct GemvSmem {
 
 // kZp: the quantized weight is w - zp[g, n], so a group's dots need (8 + zp) S_i taken off instead of 8 S_i: the
 // lane that applies the group's correction scales it by 1 + zp / 8.
-template <int MR, bool kDebug, bool kZp>
+// KB: k-blocks per warp and pass held in registers. 4 when every k-block fits in one pass of 32 (K <= 4096): the
+// kernel then holds half the weight registers it would with 8 (measured: the decode shape's kernel 3.37 -> 3.20 us);
+// 8 for longer K, which then takes fewer passes.
+template <int MR, bool kDebug, bool kZp, int KB>
 __global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvParams p) {
+    static_assert(KB == 4 || KB == kGemvKbPerPass, "4 or 8 k-blocks per warp and pass");
+    constexpr int kPassKb = kGemvWarps * KB;
     extern __shared__ __align__(128) uint8_t gemv_smem_raw[];
     GemvSmem<MR> &sm = *reinterpret_cast<GemvSmem<MR> *>(gemv_smem_raw);
     pdl_launch_dependents();
@@ -177,17 +182,17 @@ __global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvPar
     bool ok = true;
 
     int pass = 0;
-    for (int pb = 0; pb < kb_total; pb += kGemvPassKb, ++pass) {
-        const int pn = min(kGemvPassKb, kb_total - pb);
+    for (int pb = 0; pb < kb_total; pb += kPassKb, ++pass) {
+        const int pn = min(kPassKb, kb_total - pb);
         const int kw0 = pb + warp * pn / kGemvWarps, kw1 = pb + (warp + 1) * pn / kGemvWarps;
         const int nkb = kw1 - kw0;
         // weights and scales of the warp's k-blocks, all requested before any use (the scales stay fp16 until
         // they are used, so no instruction waits for them here)
-        uint4 wa[kGemvKbPerPass], wb[kGemvKbPerPass];
-        __half2 sab[kGemvKbPerPass];                   // scales of columns a and b
-        __half2 zab[kGemvKbPerPass];                   // zero points of columns a and b (first chunk lane of a group)
+        uint4 wa[KB], wb[KB];
+        __half2 sab[KB];                               // scales of columns a and b
+        __half2 zab[KB];                               // zero points of columns a and b (first chunk lane of a group)
 #pragma unroll
-        for (int j = 0; j < kGemvKbPerPass; ++j) {
+        for (int j = 0; j < KB; ++j) {
             if (j < nkb) {
                 const uint8_t *src = wbase + static_cast<size_t>(kw0 + j) * kPackedTileBytes;
                 wa[j] = ldg_stream16(src, policy);
@@ -210,7 +215,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvPar
         }
         if (!kDebug) {
 #pragma unroll
-            for (int j = 0; j < kGemvKbPerPass; ++j) {
+            for (int j = 0; j < KB; ++j) {
                 const int g = ((kw0 + j) * kKBlock + chunk * 32) >> gshift;
                 const bool in = j < nkb && g < Gn;
                 const size_t row_at = static_cast<size_t>(g) * p.group_stride + n_a;
@@ -226,7 +231,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) msd_gemv_kernel(const GemvPar
         ok = ok && mbar_wait_warp(bar, pass & 1, &sm.abort_flag, kSiteConvFull);
         if (ok) {
 #pragma unroll
-            for (int j = 0; j < kGemvKbPerPass; ++j) {
+            for (int j = 0; j < KB; ++j) {
                 if (j >= nkb) continue;                 // (not break: the loop stays fully unrolled)
                 const int kb = kw0 + j, kbl = kb - pb;
                 const int k0 = kb * kKBlock + chunk * 32;

@@ -391,9 +391,9 @@ wqbmm_status launch_large(const Shape &s, const Plan &plan, const Operands &op, 
 
 // Decode path: the unfold of the one or two rows, then the dp4a matrix-vector kernel, both under programmatic launch
 // (the GEMV kernel streams its weights while the unfold runs).
-template <int MR, bool kDebug, bool kZp>
+template <int MR, bool kDebug, bool kZp, int KB>
 bool gemv_smem_attr() {
-    return cudaFuncSetAttribute(msd_gemv_kernel<MR, kDebug, kZp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(msd_gemv_kernel<MR, kDebug, kZp, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(sizeof(GemvSmem<MR>))) == cudaSuccess;
 }
 
@@ -402,9 +402,11 @@ wqbmm_status launch_gemv(const Shape &s, const Plan &plan, const Operands &op, v
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         if (!info->gemv_smem_set) {
-            if (!gemv_smem_attr<1, false, false>() || !gemv_smem_attr<1, false, true>() ||
-                !gemv_smem_attr<1, true, false>() || !gemv_smem_attr<2, false, false>() ||
-                !gemv_smem_attr<2, false, true>() || !gemv_smem_attr<2, true, false>())
+            if (!gemv_smem_attr<1, false, false, 4>() || !gemv_smem_attr<1, false, true, 4>() ||
+                !gemv_smem_attr<2, false, false, 4>() || !gemv_smem_attr<2, false, true, 4>() ||
+                !gemv_smem_attr<1, false, false, 8>() || !gemv_smem_attr<1, false, true, 8>() ||
+                !gemv_smem_attr<1, true, false, 8>() || !gemv_smem_attr<2, false, false, 8>() ||
+                !gemv_smem_attr<2, false, true, 8>() || !gemv_smem_attr<2, true, false, 8>())
                 return WQBMM_ERR_CUDA;
             info->gemv_smem_set = true;
         }
@@ -451,15 +453,21 @@ wqbmm_status launch_gemv(const Shape &s, const Plan &plan, const Operands &op, v
         cfg.dynamicSmemBytes = smem;
         return cudaLaunchKernelEx(&cfg, kernel, gp);
     };
+    // four k-blocks per warp and pass when one pass of eight warps covers all of K, eight otherwise (debug: eight)
+    const bool one_pass = plan.kb_total <= kGemvWarps * 4;
     cudaError_t e;
     if (s.M == 1)
-        e = dbg  ? go(msd_gemv_kernel<1, true, false>, sizeof(GemvSmem<1>))
-            : zp ? go(msd_gemv_kernel<1, false, true>, sizeof(GemvSmem<1>))
-                 : go(msd_gemv_kernel<1, false, false>, sizeof(GemvSmem<1>));
+        e = dbg                 ? go(msd_gemv_kernel<1, true, false, 8>, sizeof(GemvSmem<1>))
+            : zp && one_pass    ? go(msd_gemv_kernel<1, false, true, 4>, sizeof(GemvSmem<1>))
+            : zp                ? go(msd_gemv_kernel<1, false, true, 8>, sizeof(GemvSmem<1>))
+            : one_pass          ? go(msd_gemv_kernel<1, false, false, 4>, sizeof(GemvSmem<1>))
+                                : go(msd_gemv_kernel<1, false, false, 8>, sizeof(GemvSmem<1>));
     else
-        e = dbg  ? go(msd_gemv_kernel<2, true, false>, sizeof(GemvSmem<2>))
-            : zp ? go(msd_gemv_kernel<2, false, true>, sizeof(GemvSmem<2>))
-                 : go(msd_gemv_kernel<2, false, false>, sizeof(GemvSmem<2>));
+        e = dbg                 ? go(msd_gemv_kernel<2, true, false, 8>, sizeof(GemvSmem<2>))
+            : zp && one_pass    ? go(msd_gemv_kernel<2, false, true, 4>, sizeof(GemvSmem<2>))
+            : zp                ? go(msd_gemv_kernel<2, false, true, 8>, sizeof(GemvSmem<2>))
+            : one_pass          ? go(msd_gemv_kernel<2, false, false, 4>, sizeof(GemvSmem<2>))
+                                : go(msd_gemv_kernel<2, false, false, 8>, sizeof(GemvSmem<2>));
     return e == cudaSuccess ? WQBMM_OK : WQBMM_ERR_CUDA;
 }
 
