@@ -351,6 +351,29 @@ def test_run_deterministic_and_workspace_left_clean(dev, wl):
         assert not counters.any()
 
 
+@pytest.mark.parametrize("M,K,N,G", [(1, 4096, 520, 128), (2, 2048, 1000, 64), (1, 1024, 5120, 128)])
+def test_calls_in_a_row_on_one_workspace(dev, M, K, N, G):
+    """Calls in a row on one workspace with different x and no synchronisation between them: each result is its own
+    x's, so a call's unfold pass never overwrites planes the previous call's GEMV kernel still reads, and a GEMV
+    kernel never reads planes an earlier call left in the workspace (decode with a ragged N tile, two rows with
+    G = 64, and an N with more CTAs than fit on the GPU at once)."""
+    wl = I.small_case(M, K, N, G, seed=M + K + N)
+    xa, wp, sc = I.make_inputs(wl)
+    xb = I.make_x(I.small_case(M, K, N, G, seed=M + K + N + 1, x_dist="t3_clip60"))
+    w_pre = wq.prepack_weight(to_dev(wp, dev), K, N, G)
+    sd = to_dev(sc, dev)
+    ws = wq.allocate_workspace(M, K, N, G, dev)
+    xs = [xa, xb, xa, xb]
+    ys = [torch.empty((M, N), dtype=torch.float16, device=dev) for _ in xs]
+    xds = [to_dev(x, dev) for x in xs]
+    for xd, y in zip(xds, ys):
+        wq.wqbmm_run(xd, w_pre, sd, y, M, K, N, G, ws)
+    torch.cuda.synchronize()
+    for i, (x, y) in enumerate(zip(xs, ys)):
+        T.assert_matches(y.cpu().numpy(), oracle.msd_matmul(x, wp, sc, G),
+                         oracle.msd_matmul(x, wp, sc, G, mode=oracle.MODE_F), f"call {i}")
+
+
 @pytest.mark.parametrize("wl", [I.small_case(1, 4096, 520, 128, seed=31),                   # decode
                                 I.small_case(3, 16384, 520, 64, seed=32),                   # split-K, workspace
                                 I.small_case(4, 4096, 1024, 128, seed=33),                  # split-K, cluster
