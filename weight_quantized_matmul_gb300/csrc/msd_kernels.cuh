@@ -15,14 +15,15 @@
 // of the row tile (NMMA = 16, 32 or 48 stacked rows), one MMA chain per K-group restarted at every group so the
 // integer partial sums stay exact in FP32. x is unfolded once by the pre-pass, not once per column tile. Roles
 // inside a CTA (320 threads):
-//   warp 0      TMA producer: per 128 k, bulk copies of the packed weight tile (8 KB), of the planes image and of
-//               the constants, and 2-D tensor copies of the scale (and zero-point) tile, into a ring of load stages
-//   warp 1      TMEM owner and single-thread MMA issuer (tcgen05.mma kind::f8f6f4, E4M3 x E4M3 -> F32); the planes
-//               are read in place in the load stage
-//   warps 2-9   workers: per k-block, int4 (offset binary) -> E4M3 for the weight tile (128-byte-swizzled K-major
-//               layout) into one of two operand slots, then the epilogue of the previous k-block: TMEM ->
-//               registers, Y_i = D_i - 8 S_i folded into the combine, scale, accumulate; the load stage is released
-//               after its epilogue (which has seen all of that k-block's MMAs complete)
+//   warp 0      TMA producer: per 128 k, a 2-D tensor copy of the packed weight tile (128 rows of 64 bytes, 64-byte
+//               swizzle), bulk copies of the planes image and of the constants, and 2-D tensor copies of the scale
+//               (and zero-point) tile, into a ring of load stages
+//   warp 1      TMEM owner and single-thread MMA issuer (tcgen05.mma kind::f8f6f4, E4M3 x E4M3 -> F32): A = the
+//               converted weights in tensor memory, B = the planes read in place in the load stage
+//   warps 2-5   converters: per k-block, each thread turns its weight column's 64 packed bytes (offset binary)
+//               into 128 E4M3 bytes in registers and stores them with tcgen05.st into one of two TMEM A slots
+//   warps 6-9   epilogue: per K-group, TMEM -> registers, Y_i = D_i - 8 S_i folded into the combine, scale,
+//               accumulate; the load stage is released once its constants and scales are read
 // Split-K (when there are too few column tiles to fill the GPU): up to 8 K-slices of a tile form a thread-block
 // cluster and reduce through distributed shared memory; more slices reduce through a global workspace. Either way
 // the slices are summed in slice order, so the result does not depend on timing.
@@ -42,8 +43,8 @@ namespace wqbmm {
 constexpr int kTileN = 128;                          // output columns per CTA (MMA M)
 constexpr int kKBlock = 128;                         // k per pipeline stage (one 128-byte E4M3 swizzle row)
 constexpr int kPackedTileBytes = kTileN * kKBlock / 2;  // 8192
-constexpr int kATileBytes = kTileN * kKBlock;        // 16384
-constexpr int kASlots = 2;                           // converted weight tiles in flight
+constexpr int kASlots = 2;                           // converted weight tiles (TMEM A operands) in flight
+constexpr int kACols = kKBlock / 4;                  // TMEM columns of one converted tile: 4 E4M3 bytes per column
 constexpr int kMaxTmemBufs = 8;                      // TMEM accumulators (one per K-group) in flight, at most
 constexpr int kSmemBudget = 110 * 1024;              // per CTA, so that two CTAs share an SM
 constexpr int kThreads = 320;
@@ -78,23 +79,38 @@ enum WaitSite : int {
     kSiteDebugWait = 9,
 };
 
+constexpr int kReduceNone = 0, kReduceCluster = 1, kReduceGlobal = 2;
+constexpr int kMaxClusterSplits = 8;
+
 template <int NMMA>
 struct Cfg {
     static_assert(NMMA == 16 || NMMA == 32 || NMMA == 48, "MMA N must be 16, 32 or 48");
     static constexpr int kMaxM = NMMA / 3;                         // rows of x per CTA (plane stride in B rows)
     static constexpr int kRowsPerWarp = kMaxM;                     // one epilogue warp per TMEM lane quarter
     static constexpr int kBufStride = NMMA <= 16 ? 16 : (NMMA <= 32 ? 32 : 64);   // TMEM columns per buffer
-    // eight buffers hold two k-blocks of the smallest groups; NMMA = 48 keeps four, so that two CTAs fit in TMEM
-    static constexpr int kTmemBufs = NMMA <= 32 ? 8 : 4;
-    static constexpr int kTmemCols = kTmemBufs * kBufStride;
+    // the accumulators and the two converted-weight slots share 256 columns, so that two CTAs fit in TMEM: eight
+    // buffers of 16 columns, six of 32, three of 64 (at least 1.5 k-blocks of the smallest groups)
+    static constexpr int kTmemBufs = NMMA <= 16 ? 8 : (NMMA <= 32 ? 6 : 3);
+    static constexpr int kAColBase = kTmemBufs * kBufStride;      // first column of the converted-weight slots
+    static constexpr int kTmemCols = 256;
+    static_assert(kAColBase + kASlots * kACols <= kTmemCols, "TMEM columns");
     static constexpr int kBTileBytes = NMMA * kKBlock;             // planes image of one k-block
-    // fixed part of the shared memory (offsets from a 1024-byte aligned base): the converted-weight slots
-    static constexpr int kOffA = 0;
-    static constexpr int kOffStages = kOffA + kASlots * kATileBytes;
+    // fixed part of the shared memory (offsets from a 1024-byte aligned base): the cluster reduction's partial sums,
+    // [splits][rows owned][128 columns] floats, whatever the cluster size (2..8)
+    static constexpr int red_rows() {
+        int most = 0;
+        for (int sl = 2; sl <= kMaxClusterSplits; ++sl) {
+            const int r = sl * ((kMaxM + sl - 1) / sl);
+            most = r > most ? r : most;
+        }
+        return most;
+    }
+    static constexpr int kOffRed = 0;
+    static constexpr int kOffStages = (kOffRed + red_rows() * kTileN * 4 + 1023) / 1024 * 1024;
 };
 
 // The load stages of the small-M kernel, sized by the groups per k-block (gpk = 128 / G) and by whether zero points
-// are staged: packed weights | planes image (NMMA x 128 B, the MMA's B operand, 1024-aligned) | constants (gpk x 16
+// are staged: packed weights (128 rows of 64 bytes, 64-byte swizzle) | planes image (NMMA x 128 B, the MMA's B operand, 1024-aligned) | constants (gpk x 16
 // rows x 8 floats) | scale tile (gpk x 128 n, fp16) [| zero-point tile]. As many stages as fit in the budget that
 // keeps two CTAs per SM (at least 3, at most 8), then the barriers and a few flags.
 struct SmallLayout {
@@ -132,8 +148,6 @@ struct RunParams {
     int dbg_group;              // -1 in normal runs
 };
 
-constexpr int kReduceNone = 0, kReduceCluster = 1, kReduceGlobal = 2;
-constexpr int kMaxClusterSplits = 8;
 
 // ------------------------------------------------------------------------------------------------ unfold
 
@@ -210,23 +224,6 @@ constexpr float kMmaUnit = 512.0f;     // 2^9: one MMA unit of the weight operan
 
 __device__ __forceinline__ uint4 expand_nibbles16(uint2 v) {
     return make_uint4(v.x & 0x0F0F0F0Fu, (v.x >> 4) & 0x0F0F0F0Fu, v.y & 0x0F0F0F0Fu, (v.y >> 4) & 0x0F0F0F0Fu);
-}
-
-// Weight bytes of one packed 128 x 128 tile by 256 threads: thread t takes the 16-byte pieces t and t + 256 (32 k of
-// weight row piece / 4 each) and writes their 32 E4M3 bytes as two 16-byte chunks of the 128-byte-swizzled K-major
-// operand tile. Both pieces are read before anything is written.
-__device__ __forceinline__ void convert_tile256(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int t) {
-    uint4 v[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) v[j] = *reinterpret_cast<const uint4 *>(src + (t + 256 * j) * 16);
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int piece = t + 256 * j, row = piece >> 2, ch = (piece & 3) * 2;
-        uint8_t *base = dst + (row >> 3) * 1024 + (row & 7) * 128;
-        *reinterpret_cast<uint4 *>(base + ((ch ^ (row & 7)) << 4)) = expand_nibbles16(make_uint2(v[j].x, v[j].y));
-        *reinterpret_cast<uint4 *>(base + (((ch + 1) ^ (row & 7)) << 4)) =
-            expand_nibbles16(make_uint2(v[j].z, v[j].w));
-    }
 }
 
 // The same for a whole tile by NT threads (NT divides 1024): chunks q = t, t + NT, ... All of a thread's packed
@@ -546,7 +543,7 @@ __device__ __forceinline__ void debug_rows(const uint32_t (&d)[3][16], uint32_t 
 // synchronisation (arrivals on the named barrier, waits for the MMAs' commits), so nothing can wait forever.
 template <int NMMA, bool kZp>
 __global__ void __launch_bounds__(kThreads, 2)
-    msd_kernel(const RunParams p, const __grid_constant__ CUtensorMap tmap_s,
+    msd_kernel(const RunParams p, const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
                const __grid_constant__ CUtensorMap tmap_z) {
     using C = Cfg<NMMA>;
     constexpr int kMaxM = C::kMaxM;
@@ -555,13 +552,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int P = L.p_stages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *a_ring = smem + C::kOffA;
+    float *red_buf = reinterpret_cast<float *>(smem + C::kOffRed);
     uint8_t *p_ring = smem + C::kOffStages;
     const uint32_t bar0 = smem_addr(smem + L.off_bar);
     // barriers: full_p / empty_p  load stage landed / released (converters done with the weights, epilogue with the
     //                             constants and scales after the k-block's MMAs, which read the planes)
     //           full_t / empty_t  TMEM accumulator written by the MMAs / read by the epilogue
-    //           a_free            converted weight slot read by the MMAs (their commit)
+    //           a_free            converted weight slot (TMEM) read by the MMAs (their commit)
     // and the named barriers kOperandBarrier0 + c: converted weight slot c ready for k-block i (i % 2 == c). Before
     // the converters arrive there for k-block i they have seen a_free for k-block i - 2, committed after the MMA warp
     // passed that barrier for k-block i - 2, so no arrival can count towards an earlier phase.
@@ -594,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // One load stage: the k-block's packed weight tile, planes image, constants, scale tile and zero-point tile, all
     // counted on full_p(s).
-    const uint8_t *w_src = p.w + (static_cast<size_t>(nt) * p.kb_total + kb0) * kPackedTileBytes;
+    const int w_row0 = (nt * p.kb_total + kb0) * kTileN;     // first row of this CTA's weight tiles (64 bytes each)
     const int gshift = 31 - __clz(G);                  // G is 32, 64 or 128
     auto groups_in = [&](int kb) { return (min(K, (kb + 1) * kKBlock) - kb * kKBlock) >> gshift; };
     auto stage_tx = [&](int kb) {
@@ -608,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t dst = smem_addr(p_ring + s * L.stage_bytes);
         const int kb = kb0 + i;
         mbar_arrive_expect_tx(full_p(s), stage_tx(kb));
-        bulk_g2s(dst, w_src + static_cast<size_t>(i) * kPackedTileBytes, kPackedTileBytes, full_p(s), stream_policy);
+        tma_load_2d(dst, &tmap_w, 0, w_row0 + i * kTileN, full_p(s), stream_policy);
         if (!debug) tma_load_2d(dst + L.s_off, &tmap_s, nt * kTileN, kb * gpk, full_p(s), keep_policy);
         if (kZp && !debug) tma_load_2d(dst + L.z_off, &tmap_z, nt * kTileN, kb * gpk, full_p(s), keep_policy);
     };
@@ -623,7 +620,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // ---- set-up. Thread 0 lets the next kernel on the stream start launching, initialises the barriers and at once
     // starts the weight loads of the first ring's worth of k-blocks (the slots are free), so the memory latency
-    // overlaps the rest of the set-up and, under programmatic launch, the tail of the unfold pre-pass.
+    // overlaps the rest of the set-up and, under programmatic launch, the tail of the unfold pre-pass. The planes and
+    // constants of those k-blocks follow from the producer after the set-up barrier, so that no other role waits
+    // for their issue.
     const int first_loads = nkb < P ? nkb : P;
     uint64_t stream_policy = 0, keep_policy = 0;
     if (threadIdx.x == 0) {
@@ -643,8 +642,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         keep_policy = l2_policy_evict_last();       // planes, constants and scale tiles: shared by many CTAs
         pdl_launch_dependents();
         for (int i = 0; i < first_loads; ++i) issue_static(i, stream_policy, keep_policy);
-        pdl_wait();
-        for (int i = 0; i < first_loads; ++i) issue_dynamic(i, keep_policy);
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
@@ -658,6 +655,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == kProducerWarp) {
         // ================================================================ TMA producer
         if (lane == 0) {
+            pdl_wait();
+            for (int i = 0; i < first_loads; ++i) issue_dynamic(i, keep_policy);
             int issued = first_loads;
             for (; issued < nkb; ++issued) {
                 const int s = issued % P;
@@ -683,15 +682,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int ng = groups_in(kb0 + i);
             if (lane == 0) {
                 tc_fence_after_sync();
-                const uint32_t a_base = smem_addr(a_ring + c * kATileBytes);
+                const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(C::kAColBase + c * kACols);
                 const uint32_t b_base = smem_addr(p_ring + s * L.stage_bytes + L.b_off);
                 for (int gg = 0; gg < ng; ++gg) {
                     const int jj = j + gg, b = jj % kTmemBufs;
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * C::kBufStride);
                     for (int ks = 0; ks < G / 32; ++ks) {
                         const uint32_t kofs = static_cast<uint32_t>(gg * G + ks * 32);
-                        umma_f8f6f4(d_tmem, sdesc_kmajor_sw128(a_base + kofs), sdesc_kmajor_sw128(b_base + kofs),
-                                    idesc, ks > 0 ? 1u : 0u);
+                        umma_f8f6f4_ta(d_tmem, a_tmem + kofs / 4, sdesc_kmajor_sw128(b_base + kofs), idesc,
+                                       ks > 0 ? 1u : 0u);
                     }
                     umma_commit(full_t(b));
                     last_j[b] = jj;
@@ -709,8 +708,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         __syncwarp();
     } else if (warp < kEpiWarp0) {
-        // ================================================================ converters
-        const int ct = threadIdx.x - kConvWarp0 * 32;    // 0..127
+        // ================================================================ converters: weights -> TMEM (A operand)
+        const int n_local = (warp & 3) * 32 + lane;      // this thread's weight column = its TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t swz = static_cast<uint32_t>((n_local >> 1) & 3);   // the tile's 64-byte swizzle
         bool ok = true;
         int j = 0;                                       // CTA-local group counter
         for (int i = 0; i < nkb; ++i) {
@@ -726,9 +727,28 @@ __global__ void __launch_bounds__(kThreads, 2)
                 (void)__shfl_sync(0xffffffffu, drained ? 1 : 0, 0);
             }
             if (ok) {
-                convert_tile<kConvThreads>(p_ring + s * L.stage_bytes, a_ring + c * kATileBytes, ct);
-                fence_proxy_async_smem();
+                tc_fence_after_sync();                   // the slot's last MMAs (a_free) before these stores
+                // the column's 64 packed bytes: word q holds k = 8q .. 8q+3 in its low nibbles and 8q+4 .. 8q+7 in
+                // its high nibbles, each u = w + 8; one mask (and one shift) gives four E4M3 bytes in k order, one
+                // TMEM column
+                const uint32_t row = smem_addr(p_ring + s * L.stage_bytes) + static_cast<uint32_t>(n_local * 64);
+                uint4 v[4];
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) v[ch] = lds_u128(row + 16u * (static_cast<uint32_t>(ch) ^ swz));
+                uint32_t e[32];
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    const uint32_t w4[4] = {v[ch].x, v[ch].y, v[ch].z, v[ch].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        e[2 * (4 * ch + q)] = w4[q] & 0x0F0F0F0Fu;
+                        e[2 * (4 * ch + q) + 1] = (w4[q] >> 4) & 0x0F0F0F0Fu;
+                    }
+                }
+                tmem_st32(tmem_base + lane_off + static_cast<uint32_t>(C::kAColBase + c * kACols), e);
+                tmem_wait_st();
             }
+            tc_fence_before_sync();
             // the TMEM buffers of this k-block's groups must have been read by the epilogue (their previous groups)
             // before the MMA warp issues into them; that gates the MMAs, not the expansion, so one converter warp
             // checks it after its expansion, while the others finish theirs
@@ -832,13 +852,18 @@ __global__ void __launch_bounds__(kThreads, 2)
                             __float2half_rn(p.bias != nullptr ? yacc[r] + bias_n : yacc[r]);
                 }
             } else if (p.reduce == kReduceCluster) {
-                // this slice's partial sums go to shared memory (the converted-weight slots are idle by now); the
-                // cluster reduces them after the cluster barrier below
-                float *red = reinterpret_cast<float *>(a_ring);
+                // row m is finished by CTA m % S of the cluster: this slice stores its partial sum of the row
+                // straight into that CTA's shared memory, [slice][m / S][column], summed there after the cluster
+                // barrier below
+                const int S = p.splits, owned = (kMaxM + S - 1) / S;
+                const uint32_t red = smem_addr(red_buf);
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     const int m = r;
-                    if (m < kMaxM) red[m * kTileN + n_local] = yacc[r];
+                    if (m < rows_valid) {
+                        const uint32_t off = static_cast<uint32_t>(((sp * owned + m / S) * kTileN + n_local) * 4);
+                        st_cluster_f32(cluster_map(red + off, static_cast<uint32_t>(m % S)), yacc[r]);
+                    }
                 }
             } else {
                 float *part = p.ws_part + static_cast<size_t>(sp) * M * N;
@@ -878,29 +903,23 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     if (p.reduce == kReduceCluster && !debug) {
-        // every thread of every CTA of the cluster takes part in both barriers (warps reconverged first)
+        // every thread of every CTA of the cluster takes part in the barrier (warps reconverged first); after it no
+        // CTA touches another's shared memory, so none has to stay for its peers
         __syncwarp();
-        cluster_sync_all();                                      // all partial sums are in shared memory
+        cluster_sync_all();                                      // all partial sums are in their owners' memory
         if (warp >= kEpiWarp0) {
             const int n_local = (warp & 3) * 32 + lane;
             const int n = nt * kTileN + n_local;
             const int rows_valid = min(p.m_sub, M - m0);
-            const uint32_t red = smem_addr(a_ring);
-            // CTA r of the cluster finishes rows r, r + S, ...; every row sums the slices in slice order
-            for (int m = static_cast<int>(cluster_ctarank()); m < rows_valid && n < N; m += p.splits) {
-                float v[kMaxClusterSplits];
-                const uint32_t off = static_cast<uint32_t>((m * kTileN + n_local) * 4);
-#pragma unroll
-                for (int q = 0; q < kMaxClusterSplits; ++q)
-                    v[q] = q < p.splits ? ld_cluster_f32(cluster_map(red + off, static_cast<uint32_t>(q))) : 0.0f;
+            const int S = p.splits, owned = (kMaxM + S - 1) / S;
+            // CTA sp of the cluster finishes rows sp, sp + S, ...; every row sums the slices in slice order
+            for (int mi = 0; mi * S + sp < rows_valid && n < N; ++mi) {
                 float acc = 0.0f;
-#pragma unroll
-                for (int q = 0; q < kMaxClusterSplits; ++q) acc += v[q];
+                for (int q = 0; q < S; ++q) acc += red_buf[(q * owned + mi) * kTileN + n_local];
                 if (p.bias != nullptr) acc += __half2float(p.bias[n]);
-                p.y[static_cast<size_t>(m0 + m) * N + n] = __float2half_rn(acc);
+                p.y[static_cast<size_t>(m0 + mi * S + sp) * N + n] = __float2half_rn(acc);
             }
         }
-        cluster_sync_all();                                      // peers' shared memory stays alive until read
     }
 
     __syncthreads();

@@ -117,7 +117,10 @@ Plan make_plan(const Shape &s, int sms) {
         p.reduce = kReduceNone;
         return p;
     }
-    p.m_tiles = static_cast<int>(ceil_div(s.M, 16));
+    // tiles of up to 16 rows (MMA N = 48); with G = 32 (four groups per k-block) at most 10 rows (N = 32), since
+    // three 48-row accumulators are all that fit beside the converted weights in a CTA's 256 TMEM columns
+    const int64_t max_rows = s.G == 32 ? 10 : 16;
+    p.m_tiles = static_cast<int>(ceil_div(s.M, max_rows));
     p.m_sub = static_cast<int>(ceil_div(s.M, p.m_tiles));
     p.nmma = p.m_sub <= 5 ? 16 : (p.m_sub <= 10 ? 32 : 48);
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
@@ -208,6 +211,20 @@ bool fp16_tensor_map(CUtensorMap *map, const void *base, int64_t rows, int64_t c
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Byte matrix of `rows` rows of `row_bytes` bytes (a multiple of 16, at most 64), boxes of box_rows whole rows,
+// stored in shared memory with the 64-byte swizzle (16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3)).
+bool u8_rows_tensor_map(CUtensorMap *map, const void *base, int64_t rows, int row_bytes, int box_rows) {
+    const EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(row_bytes), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t elem[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, elem,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Current device must be compute capability 10.3; caches the SM count.
 wqbmm_status current_device(int *dev_out, DeviceInfo **info_out) {
     int dev = 0;
@@ -235,6 +252,8 @@ template <int NMMA, bool kZp>
 wqbmm_status launch_msd(const RunParams &rp, const Plan &plan, DeviceInfo *info, cudaStream_t stream) {
     constexpr int idx = (kZp ? 3 : 0) + NMMA / 16 - 1;
     using C = Cfg<NMMA>;
+    // the converters check every TMEM accumulator of a k-block before its MMAs: they must all exist at once
+    if (kKBlock / rp.G > C::kTmemBufs) return WQBMM_ERR_INVALID;
     const int smem = SmallLayout(C::kBTileBytes, C::kOffStages, rp.G, kZp).smem_bytes;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
@@ -251,8 +270,12 @@ wqbmm_status launch_msd(const RunParams &rp, const Plan &plan, DeviceInfo *info,
             info->smem_set[idx] = true;
         }
     }
-    // scale and zero-point tiles: (128 / G) groups x 128 columns
-    CUtensorMap tmap_s{}, tmap_z{};
+    // weight tiles: 128 rows of 64 packed bytes per k-block, swizzled in shared memory; scale and zero-point tiles:
+    // (128 / G) groups x 128 columns
+    CUtensorMap tmap_w{}, tmap_s{}, tmap_z{};
+    if (!u8_rows_tensor_map(&tmap_w, rp.w, static_cast<int64_t>(plan.n_tiles) * plan.kb_total * kTileN,
+                            kKBlock / 2, kTileN))
+        return WQBMM_ERR_CUDA;
     if (rp.dbg_group < 0 && !fp16_tensor_map(&tmap_s, rp.scale, rp.K / rp.G, rp.N, kKBlock / rp.G, kTileN))
         return WQBMM_ERR_CUDA;
     if (kZp && rp.dbg_group < 0 && !fp16_tensor_map(&tmap_z, rp.zp, rp.K / rp.G, rp.N, kKBlock / rp.G, kTileN))
@@ -273,7 +296,7 @@ wqbmm_status launch_msd(const RunParams &rp, const Plan &plan, DeviceInfo *info,
     attr[1].val.clusterDim.z = static_cast<unsigned>(plan.splits);
     cfg.attrs = attr;
     cfg.numAttrs = rp.reduce == kReduceCluster ? 2 : 1;
-    if (cudaLaunchKernelEx(&cfg, msd_kernel<NMMA, kZp>, rp, tmap_s, tmap_z) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, msd_kernel<NMMA, kZp>, rp, tmap_w, tmap_s, tmap_z) != cudaSuccess)
         return WQBMM_ERR_CUDA;
     return WQBMM_OK;
 }
