@@ -102,7 +102,8 @@ WQBMM_API wqbmm_status wqbmm_prepack_weight_nk(const uint8_t *w_packed_nk, void 
  * Every shape needs one: x is unfolded once per call into it. For M <= 2 it holds the planes of x as int8 (3 bytes
  * per element, K padded to a multiple of 128) and, per row and group, four floats of combine constants; for
  * 3 <= M < 64 the planes as the tensor cores' operand image (16, 32 or 48 rows of 128 bytes per row tile of up to 16
- * rows and per 128 k) and 128 floats of constants per row tile and group, then split-K partial sums and per-tile
+ * rows, up to 10 when G = 32, and per 128 k) and 128 floats of constants per row tile and group, then split-K
+ * partial sums and per-tile
  * arrival counters (only shapes whose split over K is wider than one thread-block cluster need those); for M >= 64
  * the planes (3 bytes per element of x, rows padded to a multiple of 128) and the constants. Per channel it also
  * holds each row's A_max and, for M >= 3, the scale and zero-point rows repeated once per 128 k (or 64 or 32 when K

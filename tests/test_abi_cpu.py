@@ -69,6 +69,10 @@ def test_workspace_bytes():
     # 16, 32 or 48 rows x 128 bytes per row tile and k-block) plus 8 x 16 floats of constants per group. 8 column
     # tiles of 16 rows split over K into 8 slices that reduce inside a thread-block cluster need nothing more
     assert wq.wqbmm_workspace_bytes(16, 1024, 1024, 128) == 8 * 48 * 128 + 8 * 512
+    # G = 32 (four groups per k-block): row tiles of at most 10 rows, so 16 rows are two tiles of 8 (MMA N = 32);
+    # with G = 64 one tile of 16 (N = 48)
+    assert wq.wqbmm_workspace_bytes(16, 1024, 1024, 32) == 2 * 8 * 32 * 128 + 2 * 32 * 512
+    assert wq.wqbmm_workspace_bytes(16, 1024, 1024, 64) == 8 * 48 * 128 + 16 * 512
     # two column tiles and a long K: 160 slices (sized for up to 160 SMs, two CTAs each) reduce through the
     # workspace: 160 x 3 x 256 fp32 partial sums + one 256-byte block of counters after the unfolded x
     assert wq.wqbmm_workspace_bytes(3, 65536, 256, 128) == 512 * 16 * 128 + 512 * 512 + 160 * 3 * 256 * 4 + 256
